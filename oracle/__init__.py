@@ -1,0 +1,177 @@
+"""CPU oracle for the W4A16 group-128 linear layer -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``w4a16_oracle.c`` (plain C, compiled with gcc, OpenMP
+over output columns).  This module only compiles it and marshals numpy arrays
+through ctypes.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it; the library under
+``weight_only_int4_gemm_gb300`` never does, and the two share no code.
+
+Sources, by page title and section:
+  * "Give Me BF16 or Give Me Death" (summary), "W4A16-INT Quantization":
+    group-128 scales along K; dequantise-then-multiply inference.
+  * "When quantization pays -- and when it does not", "Counting c from the
+    kernel, not from intuition": uint4 codes with bias 8, exact (q - 8) first,
+    then one bf16 multiply by the group scale.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(exhaustive nearest-bf16 check, integer special cases, exact-rational brute
+force, invariants, hand-built unpack cases, the 4.125-bit accounting).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+GROUP = 128
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc, -O2, OpenMP)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int)
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_code.argtypes = [u32p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_code.restype = ctypes.c_int
+        lib.oracle_zero.argtypes = [u32p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_zero.restype = ctypes.c_int
+        lib.oracle_dequant_one.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint16]
+        lib.oracle_dequant_one.restype = ctypes.c_uint16
+        lib.oracle_dequant.argtypes = [u32p, u16p, u32p, ctypes.c_int, ctypes.c_int, u16p]
+        lib.oracle_dequant.restype = None
+        lib.oracle_gemm_cols.argtypes = [u16p, u32p, u16p, u32p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
+        lib.oracle_gemm_cols.restype = None
+        lib.oracle_format_bits_per_weight.argtypes = [ctypes.c_longlong, ctypes.c_longlong,
+                                                      ctypes.c_int]
+        lib.oracle_format_bits_per_weight.restype = ctypes.c_double
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return ctypes.cast(None, ctypes.POINTER(ctype))
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _as_u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype in (np.uint16, np.int16), a.dtype
+    return a.view(np.uint16)
+
+
+def _as_u32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype in (np.uint32, np.int32), a.dtype
+    return a.view(np.uint32)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().oracle_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def bf16_from_double(v: float) -> int:
+    return int(_load().oracle_bf16_from_double(float(v)))
+
+
+def code(qweight: np.ndarray, k: int, n: int) -> int:
+    q = _as_u32(qweight)
+    return _load().oracle_code(_ptr(q, ctypes.c_uint32), q.shape[1], k, n)
+
+
+def zero(qzeros: np.ndarray | None, N: int, g: int, n: int) -> int:
+    z = None if qzeros is None else _as_u32(qzeros)
+    return _load().oracle_zero(_ptr(z, ctypes.c_uint32), N, g, n)
+
+
+def dequant_one(q: int, z: int, scale_bits: int) -> int:
+    return int(_load().oracle_dequant_one(int(q), int(z), int(scale_bits) & 0xFFFF))
+
+
+def dequant(qweight, scales, qzeros=None) -> np.ndarray:
+    """W[K][N] as bf16 bit patterns (uint16)."""
+    q = _as_u32(qweight)
+    s = _as_u16(scales)
+    z = None if qzeros is None else _as_u32(qzeros)
+    K = q.shape[0] * 8
+    N = q.shape[1]
+    assert s.shape == (K // GROUP, N)
+    if z is not None:
+        assert z.shape == (K // GROUP, N // 8)
+    out = np.empty((K, N), dtype=np.uint16)
+    _load().oracle_dequant(_ptr(q, ctypes.c_uint32), _ptr(s, ctypes.c_uint16),
+                           _ptr(z, ctypes.c_uint32), K, N, _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def gemm(x, qweight, scales, qzeros=None, cols=None):
+    """Reference GEMM on the listed output columns (all when ``cols`` is None).
+
+    Returns ``(y_bits uint16 [B][ncols], acc float64 [B][ncols],
+    bound float64 [B][ncols])``.
+    """
+    xb = _as_u16(x)
+    q = _as_u32(qweight)
+    s = _as_u16(scales)
+    z = None if qzeros is None else _as_u32(qzeros)
+    B, K = xb.shape
+    N = q.shape[1]
+    assert q.shape[0] * 8 == K
+    assert s.shape == (K // GROUP, N)
+    if z is not None:
+        assert z.shape == (K // GROUP, N // 8)
+    c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, dtype=np.int32)
+    nc = int(c.shape[0])
+    y = np.empty((B, nc), dtype=np.uint16)
+    acc = np.empty((B, nc), dtype=np.float64)
+    bound = np.empty((B, nc), dtype=np.float64)
+    _load().oracle_gemm_cols(_ptr(xb, ctypes.c_uint16), _ptr(q, ctypes.c_uint32),
+                             _ptr(s, ctypes.c_uint16), _ptr(z, ctypes.c_uint32),
+                             B, K, N, _ptr(c, ctypes.c_int), nc,
+                             _ptr(y, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
+                             _ptr(bound, ctypes.c_double))
+    return y, acc, bound
+
+
+def format_bits_per_weight(K: int, N: int, has_zeros: bool) -> float:
+    return float(_load().oracle_format_bits_per_weight(K, N, 1 if has_zeros else 0))
+
+
+def omp_threads() -> int:
+    """Threads the oracle's OpenMP loops use (OMP_NUM_THREADS, else all cores)."""
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.isdigit():
+        return int(env)
+    return os.cpu_count() or 1

@@ -1,0 +1,79 @@
+"""Seeded synthetic inputs for the W4A16 linear layer.
+
+This module only draws random numbers; it holds none of the layer's
+arithmetic (no unpacking, dequantisation or products), so the CPU oracle and
+the CUDA library can both be fed from it without sharing any of the method.
+
+Recipe (shapes and value distributions of the workloads):
+  * codes    -- canonical ``qweight`` uint32 [K/8][N]: uniform random 32-bit
+                words, i.e. eight independent uniform codes 0..15 per word;
+  * scales   -- bf16 [K/128][N]: |N(0, 1)| * 0.02, rounded to bf16;
+  * zeros    -- canonical ``qzeros`` uint32 [K/128][N/8]: uniform random
+                words, i.e. uniform zero-points 0..15 (asymmetric variant);
+  * x        -- bf16 [B][K]: N(0, 1) rounded to bf16; with ``outlier_frac``,
+                round(outlier_frac * K) input channels picked without
+                replacement are multiplied by 20 before the rounding.
+
+Draws use ``torch.Generator(device).manual_seed(seed)``; CPU and CUDA
+generators give different streams, so each comparison uses one generated copy
+(moved between devices as needed), never two independent draws.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+GROUP = 128
+
+
+@dataclass
+class LinearProblem:
+    x: torch.Tensor          # bf16 [B][K]
+    qweight: torch.Tensor    # int32 [K/8][N]   (bit pattern of uint32 words)
+    scales: torch.Tensor     # bf16 [K/128][N]
+    qzeros: torch.Tensor | None  # int32 [K/128][N/8] or None (symmetric)
+
+    @property
+    def shape(self):
+        B, K = self.x.shape
+        return B, K, self.qweight.shape[1]
+
+    def to(self, device) -> "LinearProblem":
+        return LinearProblem(
+            self.x.to(device), self.qweight.to(device), self.scales.to(device),
+            None if self.qzeros is None else self.qzeros.to(device))
+
+
+def random_words(shape, gen: torch.Generator, device) -> torch.Tensor:
+    """Uniform random 32-bit words (int32 storage)."""
+    return torch.randint(-2**31, 2**31, shape, dtype=torch.int32, generator=gen, device=device)
+
+
+def make_weights(K: int, N: int, seed: int, *, zero_points: bool = False, device="cpu"):
+    """(qweight, scales, qzeros-or-None) for one K x N layer."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    qweight = random_words((K // 8, N), gen, device)
+    scales = (torch.randn((K // GROUP, N), generator=gen, device=device).abs_() * 0.02).to(torch.bfloat16)
+    qzeros = random_words((K // GROUP, N // 8), gen, device) if zero_points else None
+    return qweight, scales, qzeros
+
+
+def make_activations(B: int, K: int, seed: int, *, outlier_frac: float = 0.0, device="cpu"):
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    x = torch.randn((B, K), generator=gen, device=device)
+    n_out = int(round(outlier_frac * K))
+    if n_out > 0:
+        channels = torch.randperm(K, generator=gen, device=device)[:n_out]
+        x[:, channels] *= 20.0
+    return x.to(torch.bfloat16)
+
+
+def make_problem(B: int, K: int, N: int, seed: int, *, zero_points: bool = False,
+                 outlier_frac: float = 0.0, device="cpu") -> LinearProblem:
+    """One seeded layer: weights from ``seed``, activations from ``seed + 1``."""
+    qweight, scales, qzeros = make_weights(K, N, seed, zero_points=zero_points, device=device)
+    x = make_activations(B, K, seed + 1_000_003, outlier_frac=outlier_frac, device=device)
+    return LinearProblem(x, qweight, scales, qzeros)
