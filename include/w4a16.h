@@ -1,0 +1,149 @@
+/*
+ * w4a16.h -- C ABI of the W4A16 group-128 linear layer for GB300 (sm_103a).
+ *
+ *     y[B][N] = x[B][K] . dequant(Wq[K][N], S[K/128][N], Z?)
+ *
+ * with bf16 activations x, 4-bit weight codes q, one bf16 scale s per 128
+ * consecutive weights along K, and w = (q - z) * s rounded once to bf16,
+ * where z = 8 for the symmetric (GPTQ, "uint4 bias 8") format or a stored
+ * 4-bit zero-point per (group, column) for the asymmetric format.
+ *
+ * Sources, by page title and section:
+ *  - "Give Me BF16 or Give Me Death" (summary), section "W4A16-INT
+ *    Quantization", paragraphs "Group-wise quantization granularity" (one
+ *    16-bit scale per 128 consecutive weights along the input dimension) and
+ *    "Inference with W4A16" (weights rebuilt on the fly inside the matrix
+ *    multiplication, 16-bit tensor-core products, higher-precision
+ *    accumulation).
+ *  - "When quantization pays -- and when it does not", section "Counting c
+ *    from the kernel, not from intuition" (bias-8 unsigned codes decoded by
+ *    the bf16 magic number 128, exact subtraction of 136, then the group
+ *    scale), and the opening model of a decode step (memory pipe vs. math pipe).
+ *
+ * Conventions shared by every call:
+ *  - All buffer pointers are DEVICE pointers on the current CUDA device and
+ *    must be 16-byte aligned.  The caller owns every buffer; the library never
+ *    allocates device memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work and returns; it never
+ *    synchronises.
+ *  - Shapes are validated on the host before anything is enqueued: on any
+ *    error nothing is launched and a status is returned.  No C++ exception
+ *    crosses this boundary.  Inputs are never padded: K must be a multiple of
+ *    128 and N a multiple of 8.
+ *  - group_size must be 128 (the only group the format defines here).
+ *  - bf16 buffers are passed as void* and hold IEEE bfloat16 bit patterns.
+ *
+ * Data layouts:
+ *  - canonical codes   qweight uint32 [K/8][N]: nibble j (bits 4j..4j+3) of
+ *                      word [kk][n] is the code of row k = 8*kk + j, column n.
+ *  - canonical zeros   qzeros  uint32 [K/128][N/8]: nibble j of word [g][nn]
+ *                      is the zero-point of group g, column 8*nn + j.
+ *  - scales            bf16 [K/128][N], row-major.
+ *  - x                 bf16 [B][K], row-major (row stride K).
+ *  - y                 bf16 [B][N], row-major (row stride N).
+ *  - packed blob       opaque, w4a16_packed_bytes() bytes, written by
+ *                      w4a16_pack(); layout tag W4A16_PACKED_LAYOUT.
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_GROUP 128
+#define W4A16_PACKED_LAYOUT 1 /* version tag of the packed blob's layout */
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_NULL = 1,        /* a required pointer is NULL */
+    W4A16_ERR_SHAPE = 2,       /* B < 1, K % 128 != 0, N % 8 != 0, or sizes too large */
+    W4A16_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    W4A16_ERR_UNSUPPORTED = 4, /* group_size != 128, or an unknown path id */
+    W4A16_ERR_WORKSPACE = 5,   /* workspace smaller than w4a16_workspace_bytes() */
+    W4A16_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+    W4A16_ERR_TIMEOUT = 7      /* a device-side bounded wait ran out (see
+                                  w4a16_device_status) */
+} w4a16_status;
+
+/* Kernel paths the dispatcher chooses from (w4a16_select_path, forcing). */
+typedef enum {
+    W4A16_PATH_AUTO = -1,
+    W4A16_PATH_SKINNY = 0,  /* memory-bound small-batch split-K kernel */
+    W4A16_PATH_TCGEN05 = 1  /* compute-bound tcgen05/TMEM tensor-core kernel */
+} w4a16_path;
+
+/* Bytes of the packed blob for a K x N layer (codes, plus zero-points when
+ * has_zeros != 0): K*N/2 [+ (K/128)*(N/8)*4].  Returns 0 for invalid shapes. */
+size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros);
+
+/* Bytes of device workspace w4a16_gemm needs for this shape (0 if none).
+ * The workspace holds fp32 split-K partial sums and arrival counters.  It
+ * must be zero-filled once before its first use; every call leaves the
+ * counters at zero again, so it can be reused by later calls on the same
+ * stream.  Calls that run concurrently must use different workspaces.
+ * Returns (size_t)-1 for invalid shapes. */
+size_t w4a16_workspace_bytes(int B, int K, int N, int group_size);
+
+/* Offline repack ("Counting c from the kernel": the lop3 magic-number decode
+ * takes one nibble from each 16-bit half of a 32-bit word, so the codes of
+ * each pair of consecutive k are moved into the two halves of one word).
+ *   qweight  device, canonical codes uint32 [K/8][N]            (read)
+ *   qzeros   device, canonical zeros uint32 [K/128][N/8], or NULL for the
+ *            symmetric format                                   (read)
+ *   packed   device, w4a16_packed_bytes(K, N, 128, qzeros != NULL) bytes
+ *                                                               (written)
+ * Integer-only; the result is a pure permutation of the input nibbles. */
+w4a16_status w4a16_pack(const uint32_t *qweight, const uint32_t *qzeros, int K, int N,
+                        int group_size, void *packed, void *stream);
+
+/* y = x . dequant(packed, scales) with fp32 accumulation and one final
+ * round-to-nearest-even to bf16 ("Inference with W4A16").
+ *   x          device bf16 [B][K]                              (read)
+ *   packed     device blob from w4a16_pack                     (read)
+ *   scales     device bf16 [K/128][N]                          (read)
+ *   has_zeros  1 if the blob was packed with zero-points, else 0
+ *   y          device bf16 [B][N]                              (written)
+ *   workspace  device, >= w4a16_workspace_bytes(B, K, N, 128) bytes,
+ *              zero-filled before first use (may be NULL when that size is 0)
+ * The kernel path is chosen from (B, K, N) by w4a16_select_path. */
+w4a16_status w4a16_gemm(const void *x, const void *packed, const void *scales, int has_zeros,
+                        void *y, int B, int K, int N, int group_size,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+/* As w4a16_gemm, but with the kernel path forced (W4A16_PATH_*; AUTO = same
+ * as w4a16_gemm).  For tests and ablations; the result must agree with
+ * every other path within the GEMM error bound. */
+w4a16_status w4a16_gemm_path(const void *x, const void *packed, const void *scales, int has_zeros,
+                             void *y, int B, int K, int N, int group_size,
+                             void *workspace, size_t ws_bytes, int path, void *stream);
+
+/* Materialise the dequantised weights W[K][N] (bf16, row-major) from the
+ * packed blob with the same device decode routine the GEMM kernels use, so
+ * that every weight can be compared bit for bit with RNE_bf16((q - z) * s).
+ *   w  device bf16 [K][N] (written) */
+w4a16_status w4a16_dequant_ref(const void *packed, const void *scales, int has_zeros, void *w,
+                               int K, int N, int group_size, void *stream);
+
+/* Path w4a16_gemm would take for this shape on the current device
+ * (W4A16_PATH_*), or -1 for invalid shapes. */
+int w4a16_select_path(int B, int K, int N);
+
+/* Device-side status word of the tensor-core kernel: 0 when every bounded
+ * wait completed, else W4A16_ERR_TIMEOUT.  Synchronises the current device;
+ * clears the word when `clear` != 0.  Returns W4A16_ERR_CUDA if the query
+ * itself fails. */
+w4a16_status w4a16_device_status(int clear);
+
+/* Static description of a status code; never NULL. */
+const char *w4a16_status_string(w4a16_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

@@ -1,0 +1,109 @@
+"""The C-ABI library loads, exports every symbol the header declares, and its
+host-side validation returns the documented status without launching
+anything (these calls never reach a kernel, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_int4_gemm_gb300 as w
+from weight_only_int4_gemm_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_UNSUP, ERR_WS = 0, 1, 2, 3, 4, 5
+FAKE = 0x10000  # an aligned, never-dereferenced address
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _lib.load()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "w4a16_gemm" in names and "w4a16_pack" in names and "w4a16_dequant_ref" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with header"
+
+
+def test_packed_bytes():
+    assert w.w4a16_packed_bytes(4096, 4096, False) == 4096 * 4096 // 2
+    assert w.w4a16_packed_bytes(4096, 4096, True) == 4096 * 4096 // 2 + 32 * 512 * 4
+    lib = _lib.load()
+    assert lib.w4a16_packed_bytes(100, 4096, 128, 0) == 0
+    assert lib.w4a16_packed_bytes(128, 12, 128, 0) == 0
+    assert lib.w4a16_packed_bytes(128, 8, 64, 0) == 0
+
+
+def test_workspace_bytes_invalid_shapes(lib):
+    bad = ctypes.c_size_t(-1).value
+    assert lib.w4a16_workspace_bytes(0, 128, 8, 128) == bad
+    assert lib.w4a16_workspace_bytes(1, 130, 8, 128) == bad
+    assert lib.w4a16_workspace_bytes(1, 128, 9, 128) == bad
+    assert lib.w4a16_workspace_bytes(1, 128, 8, 32) == bad
+
+
+def _gemm(lib, x=FAKE, packed=FAKE, scales=FAKE, y=FAKE, B=1, K=128, N=8, group=128,
+          ws=None, ws_bytes=0, path=-1):
+    return lib.w4a16_gemm_path(x, packed, scales, 0, y, B, K, N, group, ws, ws_bytes, path, None)
+
+
+def test_gemm_validation(lib):
+    assert _gemm(lib, group=64) == ERR_UNSUP
+    assert _gemm(lib, K=100) == ERR_SHAPE
+    assert _gemm(lib, K=0) == ERR_SHAPE
+    assert _gemm(lib, N=12) == ERR_SHAPE
+    assert _gemm(lib, B=0) == ERR_SHAPE
+    assert _gemm(lib, B=-3) == ERR_SHAPE
+    assert _gemm(lib, x=None) == ERR_NULL
+    assert _gemm(lib, y=None) == ERR_NULL
+    assert _gemm(lib, x=FAKE + 8) == ERR_ALIGN
+    assert _gemm(lib, scales=FAKE + 2) == ERR_ALIGN
+    assert _gemm(lib, path=7) == ERR_UNSUP
+    # a shape that needs split-K workspace: missing / too small / misaligned
+    B, K, N = 1, 4096, 4096
+    need = lib.w4a16_workspace_bytes(B, K, N, 128)
+    assert need > 0
+    assert _gemm(lib, B=B, K=K, N=N, path=0) == ERR_NULL
+    assert _gemm(lib, B=B, K=K, N=N, ws=FAKE, ws_bytes=need - 1, path=0) == ERR_WS
+    assert _gemm(lib, B=B, K=K, N=N, ws=FAKE + 4, ws_bytes=need, path=0) == ERR_ALIGN
+
+
+def test_pack_and_dequant_validation(lib):
+    assert lib.w4a16_pack(FAKE, None, 128, 8, 64, FAKE, None) == ERR_UNSUP
+    assert lib.w4a16_pack(FAKE, None, 120, 8, 128, FAKE, None) == ERR_SHAPE
+    assert lib.w4a16_pack(None, None, 128, 8, 128, FAKE, None) == ERR_NULL
+    assert lib.w4a16_pack(FAKE, FAKE + 4, 128, 8, 128, FAKE, None) == ERR_ALIGN
+    assert lib.w4a16_dequant_ref(FAKE, FAKE, 0, None, 128, 8, 128, None) == ERR_NULL
+    assert lib.w4a16_dequant_ref(FAKE, FAKE, 0, FAKE, 128, 7, 128, None) == ERR_SHAPE
+    assert lib.w4a16_dequant_ref(FAKE + 1, FAKE, 0, FAKE, 128, 8, 128, None) == ERR_ALIGN
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.w4a16_status_string(s)
+    assert lib.w4a16_status_string(99) == b"unknown status"
+
+
+def test_select_path(lib):
+    assert lib.w4a16_select_path(1, 4096, 4096) == w.PATH_SKINNY
+    assert lib.w4a16_select_path(0, 4096, 4096) == -1
+    assert lib.w4a16_select_path(16, 100, 4096) == -1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load()

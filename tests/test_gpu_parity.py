@@ -1,0 +1,196 @@
+"""GPU parity: the CUDA library against the CPU oracle on identical seeded
+inputs, through the C ABI (via its Python binding).
+
+Bars: dequantised weights bit-exact; every GEMM output within
+|y_gpu - y_oracle| <= 8e-3 * sum_k |x_k * w_kn| + 1e-6.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_int4_gemm_gb300 as w
+from tests.bf16_exact import bits_to_f64
+from tests.gpu_util import assert_within_bound, bits, oracle_gemm, sample_columns
+from weight_only_int4_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+LAYER_SHAPES = {"qkv": (4096, 6144), "o_proj": (4096, 4096), "gate_up": (4096, 28672),
+                "down": (14336, 4096)}
+
+
+def available_paths():
+    paths = [w.PATH_SKINNY]
+    # the tensor-core path exists when the library reports it can select it
+    if w.w4a16_select_path(4096, 4096, 4096) == w.PATH_TCGEN05:
+        paths.append(w.PATH_TCGEN05)
+    return paths
+
+
+def run_gemm(p, path=w.PATH_AUTO):
+    g = p.to("cuda")
+    packed = w.w4a16_pack(g.qweight, g.qzeros)
+    y = w.w4a16_gemm(g.x, packed, g.scales, g.qzeros is not None, path=path)
+    torch.cuda.synchronize()
+    assert w.w4a16_device_status() == 0
+    return y.cpu()
+
+
+# ------------------------------------------------------------ dequant, bit-exact
+
+def _all_codes_by_all_scales():
+    N = 0x10000
+    qweight = np.full((16, N), 0x88888888, dtype=np.uint32)
+    qweight[0, :] = 0x76543210
+    qweight[1, :] = 0xFEDCBA98
+    scale_bits = np.arange(N, dtype=np.uint32).astype(np.uint16)
+    finite = np.isfinite(bits_to_f64(scale_bits))
+    scales = np.where(finite, scale_bits, 0).astype(np.uint16)[None, :]
+    return qweight, scales, finite
+
+
+def _gpu_dequant(qweight, scales, qzeros=None):
+    K = qweight.shape[0] * 8
+    qw = torch.from_numpy(qweight.view(np.int32)).cuda()
+    sc = torch.from_numpy(scales.view(np.int16)).view(torch.bfloat16).cuda()
+    qz = None if qzeros is None else torch.from_numpy(qzeros.view(np.int32)).cuda()
+    packed = w.w4a16_pack(qw, qz)
+    out = w.w4a16_dequant_ref(packed, sc, qz is not None, K)
+    torch.cuda.synchronize()
+    return bits(out)
+
+
+def test_dequant_exhaustive_symmetric_bit_exact():
+    qweight, scales, finite = _all_codes_by_all_scales()
+    got = _gpu_dequant(qweight, scales)
+    want = oracle.dequant(qweight, scales)
+    mism = (got != want)[:, finite]
+    assert not mism.any(), f"{int(mism.sum())} mismatching weights"
+
+
+def test_dequant_exhaustive_zero_points_bit_exact():
+    qweight, scales, finite = _all_codes_by_all_scales()
+    for z in range(16):
+        qzeros = np.full((1, 0x10000 // 8), z * 0x11111111, dtype=np.uint32)
+        got = _gpu_dequant(qweight, scales, qzeros)
+        want = oracle.dequant(qweight, scales, qzeros)
+        mism = (got != want)[:, finite]
+        assert not mism.any(), f"z={z}: {int(mism.sum())} mismatching weights"
+
+
+@pytest.mark.parametrize("zp", [False, True])
+@pytest.mark.parametrize("K,N", [(128, 8), (384, 264), (4096, 4104)])
+def test_dequant_random_layers_bit_exact(K, N, zp):
+    p = inputs.make_problem(1, K, N, seed=K + N, zero_points=zp)
+    qw, sc = bits(p.qweight), bits(p.scales)
+    qz = None if p.qzeros is None else bits(p.qzeros)
+    np.testing.assert_array_equal(_gpu_dequant(qw, sc, qz), oracle.dequant(qw, sc, qz))
+
+
+# ------------------------------------------------------------ GEMM, small shapes
+
+SMALL = [(1, 128, 8), (2, 256, 16), (3, 384, 24), (5, 128, 72), (8, 512, 64), (9, 256, 136),
+         (16, 1024, 200), (17, 384, 64), (33, 256, 40), (64, 512, 128), (100, 384, 264),
+         (257, 256, 136)]
+
+
+@pytest.mark.parametrize("zp", [False, True])
+@pytest.mark.parametrize("B,K,N", SMALL)
+def test_gemm_small_shapes_all_paths(B, K, N, zp):
+    p = inputs.make_problem(B, K, N, seed=B * 7 + K + N, zero_points=zp)
+    for path in [w.PATH_AUTO] + available_paths():
+        assert_within_bound(run_gemm(p, path), p)
+
+
+@pytest.mark.parametrize("zp", [False, True])
+@pytest.mark.parametrize("B,K,N", [(1, 4096, 4096), (16, 4096, 264), (40, 1024, 520), (300, 512, 392)])
+def test_gemm_integer_case_is_bit_exact(B, K, N, zp):
+    """Unit scales and integer x in [-4, 4]: every partial sum is an integer
+    below 2^24, so any fp32 accumulation order is exact and the GPU result
+    must equal the oracle's bit for bit."""
+    p = inputs.make_problem(B, K, N, seed=99, zero_points=zp)
+    gen = torch.Generator().manual_seed(5)
+    xi = torch.randint(-4, 5, (B, K), generator=gen).to(torch.bfloat16)
+    p = inputs.LinearProblem(xi, p.qweight, torch.ones_like(p.scales), p.qzeros)
+    y_o, acc, _ = oracle_gemm(p)
+    assert np.all(np.abs(acc) < 2 ** 24)
+    for path in available_paths():
+        np.testing.assert_array_equal(bits(run_gemm(p, path)), y_o, err_msg=f"path {path}")
+
+
+# ------------------------------------------------------------ workload-sized parity
+
+def test_single_linear_4096_b1_seed0_full():
+    """Single linear 4096 -> 4096 at B = 1, seed 0: every output."""
+    p = inputs.make_problem(1, 4096, 4096, seed=0)
+    assert_within_bound(run_gemm(p), p)
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
+def test_decoder_layer_linear_set_full(B):
+    """One Llama-3-8B decoder layer's four linears at decode: every output."""
+    for i, (name, (K, N)) in enumerate(LAYER_SHAPES.items()):
+        p = inputs.make_problem(B, K, N, seed=1000 + 10 * i)
+        assert_within_bound(run_gemm(p), p)
+
+
+@pytest.mark.parametrize("B", [1, 16, 64, 270, 1024])
+def test_lm_head_sampled_columns(B):
+    """4096 -> 128256 lm_head (largest N): sampled columns, all rows."""
+    p = inputs.make_problem(B, 4096, 128256, seed=77)
+    y = run_gemm(p)
+    assert_within_bound(y, p, cols=sample_columns(128256, 96 if B > 64 else 384))
+
+
+@pytest.mark.parametrize("name", ["qkv", "gate_up", "down"])
+def test_prefill_m2048_with_outliers_sampled(name):
+    K, N = LAYER_SHAPES[name]
+    p = inputs.make_problem(2048, K, N, seed=4000 + K + N, outlier_frac=0.01)
+    y = run_gemm(p)
+    assert_within_bound(y, p, cols=sample_columns(N, 64))
+
+
+@pytest.mark.parametrize("B", [1, 64, 512])
+@pytest.mark.parametrize("K,N", [(8192, 10240), (8192, 57344), (28672, 8192)])
+def test_zero_point_70b_shapes_sampled(K, N, B):
+    p = inputs.make_problem(B, K, N, seed=5000 + K + N, zero_points=True)
+    y = run_gemm(p)
+    assert_within_bound(y, p, cols=sample_columns(N, 64 if B >= 512 else 192))
+
+
+# ------------------------------------------------------------ behaviour
+
+def test_repeated_calls_are_deterministic_and_reuse_workspace():
+    p = inputs.make_problem(4, 4096, 4096, seed=3).to("cuda")
+    packed = w.w4a16_pack(p.qweight)
+    ys = [w.w4a16_gemm(p.x, packed, p.scales, False).clone() for _ in range(3)]
+    # interleave another shape on the same workspace, then repeat
+    q = inputs.make_problem(2, 14336, 4096, seed=4).to("cuda")
+    w.w4a16_gemm(q.x, w.w4a16_pack(q.qweight), q.scales, False)
+    ys.append(w.w4a16_gemm(p.x, packed, p.scales, False))
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+
+
+def test_output_guard_band_untouched():
+    B, K, N = 3, 1024, 200
+    p = inputs.make_problem(B, K, N, seed=8).to("cuda")
+    packed = w.w4a16_pack(p.qweight)
+    buf = torch.full((B * N + 4096,), 12345, dtype=torch.int16, device="cuda")
+    y = buf[:B * N].view(torch.bfloat16).view(B, N)
+    w.w4a16_gemm(p.x, packed, p.scales, False, out=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[B * N:] == 12345)
+    assert_within_bound(y.cpu(), p.to("cpu"))
+
+
+def test_runs_on_a_side_stream():
+    p = inputs.make_problem(8, 2048, 1024, seed=9).to("cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        packed = w.w4a16_pack(p.qweight)
+        y = w.w4a16_gemm(p.x, packed, p.scales, False)
+    s.synchronize()
+    assert_within_bound(y.cpu(), p.to("cpu"))

@@ -1,1 +1,9 @@
-"""W4A16 (bf16 activation x INT4 weight, group-128) linear layer for GB300."""
+"""W4A16 (bf16 activation x INT4 weight, group-128) linear layer for GB300.
+
+The compute lives in the CUDA library ``libw4a16.so`` (C ABI declared in
+``include/w4a16.h``); the functions below are its Python binding, with the
+same names.  The library is loaded on first use and a missing build raises.
+"""
+from ._lib import (GROUP, PATH_AUTO, PATH_NAMES, PATH_SKINNY, PATH_TCGEN05, W4A16Error,  # noqa: F401
+                   load, w4a16_dequant_ref, w4a16_device_status, w4a16_gemm, w4a16_pack,
+                   w4a16_packed_bytes, w4a16_select_path, w4a16_workspace_bytes)

@@ -1,0 +1,192 @@
+"""ctypes binding of ``libw4a16.so``: argument marshalling only.
+
+Every function here has the name of the C entry point it wraps, takes torch
+tensors (device memory and streams come from PyTorch), checks dtypes and
+shapes enough to build the call, and raises ``W4A16Error`` on a non-OK
+status.  All arithmetic happens in the library's CUDA kernels; there is no
+fallback of any kind -- if the library is missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a16.so")
+GROUP = 128
+
+PATH_AUTO, PATH_SKINNY, PATH_TCGEN05 = -1, 0, 1
+PATH_NAMES = {PATH_SKINNY: "skinny", PATH_TCGEN05: "tcgen05"}
+
+_STATUS = {0: "W4A16_OK", 1: "W4A16_ERR_NULL", 2: "W4A16_ERR_SHAPE", 3: "W4A16_ERR_ALIGN",
+           4: "W4A16_ERR_UNSUPPORTED", 5: "W4A16_ERR_WORKSPACE", 6: "W4A16_ERR_CUDA",
+           7: "W4A16_ERR_TIMEOUT"}
+
+# (name, restype, argtypes) of every exported symbol, in header order.
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "w4a16_packed_bytes": (_S, [_I, _I, _I, _I]),
+    "w4a16_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "w4a16_pack": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "w4a16_gemm": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "w4a16_gemm_path": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
+    "w4a16_dequant_ref": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
+    "w4a16_select_path": (_I, [_I, _I, _I]),
+    "w4a16_device_status": (_I, [_I]),
+    "w4a16_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)} ({msg})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {LIB_PATH} is missing "
+                "(run __graft_entry__.build() or python -m weight_only_int4_gemm_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        msg = load().w4a16_status_string(status).decode()
+        raise W4A16Error(fn, status, msg)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+
+
+def w4a16_packed_bytes(K: int, N: int, has_zeros: bool) -> int:
+    return int(load().w4a16_packed_bytes(K, N, GROUP, 1 if has_zeros else 0))
+
+
+def w4a16_workspace_bytes(B: int, K: int, N: int) -> int:
+    v = int(load().w4a16_workspace_bytes(B, K, N, GROUP))
+    if v == ctypes.c_size_t(-1).value:
+        raise ValueError(f"invalid shape B={B} K={K} N={N}")
+    return v
+
+
+def w4a16_select_path(B: int, K: int, N: int) -> int:
+    return int(load().w4a16_select_path(B, K, N))
+
+
+def w4a16_pack(qweight: torch.Tensor, qzeros: torch.Tensor | None = None, *,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Repack canonical codes (int32 [K/8][N]) and zeros (int32 [K/128][N/8])."""
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    _need(qweight, torch.int32, (K // 8, N), "qweight")
+    if qzeros is not None:
+        _need(qzeros, torch.int32, (K // GROUP, N // 8), "qzeros")
+    nbytes = w4a16_packed_bytes(K, N, qzeros is not None)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    _check("w4a16_pack", load().w4a16_pack(
+        qweight.data_ptr(), None if qzeros is None else qzeros.data_ptr(), K, N, GROUP,
+        out.data_ptr(), _stream(stream)))
+    return out
+
+
+class Workspace:
+    """A zero-filled device workspace per device, grown on demand."""
+
+    def __init__(self):
+        self._bufs: dict[int, torch.Tensor] = {}
+
+    def get(self, nbytes: int, device: torch.device) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        buf = self._bufs.get(idx)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+            self._bufs[idx] = buf
+        return buf
+
+
+_default_ws = Workspace()
+
+
+def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, has_zeros: bool,
+               N: int | None = None, *, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, path: int = PATH_AUTO,
+               stream=None) -> torch.Tensor:
+    """y[B][N] = x[B][K] . dequant(packed, scales)."""
+    B, K = x.shape
+    N = scales.shape[1] if N is None else N
+    _need(x, torch.bfloat16, (B, K), "x")
+    _need(scales, torch.bfloat16, (K // GROUP, N), "scales")
+    if packed.numel() * packed.element_size() < w4a16_packed_bytes(K, N, has_zeros):
+        raise ValueError("packed: too small for this shape")
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (B, N), "out")
+    need = w4a16_workspace_bytes(B, K, N)
+    if workspace is None:
+        workspace = _default_ws.get(need, x.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = load()
+    if path == PATH_AUTO:
+        st = lib.w4a16_gemm(x.data_ptr(), packed.data_ptr(), scales.data_ptr(),
+                            1 if has_zeros else 0, out.data_ptr(), B, K, N, GROUP,
+                            ws_ptr, ws_bytes, _stream(stream))
+        _check("w4a16_gemm", st)
+    else:
+        st = lib.w4a16_gemm_path(x.data_ptr(), packed.data_ptr(), scales.data_ptr(),
+                                 1 if has_zeros else 0, out.data_ptr(), B, K, N, GROUP,
+                                 ws_ptr, ws_bytes, int(path), _stream(stream))
+        _check("w4a16_gemm_path", st)
+    return out
+
+
+def w4a16_dequant_ref(packed: torch.Tensor, scales: torch.Tensor, has_zeros: bool, K: int, *,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Dequantised W[K][N] (bf16) through the kernels' own decode routine."""
+    N = scales.shape[1]
+    _need(scales, torch.bfloat16, (K // GROUP, N), "scales")
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.bfloat16, device=scales.device)
+    _need(out, torch.bfloat16, (K, N), "out")
+    _check("w4a16_dequant_ref", load().w4a16_dequant_ref(
+        packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0, out.data_ptr(), K, N,
+        GROUP, _stream(stream)))
+    return out
+
+
+def w4a16_device_status(clear: bool = True) -> int:
+    return int(load().w4a16_device_status(1 if clear else 0))

@@ -1,0 +1,189 @@
+// api.cu -- the C ABI: host-side validation, path selection and launches.
+// Nothing here allocates device memory or synchronises (except
+// w4a16_device_status, which is documented to).
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/w4a16.h"
+#include "launch.cuh"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kMaxK = 1 << 20;
+constexpr int kMaxN = 1 << 22;
+constexpr int kMaxB = 1 << 20;
+
+__device__ unsigned int g_device_status;  // tensor-core kernel's timeout flag
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool shape_ok(int K, int N) {
+    return K > 0 && N > 0 && K % kGroup == 0 && N % 8 == 0 && K <= kMaxK && N <= kMaxN;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int major = 0, minor = 0;
+};
+
+DeviceInfo device_info() {
+    static std::mutex mu;
+    static std::unordered_map<int, DeviceInfo> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DeviceInfo{};
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    DeviceInfo info;
+    cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&info.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&info.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cache[dev] = info;
+    return info;
+}
+
+int num_sms() {
+    const int s = device_info().sms;
+    return s > 0 ? s : 152;
+}
+
+// Batch above which the tensor-core kernel takes over from the split-K
+// kernel (the split-K kernel pads the batch to 8/16/32 rows and re-streams
+// the weights for every further 32 rows).
+constexpr int kSkinnyMaxB = 32;
+
+int choose_path(int B, int K, int N) {
+    (void)K;
+    (void)N;
+    if (B <= kSkinnyMaxB || !tc_available()) return W4A16_PATH_SKINNY;
+    return W4A16_PATH_TCGEN05;
+}
+
+size_t path_workspace(int path, int B, int K, int N) {
+    if (path == W4A16_PATH_SKINNY)
+        return skinny_workspace_bytes(plan_skinny(B, K, N, num_sms()), B, N);
+    return tc_workspace_bytes(plan_tc(B, K, N, num_sms()), B, N);
+}
+
+w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, int has_zeros,
+                       void* y, int B, int K, int N, int group_size, void* workspace,
+                       size_t ws_bytes, int path, void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N) || B < 1 || B > kMaxB) return W4A16_ERR_SHAPE;
+    if (!x || !packed || !scales || !y) return W4A16_ERR_NULL;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales) || !aligned16(y))
+        return W4A16_ERR_ALIGN;
+    if (path == W4A16_PATH_AUTO) path = choose_path(B, K, N);
+    if (path != W4A16_PATH_SKINNY && path != W4A16_PATH_TCGEN05) return W4A16_ERR_UNSUPPORTED;
+    if (path == W4A16_PATH_TCGEN05 && !tc_available()) return W4A16_ERR_UNSUPPORTED;
+    const size_t need = path_workspace(path, B, K, N);
+    if (need > 0) {
+        if (workspace == nullptr) return W4A16_ERR_NULL;
+        if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
+        if (ws_bytes < need) return W4A16_ERR_WORKSPACE;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (path == W4A16_PATH_SKINNY)
+        return from_cuda(launch_skinny(plan_skinny(B, K, N, num_sms()), x, packed, scales,
+                                       has_zeros != 0, y, B, K, N, workspace, s));
+    unsigned int* status = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_device_status) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    return from_cuda(launch_tc(plan_tc(B, K, N, num_sms()), x, packed, scales, has_zeros != 0,
+                               y, B, K, N, workspace, status, s));
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros) {
+    if (group_size != kGroup || !shape_ok(K, N)) return 0;
+    return packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);
+}
+
+size_t w4a16_workspace_bytes(int B, int K, int N, int group_size) {
+    if (group_size != kGroup || !shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
+    // Enough for whichever path a call may take (auto or forced).
+    size_t a = path_workspace(W4A16_PATH_SKINNY, B, K, N);
+    if (tc_available()) {
+        const size_t b = path_workspace(W4A16_PATH_TCGEN05, B, K, N);
+        if (b > a) a = b;
+    }
+    return a;
+}
+
+w4a16_status w4a16_pack(const uint32_t* qweight, const uint32_t* qzeros, int K, int N,
+                        int group_size, void* packed, void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (!qweight || !packed) return W4A16_ERR_NULL;
+    if (!aligned16(qweight) || !aligned16(packed) || (qzeros && !aligned16(qzeros)))
+        return W4A16_ERR_ALIGN;
+    return from_cuda(launch_repack(qweight, qzeros, K, N, packed, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_gemm(const void* x, const void* packed, const void* scales, int has_zeros,
+                        void* y, int B, int K, int N, int group_size, void* workspace,
+                        size_t ws_bytes, void* stream) {
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     W4A16_PATH_AUTO, stream);
+}
+
+w4a16_status w4a16_gemm_path(const void* x, const void* packed, const void* scales,
+                             int has_zeros, void* y, int B, int K, int N, int group_size,
+                             void* workspace, size_t ws_bytes, int path, void* stream) {
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     path, stream);
+}
+
+w4a16_status w4a16_dequant_ref(const void* packed, const void* scales, int has_zeros, void* w,
+                               int K, int N, int group_size, void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (!packed || !scales || !w) return W4A16_ERR_NULL;
+    if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return W4A16_ERR_ALIGN;
+    return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_select_path(int B, int K, int N) {
+    if (!shape_ok(K, N) || B < 1 || B > kMaxB) return -1;
+    return choose_path(B, K, N);
+}
+
+w4a16_status w4a16_device_status(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4A16_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+            return W4A16_ERR_CUDA;
+    }
+    return v == 0 ? W4A16_OK : W4A16_ERR_TIMEOUT;
+}
+
+const char* w4a16_status_string(w4a16_status status) {
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4A16_ERR_NULL: return "a required pointer is NULL";
+        case W4A16_ERR_SHAPE: return "invalid shape (need B >= 1, K % 128 == 0, N % 8 == 0)";
+        case W4A16_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case W4A16_ERR_UNSUPPORTED: return "unsupported group size or kernel path";
+        case W4A16_ERR_WORKSPACE: return "workspace too small";
+        case W4A16_ERR_CUDA: return "CUDA error";
+        case W4A16_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

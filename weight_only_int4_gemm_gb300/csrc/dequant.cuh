@@ -1,0 +1,84 @@
+// dequant.cuh -- packed weight layout and the register-level INT4 -> bf16
+// decode shared by every kernel of the library (GEMMs and dequant_ref).
+//
+// Decode ("When quantization pays -- and when it does not", section
+// "Counting c from the kernel, not from intuition"): OR-ing a 4-bit code q
+// into the low fraction bits of bf16 128.0 (0x4300) gives exactly bf16(128+q);
+// subtracting bf16(128+z) (z = 8 for the symmetric format, i.e. 136.0 =
+// 0x4308) gives the exact integer q - z; one round-to-nearest-even bf16
+// multiply by the group scale then gives w = RNE_bf16((q - z) * s).  One
+// lop3 builds two such values at once, one in each 16-bit half.
+//
+// Packed layout (version W4A16_PACKED_LAYOUT = 1):
+//   codes: uint32 [K/32][N][4].  The 16 bytes at chunk c, column n hold the
+//   32 codes of rows k = 32c .. 32c+31 of column n; word j holds rows
+//   32c + 8j .. 32c + 8j + 7.  Inside a word, the codes of rows (2i, 2i+1)
+//   (offsets within the word) sit in nibbles i and i + 4, i.e. in the low and
+//   high 16-bit halves at the same bit offset 4i, so
+//        (word >> 4i) & 0x000F000F  ==  { code(2i), code(2i+1) }.
+//   zeros (asymmetric format only): the canonical uint32 [K/128][N/8] array,
+//   copied unchanged after the codes.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+// Nibble position of row offset r (0..7) inside a packed word.
+__host__ __device__ constexpr int packed_nibble_of_row(int r) {
+    return (r & 1) ? 4 + (r >> 1) : (r >> 1);
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    // (a & b) | c, as one LOP3 (lookup table 0xF0 & 0xCC | 0xAA = 0xEA).
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16(128 + z) in both halves: the value subtracted after the magic OR.
+__device__ __forceinline__ uint32_t zero_pair(uint32_t z) {
+    return 0x43004300u | (z * 0x00010001u);
+}
+constexpr uint32_t kSymmetricZeroPair = 0x43084308u;  // bf16 136.0 = 128 + 8, twice
+
+// Scale broadcast to both halves.
+__device__ __forceinline__ uint32_t scale_pair(uint16_t s) {
+    return (uint32_t)s * 0x00010001u;
+}
+
+// Pair i (0..3) of a packed word: rows (2i, 2i+1) as bf16x2, exact
+// RNE_bf16((q - z) * s) in each half.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int i, uint32_t zero2,
+                                                 uint32_t scale2) {
+    const uint32_t magic = lop3_and_or(word >> (4 * i), 0x000F000Fu, 0x43004300u);
+    return bf16x2_mul(bf16x2_sub(magic, zero2), scale2);
+}
+
+// All 8 rows of a packed word, out[i] = rows (2i, 2i+1).
+__device__ __forceinline__ void dequant_word(uint32_t word, uint32_t zero2, uint32_t scale2,
+                                             uint32_t out[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = dequant_pair(word, i, zero2, scale2);
+}
+
+// Zero-point nibble of column n, group g, from the canonical zeros array.
+__device__ __forceinline__ uint32_t load_zero(const uint32_t* zeros, int N, int g, int n) {
+    const uint32_t w = __ldg(zeros + (size_t)g * (N >> 3) + (n >> 3));
+    return (w >> (4 * (n & 7))) & 0xFu;
+}
+
+}  // namespace w4a16

@@ -1,0 +1,50 @@
+// launch.cuh -- internal launchers and planners behind the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+constexpr int kGroup = 128;
+
+inline size_t packed_code_bytes(int K, int N) { return (size_t)K * (size_t)N / 2; }
+inline size_t packed_zero_bytes(int K, int N) { return (size_t)(K / kGroup) * (size_t)(N / 8) * 4; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K, int N,
+                          void* packed, cudaStream_t stream);
+cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,
+                               int K, int N, cudaStream_t stream);
+
+// ---- small-batch split-K kernel (skinny.cu) ----
+struct SkinnyPlan {
+    int nt;            // n8 batch tiles per CTA pass: 1, 2 or 4 (8, 16 or 32 rows)
+    int batch_chunks;  // ceil(B / (8 * nt))
+    int col_blocks;    // ceil(N / columns per CTA)
+    int gps;           // groups of 128 rows per K split
+    int split;         // number of K splits (1 = no workspace)
+};
+SkinnyPlan plan_skinny(int B, int K, int N, int num_sms);
+size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N);
+cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
+                          const void* scales, bool has_zeros, void* y, int B, int K, int N,
+                          void* workspace, cudaStream_t stream);
+
+// ---- tcgen05 tensor-core kernel (tc_gemm.cu) ----
+struct TcPlan {
+    int bn;          // batch rows per CTA tile (MMA N): 16 .. 256, multiple of 16
+    int batch_tiles; // ceil(B / bn)
+    int col_tiles;   // ceil(N / 128)
+    int kb_per_split;// 64-row K blocks per split
+    int split;       // K splits (1 = no workspace)
+};
+TcPlan plan_tc(int B, int K, int N, int num_sms);
+size_t tc_workspace_bytes(const TcPlan& p, int B, int N);
+cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
+                      bool has_zeros, void* y, int B, int K, int N, void* workspace,
+                      unsigned int* status, cudaStream_t stream);
+bool tc_available();
+
+}  // namespace w4a16
