@@ -275,9 +275,53 @@ def run_gpu(args, gemms, rank, world, device):
     ms = start.elapsed_time(stop)
     assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
 
+    if args.per_gemm:
+        per_gemm_table(gemms, layers, ws, stream, device, hbm)
     # end to end through the public API with host buffers
     e2e = run_e2e(args, gemms, layers, device, ws, pick)
     return ms, clk.summary(), paths, n_copies, e2e
+
+
+def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200):
+    """Each distinct (B, K, N) alone, in a CUDA graph of `reps` launches that
+    rotate over the weight copies; prints one line per GEMM to stderr."""
+    import torch
+
+    import weight_only_int4_gemm_gb300 as w
+    from weight_only_int4_gemm_gb300 import model
+
+    seen = set()
+    for i, (label, B, K, N, zp, _) in enumerate(gemms):
+        if (B, K, N, zp) in seen:
+            continue
+        seen.add((B, K, N, zp))
+        reps_list = layers[(K, N, zp)]
+        x = torch.randn((B, K), device=device).to(torch.bfloat16)
+        y = torch.empty((B, N), dtype=torch.bfloat16, device=device)
+        with torch.cuda.stream(stream):
+            for r in range(3):
+                packed, sc = reps_list[r % len(reps_list)]
+                w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                packed, sc = reps_list[r % len(reps_list)]
+                w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream)
+        for _ in range(2):
+            g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        byts = model.linear_bytes(B, K, N, zp)
+        fl = model.linear_flops(B, K, N)
+        print(f"per-gemm B={B:5d} K={K:6d} N={N:6d} zp={int(zp)} path={w.PATH_NAMES[w.w4a16_select_path(B, K, N)]:8s} "
+              f"{us:9.2f} us  {byts / us / 1e3:8.1f} GB/s ({byts / us / 1e3 / hbm_gbs * 100:5.1f}% hbm)  "
+              f"{fl / us / 1e6:8.1f} TFLOP/s", file=sys.stderr, flush=True)
 
 
 def run_e2e(args, gemms, layers, device, ws, pick):
@@ -336,7 +380,7 @@ class OracleSampler:
             return t.view(__import__("torch").int16).numpy().view(np.uint16) \
                 if str(t.dtype) == "torch.bfloat16" else t.numpy().view(np.uint32)
 
-        self.MAX_COLS = 1024
+        self.MAX_COLS = 4096
         self.np, self.oracle, self.gemms = np, oracle, gemms
         self.probs = []
         for i, (label, B, K, N, zp, outl) in enumerate(gemms):
@@ -355,7 +399,7 @@ class OracleSampler:
         return est
 
     def calibrate(self, seconds_per_step: float):
-        """Grow the column sample (1 .. 1024) until one sampled step costs about
+        """Grow the column sample (1 .. 4096) until one sampled step costs about
         ``seconds_per_step`` of CPU time."""
         while self.cols < self.MAX_COLS:
             t0 = time.perf_counter()
@@ -384,6 +428,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-gemm", action="store_true",
+                    help="also time each distinct GEMM alone (table on stderr)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

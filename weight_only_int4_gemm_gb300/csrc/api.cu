@@ -99,6 +99,22 @@ w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, in
 }
 
 }  // namespace
+
+cudaError_t launch_with_pdl(const void* func, dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, void** args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
 }  // namespace w4a16
 
 using namespace w4a16;

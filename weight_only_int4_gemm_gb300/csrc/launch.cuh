@@ -13,6 +13,28 @@ inline size_t packed_code_bytes(int K, int N) { return (size_t)K * (size_t)N / 2
 inline size_t packed_zero_bytes(int K, int N) { return (size_t)(K / kGroup) * (size_t)(N / 8) * 4; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Workspace layout shared by every split-K kernel: a fixed prefix of arrival
+// counters (zero-filled once by the caller, left at zero by every call) and,
+// after it, the fp32 partial sums (no initialisation needed).  The prefix
+// does not depend on the shape, so calls of different shapes can share one
+// workspace.  Shapes with more output tiles than counters never split K.
+constexpr int kMaxCounters = 16384;
+constexpr size_t kCounterBytes = kMaxCounters * sizeof(uint32_t);
+inline size_t split_workspace_bytes(int split, int B, int N) {
+    return split <= 1 ? 0 : kCounterBytes + (size_t)split * B * N * sizeof(float);
+}
+inline uint32_t* ws_counters(void* ws) { return static_cast<uint32_t*>(ws); }
+inline float* ws_partials(void* ws) {
+    return ws == nullptr ? nullptr
+                         : reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+}
+
+// Programmatic dependent launch: kernels may start (and prefetch weights)
+// while the previous kernel on the stream finishes; they wait before reading
+// activations or touching outputs and workspace.
+cudaError_t launch_with_pdl(const void* func, dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, void** args);
+
 cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K, int N,
                           void* packed, cudaStream_t stream);
 cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,

@@ -38,7 +38,8 @@ constexpr int kWarpsK = 2;                 // warps across K groups
 constexpr int kThreads = 32 * kWarpsN * kWarpsK;
 constexpr int kColsPerCta = 16 * kWarpsN;  // 64
 constexpr int kPrefetch = 4;               // groups of codes in flight per warp
-constexpr int kMaxGroupsTimesNt = 16;      // caps the staged x slice at 32 KB
+constexpr int kMaxGps = kWarpsK * kPrefetch;  // groups per CTA = one round of loads
+constexpr int kMaxRowsTimesGps = 128;      // caps the staged x slice at 64 KB
 
 struct Args {
     const uint16_t* x;
@@ -47,7 +48,7 @@ struct Args {
     const uint32_t* zeros;
     uint16_t* y;
     float* partial;      // [split][B][N]
-    uint32_t* counters;  // [batch_chunks][col_blocks]
+    uint32_t* counters;  // [batch_chunks][col_blocks] (fixed workspace prefix)
     int B, K, N;
     int gps, split;
 };
@@ -75,7 +76,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 }
 
 template <int NT, bool kHasZeros>
-__global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const Args a) {
     extern __shared__ uint4 smem[];
     constexpr int kRows = 8 * NT;  // batch rows per CTA pass
 
@@ -90,42 +91,17 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
     const int g_begin = blockIdx.y * a.gps;
     const int ng = min(a.gps, G - g_begin);
     const int b0 = blockIdx.z * kRows;
+    const int rows = min(kRows, a.B - b0);
     const int n_cta = blockIdx.x * kColsPerCta;
-
-    // 1. Stage x[b0 .. b0+kRows)[group range] in fragment order:
-    //    entry ((gl*4 + m)*kRows + r)*4 + t = x[b0+r][128*(g_begin+gl) + 32t + 8m .. +8].
-    uint4* xs = smem;
-    {
-        const int pieces_per_row = ng * 16;
-        const int total = pieces_per_row * kRows;
-        for (int e = threadIdx.x; e < total; e += kThreads) {
-            const int r = e / pieces_per_row;
-            const int p = e - r * pieces_per_row;
-            const int gl = p >> 4;
-            const int within = p & 15;  // 8-row piece within the group
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (b0 + r < a.B)
-                v = __ldg(reinterpret_cast<const uint4*>(
-                    a.x + (size_t)(b0 + r) * a.K + (size_t)kGroup * (g_begin + gl) + 8 * within));
-            xs[((gl * 4 + (within & 3)) * kRows + r) * 4 + (within >> 2)] = v;
-        }
-    }
-    __syncthreads();
-
-    // 2. Stream this warp's 16 columns over its groups.
     const int n0 = n_cta + wn * 16;
     const int na = min(n0 + gid, a.N - 1);
     const int nb = min(n0 + gid + 8, a.N - 1);
 
-    float acc[NT][4];
-#pragma unroll
-    for (int bt = 0; bt < NT; ++bt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[bt][i] = 0.f;
-
-    for (int gl0 = wk; gl0 < ng; gl0 += kWarpsK * kPrefetch) {
-        uint4 wa[kPrefetch], wb[kPrefetch];
-        uint32_t sa[kPrefetch], sb[kPrefetch], za[kPrefetch], zb[kPrefetch];
+    // 1. Weights, scales and zero-points do not depend on the previous kernel:
+    //    put this warp's first round of loads in flight before anything else.
+    uint4 wa[kPrefetch], wb[kPrefetch];
+    uint32_t sa[kPrefetch], sb[kPrefetch], za[kPrefetch], zb[kPrefetch];
+    auto load_round = [&](int gl0) {
 #pragma unroll
         for (int u = 0; u < kPrefetch; ++u) {
             const int gl = gl0 + u * kWarpsK;
@@ -144,6 +120,43 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
                 }
             }
         }
+    };
+    load_round(wk);
+
+    // 2. Let the next kernel on the stream start its own weight stream, then
+    //    wait for the previous one before reading x or touching outputs.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // 3. Stage x[b0 .. b0+kRows)[group range] in fragment order:
+    //    entry ((gl*4 + m)*kRows + r)*4 + t = x[b0+r][128*(g_begin+gl) + 32t + 8m .. +8].
+    uint4* xs = smem;
+    {
+        const int pieces_per_row = ng * 16;
+        const int total = pieces_per_row * kRows;
+        for (int e = threadIdx.x; e < total; e += kThreads) {
+            const int r = e / pieces_per_row;
+            const int p = e - r * pieces_per_row;
+            const int gl = p >> 4;
+            const int within = p & 15;  // 8-row piece within the group
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows)
+                v = __ldg(reinterpret_cast<const uint4*>(
+                    a.x + (size_t)(b0 + r) * a.K + (size_t)kGroup * (g_begin + gl) + 8 * within));
+            xs[((gl * 4 + (within & 3)) * kRows + r) * 4 + (within >> 2)] = v;
+        }
+    }
+    __syncthreads();
+
+    // 4. Decode and multiply, one round of prefetched groups at a time.
+    float acc[NT][4];
+#pragma unroll
+    for (int bt = 0; bt < NT; ++bt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[bt][i] = 0.f;
+
+    for (int gl0 = wk; gl0 < ng; gl0 += kWarpsK * kPrefetch) {
+        if (gl0 != wk) load_round(gl0);
 #pragma unroll
         for (int u = 0; u < kPrefetch; ++u) {
             const int gl = gl0 + u * kWarpsK;
@@ -165,15 +178,16 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
                         const uint32_t a3 = dequant_pair(wB[j], 2 * h + 1, zb[u], sb[u]);
 #pragma unroll
                         for (int bt = 0; bt < NT; ++bt)
-                            mma_bf16(acc[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
-                                     h ? xf[bt].w : xf[bt].y);
+                            if (bt * 8 < rows)  // warp-uniform: skip all-padding tiles
+                                mma_bf16(acc[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
+                                         h ? xf[bt].w : xf[bt].y);
                     }
                 }
             }
         }
     }
 
-    // 3. Reduce the K-warps through shared memory (fixed order).
+    // 5. Reduce the K-warps through shared memory (fixed order).
     float* red = reinterpret_cast<float*>(smem + (size_t)a.gps * 16 * kRows);
     if (kWarpsK > 1) {
         if (wk > 0) {
@@ -195,8 +209,8 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
         }
     }
 
-    // 4. Output: D row (gid or gid+8) is a weight column, D column (2*tig + i&1)
-    //    a batch row.
+    // 6. Output: D row (gid or gid+8) is a weight column, D column
+    //    (2*tig + (i & 1)) a batch row.
     if (wk == 0) {
 #pragma unroll
         for (int bt = 0; bt < NT; ++bt)
@@ -214,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
     }
     if (a.split == 1) return;
 
-    // 5. Last CTA of this column block sums the split partials in order.
+    // 7. Last CTA of this column block sums the split partials in order.
     __shared__ int s_is_last;
     __threadfence();
     __syncthreads();
@@ -230,7 +244,6 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
     __syncthreads();
     if (!s_is_last) return;
     __threadfence();
-    const int rows = min(kRows, a.B - b0);
     const int cols = min(kColsPerCta, a.N - n_cta);
     for (int e = threadIdx.x; e < rows * cols; e += kThreads) {
         const int r = e / cols;
@@ -244,17 +257,28 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const Args a) {
     if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
 }
 
+template <int NT>
+size_t smem_for(int gps) {
+    return (size_t)gps * 16 * 8 * NT * sizeof(uint4) +
+           (size_t)(kWarpsK - 1) * kWarpsN * NT * 4 * 32 * sizeof(float);
+}
+
 template <int NT, bool Z>
-cudaError_t launch_t(const SkinnyPlan& p, const Args& a, cudaStream_t stream) {
-    const size_t smem = (size_t)p.gps * 16 * 8 * NT * sizeof(uint4) +
-                        (size_t)(kWarpsK - 1) * kWarpsN * NT * 4 * 32 * sizeof(float);
-    auto kern = skinny_kernel<NT, Z>;
+cudaError_t launch_t(const SkinnyPlan& p, Args a, cudaStream_t stream) {
+    const size_t smem = smem_for<NT>(p.gps);
+    const void* kern = reinterpret_cast<const void*>(skinny_kernel<NT, Z>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(p.col_blocks, p.split, p.batch_chunks);
-    kern<<<grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    void* args[] = {&a};
+    return launch_with_pdl(kern, dim3(p.col_blocks, p.split, p.batch_chunks), dim3(kThreads),
+                           smem, stream, args);
+}
+
+int resident_ctas_per_sm(int nt) {
+    // registers bound the residency; two CTAs per SM is what the kernel is
+    // built for (launch bounds), one when the staged slice is large
+    return nt >= 4 ? 1 : 2;
 }
 
 }  // namespace
@@ -265,22 +289,35 @@ SkinnyPlan plan_skinny(int B, int K, int N, int num_sms) {
     p.batch_chunks = (B + 8 * p.nt - 1) / (8 * p.nt);
     p.col_blocks = (N + kColsPerCta - 1) / kColsPerCta;
     const int G = K / kGroup;
-    const int max_gps = std::max(1, kMaxGroupsTimesNt / p.nt);
+    const int cap = std::max(1, std::min(kMaxGps, kMaxRowsTimesGps / (8 * p.nt)));
     const long long base = (long long)p.col_blocks * p.batch_chunks;
-    const long long target = 4LL * num_sms;  // CTAs wanted in flight
-    int split = (int)std::min<long long>(G, std::max<long long>(1, (target + base - 1) / base));
-    int gps = (G + split - 1) / split;
-    gps = std::min(gps, max_gps);
-    p.gps = gps;
-    p.split = (G + gps - 1) / gps;
+    const long long slots = (long long)num_sms * resident_ctas_per_sm(p.nt);
+    // choose groups per CTA minimising (waves x per-CTA time), per-CTA time
+    // being its groups plus a fixed cost (launch, staging, reduction)
+    double best = 1e300;
+    int best_gps = std::min(cap, G);
+    for (int gps = std::min(cap, G); gps >= 1; --gps) {
+        const int split = (G + gps - 1) / gps;
+        if (split > 1 && base > kMaxCounters) break;
+        const long long ctas = base * split;
+        const long long waves = (ctas + slots - 1) / slots;
+        const double cost = (double)waves * (gps + 2.0) + (split > 1 ? 0.5 : 0.0);
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_gps = gps;
+        }
+    }
+    p.gps = best_gps;
+    p.split = (G + best_gps - 1) / best_gps;
+    if (p.split > 1 && base > kMaxCounters) {  // no counters to spare: one CTA per column block
+        p.gps = G;
+        p.split = 1;
+    }
     return p;
 }
 
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N) {
-    if (p.split <= 1) return 0;
-    const size_t partial = align_up((size_t)p.split * B * N * sizeof(float), 256);
-    const size_t counters = (size_t)p.batch_chunks * p.col_blocks * sizeof(uint32_t);
-    return partial + align_up(counters, 256);
+    return split_workspace_bytes(p.split, B, N);
 }
 
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
@@ -293,12 +330,8 @@ cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed
     a.zeros = reinterpret_cast<const uint32_t*>(static_cast<const char*>(packed) +
                                                 packed_code_bytes(K, N));
     a.y = static_cast<uint16_t*>(y);
-    a.partial = static_cast<float*>(workspace);
-    a.counters = workspace == nullptr
-                     ? nullptr
-                     : reinterpret_cast<uint32_t*>(
-                           static_cast<char*>(workspace) +
-                           align_up((size_t)p.split * B * N * sizeof(float), 256));
+    a.partial = ws_partials(workspace);
+    a.counters = ws_counters(workspace);
     a.B = B;
     a.K = K;
     a.N = N;

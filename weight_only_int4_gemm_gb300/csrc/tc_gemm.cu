@@ -1,27 +1,567 @@
-// tc_gemm.cu -- tcgen05/TMEM tensor-core W4A16 GEMM (large batch).
+// tc_gemm.cu -- compute-bound W4A16 GEMM on the 5th-generation tensor cores
+// (tcgen05 MMA with TMEM accumulators, TMA-fed operands), for large batches.
+//
+// "Give Me BF16 or Give Me Death" (summary), "Inference with W4A16": the
+// 4-bit weights are rebuilt to 16-bit values inside the matrix
+// multiplication and multiplied on 16-bit tensor cores with higher-precision
+// accumulation; at large batch the layer is compute-bound.  "When
+// quantization pays -- and when it does not" (model of a decode step): the
+// dequantisation runs on the CUDA cores and is only free while another pipe is
+// longer -- so here it runs in dedicated producer warps, overlapped with the
+// asynchronous tensor pipe.
+//
+// Tile (operands swapped so the weight tile is the 128-row MMA operand):
+//   D[128 weight columns][bn batch rows] (fp32, TMEM)
+//     += W^T[128][64 k] (bf16, smem, dequantised by producer warps)
+//      . X^T[64 k][bn]  (bf16, smem, TMA from x[B][K])
+// Warp roles (one CTA per tile, K streamed in 64-row blocks through a ring of
+// kSlots shared-memory slots):
+//   warp 0     : TMA thread -- bulk-copies the packed codes of the block and
+//                tensor-copies the x block (128-byte swizzle), one mbarrier
+//                with the expected byte count per slot;
+//   warp 1     : TMEM allocator + the single MMA-issuing thread
+//                (tcgen05.mma kind::f16, 4 x K=16 per block, commit to the
+//                slot's "empty" barrier);
+//   warps 2..9 : dequant producers -- packed codes (smem) -> lop3 magic
+//                decode -> bf16 (q - z) * s -> 128-byte-swizzled K-major
+//                rows of the weight tile; proxy fence; arrive;
+//   warps 4..7 : after the K loop, the epilogue (tcgen05.ld 32 lanes x 16
+//                columns -> bf16 y, or fp32 split-K partials).
+// Every mbarrier wait is bounded; on expiry the kernel records
+// W4A16_ERR_TIMEOUT in the device status word, drains and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "dequant.cuh"
 #include "launch.cuh"
 
 namespace w4a16 {
+namespace {
 
-bool tc_available() { return false; }
+constexpr int kBlockK = 64;                  // K rows per pipeline slot
+constexpr int kTileN = 128;                  // weight columns per CTA (MMA M)
+constexpr int kSlots = 4;
+constexpr int kNumWarps = 10;
+constexpr int kThreads = 32 * kNumWarps;
+constexpr int kDequantWarp0 = 2;
+constexpr int kDequantWarps = 8;
+constexpr int kEpilogueWarp0 = 4;            // warps 4..7 = TMEM lane quadrants 0..3
+constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
+constexpr uint32_t kRawBytes = kTileN * kBlockK / 2;     // 4 KB of packed codes
+constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
+constexpr unsigned int kStatusTimeout = 7;               // W4A16_ERR_TIMEOUT
+
+struct Args {
+    const uint8_t* packed;
+    const uint16_t* scales;
+    const uint32_t* zeros;
+    uint16_t* y;
+    float* partial;
+    uint32_t* counters;
+    unsigned int* status;
+    int B, K, N;
+    int bn;             // MMA N (batch rows per tile), multiple of 16
+    int kb_per_split;   // K blocks per split
+    int split;
+    int nkb;            // total K blocks (K / 64)
+    uint32_t tmem_cols; // power of two >= max(32, bn)
+    int force_timeout;  // test hook: wait on a barrier nobody arrives at
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase with this parity completed; false when the
+// CTA is aborting (another wait expired) or this wait expired (then it sets
+// the abort flag and the device status word).
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* status, unsigned long long limit_ns) {
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            *abort = 1;
+            atomicExch(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart; start address in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);       // start address
+    d |= (uint64_t)1 << 16;                        // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset
+    d |= (uint64_t)1 << 46;                        // descriptor version
+    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// M = 128, N = n.
+__device__ __forceinline__ uint32_t instr_desc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kTileN >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// ------------------------------------------------------------ kernel
+
+struct SharedTail {
+    uint64_t full_tma[kSlots];   // TMA bytes landed (codes + x)
+    uint64_t full_ops[kSlots];   // weight tile dequantised (8 warp arrivals)
+    uint64_t empty[kSlots];      // MMAs reading the slot finished (commit)
+    uint64_t accum;              // all MMAs finished (commit)
+    uint64_t never;              // test hook: nobody arrives here
+    uint32_t tmem_base;
+    int abort;
+    int is_last;
+};
+
+__host__ __device__ constexpr uint32_t slot_bytes(int bn) {
+    return kATileBytes + (uint32_t)bn * kBlockK * 2 + kRawBytes;
+}
+
+template <bool kHasZeros>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled operand tiles
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sbytes = slot_bytes(a.bn);
+    SharedTail* tail = reinterpret_cast<SharedTail*>(smem + kSlots * sbytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int col_tile = blockIdx.x;
+    const int batch_tile = blockIdx.y;
+    const int split_idx = blockIdx.z;
+    const int n0 = col_tile * kTileN;
+    const int b0 = batch_tile * a.bn;
+    const int nvalid = min(kTileN, a.N - n0);
+    const int kb_begin = split_idx * a.kb_per_split;
+    const int nkb = min(a.kb_per_split, a.nkb - kb_begin);
+    volatile int* abort = &tail->abort;
+
+    auto a_tile = [&](int s) { return smem + s * sbytes; };
+    auto x_tile = [&](int s) { return smem + s * sbytes + kATileBytes; };
+    auto raw_tile = [&](int s) { return smem + s * sbytes + kATileBytes + a.bn * kBlockK * 2; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(smem_u32(&tail->full_tma[s]), 1);
+            mbar_init(smem_u32(&tail->full_ops[s]), kDequantWarps);
+            mbar_init(smem_u32(&tail->empty[s]), 1);
+        }
+        mbar_init(smem_u32(&tail->accum), 1);
+        mbar_init(smem_u32(&tail->never), 1);
+        tail->abort = 0;
+        tail->is_last = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&tail->tmem_base)), "r"(a.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = tail->tmem_base;
+    // the next kernel on the stream may start now; this one reads x and writes
+    // y / workspace only after the previous kernel has finished (the TMA
+    // thread waits; everything else is ordered after it through mbarriers)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            const uint32_t raw_chunk = (uint32_t)nvalid * 16;
+            const uint32_t tx = 2 * raw_chunk + (uint32_t)a.bn * kBlockK * 2;
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % kSlots;
+                if (i >= kSlots &&
+                    !wait_bounded(smem_u32(&tail->empty[s]), ((i / kSlots) - 1) & 1, abort,
+                                  a.status, kTimeoutNs))
+                    break;
+                const uint32_t bar = smem_u32(&tail->full_tma[s]);
+                const int kb = kb_begin + i;
+                mbar_arrive_expect_tx(bar, tx);
+                const uint8_t* src0 = a.packed + ((size_t)(2 * kb) * a.N + n0) * 16;
+                const uint8_t* src1 = a.packed + ((size_t)(2 * kb + 1) * a.N + n0) * 16;
+                bulk_g2s(smem_u32(raw_tile(s)), src0, raw_chunk, bar);
+                bulk_g2s(smem_u32(raw_tile(s)) + kTileN * 16, src1, raw_chunk, bar);
+                tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, b0, bar);
+                issued = i + 1;
+            }
+            // drain: the copies of the last slots must land before the CTA exits
+            for (int i = max(0, issued - kSlots); i < issued; ++i)
+                wait_bounded(smem_u32(&tail->full_tma[i % kSlots]), (i / kSlots) & 1, abort,
+                             a.status, kTimeoutNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc_bf16(a.bn);
+            bool ok = true;
+            if (a.force_timeout)
+                ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
+                                  (unsigned long long)a.force_timeout * 1000000ull);
+            for (int i = 0; ok && i < nkb; ++i) {
+                const int s = i % kSlots;
+                const uint32_t ph = (i / kSlots) & 1;
+                if (!wait_bounded(smem_u32(&tail->full_tma[s]), ph, abort, a.status, kTimeoutNs) ||
+                    !wait_bounded(smem_u32(&tail->full_ops[s]), ph, abort, a.status, kTimeoutNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t abase = smem_u32(a_tile(s));
+                const uint32_t xbase = smem_u32(x_tile(s));
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / 16; ++kk)
+                    mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
+                                smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
+                mma_commit(smem_u32(&tail->empty[s]));
+            }
+            mma_commit(smem_u32(&tail->accum));  // fires once every issued MMA is done
+        }
+    } else {
+        // ---------------- dequant producers (warps 2..9)
+        const int t = threadIdx.x - 32 * kDequantWarp0;  // 0..255
+        const int r = t & (kTileN - 1);                   // weight column within the tile
+        const int h = t >> 7;                             // which 32-row chunk of the block
+        const int n = min(n0 + r, a.N - 1);
+        int cur_g = -1;
+        uint32_t s2 = 0, z2 = kSymmetricZeroPair;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % kSlots;
+            const int kb = kb_begin + i;
+            const int g = kb >> 1;  // two 64-row blocks per group of 128
+            if (g != cur_g) {
+                s2 = scale_pair(__ldg(a.scales + (size_t)g * a.N + n));
+                if (kHasZeros) z2 = zero_pair(load_zero(a.zeros, a.N, g, n));
+                cur_g = g;
+            }
+            const bool landed = wait_bounded(smem_u32(&tail->full_tma[s]), (i / kSlots) & 1,
+                                             abort, a.status, kTimeoutNs);
+            if (!__all_sync(0xffffffffu, landed)) break;  // warp-uniform exit
+            const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * kTileN + r];
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            uint8_t* row = a_tile(s) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t p[4];
+                dequant_word(words[j], z2, s2, p);
+                const int chunk = (4 * h + j) ^ (r & 7);  // 128-byte swizzle
+                *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(p[0], p[1], p[2], p[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tail->full_ops[s]));
+        }
+
+        // ---------------- epilogue (warps 4..7 = lane quadrants 0..3)
+        if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+            const int quad = warp - kEpilogueWarp0;
+            const bool done = wait_bounded(smem_u32(&tail->accum), 0, abort, a.status, kTimeoutNs);
+            tc_fence_after();
+            if (__all_sync(0xffffffffu, done && !*abort)) {  // tcgen05.ld is warp-collective
+                const int nn = n0 + quad * 32 + lane;
+                const uint32_t taddr = tmem_d + ((uint32_t)(quad * 32) << 16);
+                for (int c0 = 0; c0 < a.bn; c0 += 16) {
+                    float v[16];
+                    tmem_ld_16(taddr + c0, v);
+                    if (nn < a.N) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int b = b0 + c0 + j;
+                            if (b < a.B) {
+                                if (a.split == 1)
+                                    a.y[(size_t)b * a.N + nn] = f32_to_bf16_rn(v[j]);
+                                else
+                                    a.partial[((size_t)split_idx * a.B + b) * a.N + nn] = v[j];
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
+                     "r"(a.tmem_cols)
+                     : "memory");
+    }
+    if (a.split == 1 || *abort) return;
+
+    // ---------------- split-K: the last CTA of this tile sums the partials in order
+    __threadfence();
+    __syncthreads();
+    uint32_t* counter = a.counters + (size_t)batch_tile * gridDim.x + col_tile;
+    if (threadIdx.x == 0) {
+        uint32_t prev;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(counter)
+                     : "memory");
+        tail->is_last = (prev == (uint32_t)(a.split - 1));
+    }
+    __syncthreads();
+    if (!tail->is_last) return;
+    __threadfence();
+    const int rows = min(a.bn, a.B - b0);
+    for (int e = threadIdx.x; e < rows * nvalid; e += kThreads) {
+        const int rr = e / nvalid;
+        const int cc = e - rr * nvalid;
+        const size_t off = (size_t)(b0 + rr) * a.N + n0 + cc;
+        float sum = 0.f;
+        for (int sk = 0; sk < a.split; ++sk) sum += __ldcg(a.partial + (size_t)sk * a.B * a.N + off);
+        a.y[off] = f32_to_bf16_rn(sum);
+    }
+    if (threadIdx.x == 0) *counter = 0u;
+}
+
+// ------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+size_t smem_bytes(int bn) { return (size_t)kSlots * slot_bytes(bn) + sizeof(SharedTail) + 1024; }
+
+uint32_t tmem_cols_for(int bn) {
+    uint32_t c = 32;
+    while (c < (uint32_t)bn) c <<= 1;
+    return c;
+}
+
+}  // namespace
+
+bool tc_available() {
+    // cached per device: sm_103 and the tensor-map encoder are both needed
+    static std::mutex mu;
+    static int known[64] = {0};  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (known[dev] == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        known[dev] = (major == 10 && minor == 3 && encode_fn() != nullptr) ? 1 : 2;
+    }
+    return known[dev] == 1;
+}
 
 TcPlan plan_tc(int B, int K, int N, int num_sms) {
-    (void)K;
-    (void)num_sms;
     TcPlan p{};
-    p.bn = 256;
     p.batch_tiles = (B + 255) / 256;
-    p.col_tiles = (N + 127) / 128;
-    p.kb_per_split = 0;
-    p.split = 1;
+    const int per = (B + p.batch_tiles - 1) / p.batch_tiles;
+    p.bn = std::min(256, (per + 15) / 16 * 16);
+    p.col_tiles = (N + kTileN - 1) / kTileN;
+    const int nkb = K / kBlockK;
+    const long long tiles = (long long)p.col_tiles * p.batch_tiles;
+    // K split that minimises (waves x blocks per CTA), a little cost per split
+    double best = 1e300;
+    int best_split = 1, best_kbps = nkb;
+    for (int split = 1; split <= std::min(16, nkb); ++split) {
+        const int kbps = (nkb + split - 1) / split;
+        if (split > 1 && (kbps < 8 || tiles > kMaxCounters)) break;
+        const int s = (nkb + kbps - 1) / kbps;
+        const long long ctas = tiles * s;
+        const long long waves = (ctas + num_sms - 1) / num_sms;
+        const double cost = (double)waves * (kbps + 6) * (1.0 + 0.02 * (s - 1));
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_split = s;
+            best_kbps = kbps;
+        }
+    }
+    p.split = best_split;
+    p.kb_per_split = best_kbps;
     return p;
 }
 
-size_t tc_workspace_bytes(const TcPlan&, int, int) { return 0; }
+size_t tc_workspace_bytes(const TcPlan& p, int B, int N) {
+    return split_workspace_bytes(p.split, B, N);
+}
 
-cudaError_t launch_tc(const TcPlan&, const void*, const void*, const void*, bool, void*, int, int,
-                      int, void*, unsigned int*, cudaStream_t) {
-    return cudaErrorNotSupported;
+cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
+                           bool has_zeros, void* y, int B, int K, int N, void* workspace,
+                           unsigned int* status, int force_timeout_ms, cudaStream_t stream) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    CUtensorMap xmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)B};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)p.bn};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    Args a;
+    a.packed = static_cast<const uint8_t*>(packed);
+    a.scales = static_cast<const uint16_t*>(scales);
+    a.zeros = reinterpret_cast<const uint32_t*>(static_cast<const char*>(packed) +
+                                                packed_code_bytes(K, N));
+    a.y = static_cast<uint16_t*>(y);
+    a.partial = ws_partials(workspace);
+    a.counters = ws_counters(workspace);
+    a.status = status;
+    a.B = B;
+    a.K = K;
+    a.N = N;
+    a.bn = p.bn;
+    a.kb_per_split = p.kb_per_split;
+    a.split = p.split;
+    a.nkb = K / kBlockK;
+    a.tmem_cols = tmem_cols_for(p.bn);
+    a.force_timeout = force_timeout_ms;
+
+    const size_t smem = smem_bytes(p.bn);
+    const void* kern = has_zeros ? reinterpret_cast<const void*>(tc_kernel<true>)
+                                 : reinterpret_cast<const void*>(tc_kernel<false>);
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    void* args[] = {&xmap, &a};
+    return launch_with_pdl(kern, dim3(p.col_tiles, p.batch_tiles, p.split), dim3(kThreads), smem,
+                           stream, args);
+}
+
+cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
+                      bool has_zeros, void* y, int B, int K, int N, void* workspace,
+                      unsigned int* status, cudaStream_t stream) {
+    return launch_tc_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status, 0,
+                          stream);
 }
 
 }  // namespace w4a16
