@@ -276,7 +276,7 @@ def run_gpu(args, gemms, rank, world, device):
     assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
 
     if args.per_gemm:
-        per_gemm_table(gemms, layers, ws, stream, device, hbm)
+        per_gemm_table(gemms, layers, ws, stream, device, load_peaks()[0])
     # end to end through the public API with host buffers
     e2e = run_e2e(args, gemms, layers, device, ws, pick)
     return ms, clk.summary(), paths, n_copies, e2e
