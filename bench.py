@@ -308,13 +308,13 @@ def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200):
             for r in range(reps):
                 packed, sc = reps_list[r % len(reps_list)]
                 w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream)
-        for _ in range(2):
-            g.replay()
-        stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
         e1.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
         byts = model.linear_bytes(B, K, N, zp)

@@ -139,6 +139,20 @@ int w4a16_select_path(int B, int K, int N);
  * itself fails. */
 w4a16_status w4a16_device_status(int clear);
 
+/* Test hook for the bounded waits of the tensor-core kernel (no counterpart
+ * on the pages).  Launches the tensor-core kernel on a valid problem (same
+ * arguments and rules as w4a16_gemm_path with W4A16_PATH_TCGEN05), but its
+ * MMA thread first waits on a barrier that nothing ever arrives at, limited
+ * to wait_ms milliseconds (1..10000).  The wait expires, the kernel records
+ * W4A16_ERR_TIMEOUT in the device status word (read it with
+ * w4a16_device_status), lets its in-flight copies land, frees its tensor
+ * memory and returns without writing y.  The CUDA context stays usable.
+ * Returns W4A16_ERR_UNSUPPORTED where the tensor-core kernel is unavailable. */
+w4a16_status w4a16_debug_forced_timeout(const void *x, const void *packed, const void *scales,
+                                        int has_zeros, void *y, int B, int K, int N,
+                                        int group_size, void *workspace, size_t ws_bytes,
+                                        int wait_ms, void *stream);
+
 /* Static description of a status code; never NULL. */
 const char *w4a16_status_string(w4a16_status status);
 

@@ -194,3 +194,43 @@ def test_runs_on_a_side_stream():
         y = w.w4a16_gemm(p.x, packed, p.scales, False)
     s.synchronize()
     assert_within_bound(y.cpu(), p.to("cpu"))
+
+
+def test_workspace_validation_on_tensor_core_split():
+    """A tensor-core shape that splits K needs workspace: missing / too small."""
+    B, K, N = 64, 4096, 4096
+    need = w.w4a16_workspace_bytes(B, K, N)
+    if w.PATH_TCGEN05 not in available_paths() or need == 0:
+        pytest.skip("no split-K tensor-core plan for this shape on this device")
+    lib = w.load()
+    p = inputs.make_problem(B, K, N, seed=12).to("cuda")
+    packed = w.w4a16_pack(p.qweight)
+    y = torch.empty((B, N), dtype=torch.bfloat16, device="cuda")
+    args = (p.x.data_ptr(), packed.data_ptr(), p.scales.data_ptr(), 0, y.data_ptr(), B, K, N, 128)
+    assert lib.w4a16_gemm_path(*args, None, 0, w.PATH_TCGEN05, None) == 1          # NULL
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    assert lib.w4a16_gemm_path(*args, ws.data_ptr(), need - 1, w.PATH_TCGEN05, None) == 5  # WORKSPACE
+    assert lib.w4a16_gemm_path(*args, ws.data_ptr(), need, w.PATH_TCGEN05, None) == 0
+    torch.cuda.synchronize()
+    assert_within_bound(y.cpu(), p.to("cpu"), cols=sample_columns(N, 64))
+
+
+def test_bounded_wait_expires_cleanly_and_context_survives():
+    """A wait that nothing satisfies expires after ~50 ms: the status word says
+    TIMEOUT, y is untouched, and the next GEMM on the same context is correct."""
+    if w.PATH_TCGEN05 not in available_paths():
+        pytest.skip("tensor-core kernel unavailable")
+    assert w.w4a16_device_status(clear=True) == 0
+    B, K, N = 64, 1024, 256
+    p = inputs.make_problem(B, K, N, seed=13).to("cuda")
+    packed = w.w4a16_pack(p.qweight)
+    y = torch.full((B, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    assert w.w4a16_debug_forced_timeout(p.x, packed, p.scales, False, y, wait_ms=50) == 0
+    torch.cuda.synchronize()
+    assert w.w4a16_device_status(clear=True) == 7
+    assert torch.all(y == 7.0)
+    assert w.w4a16_device_status(clear=False) == 0
+    y2 = w.w4a16_gemm(p.x, packed, p.scales, False, path=w.PATH_TCGEN05)
+    torch.cuda.synchronize()
+    assert w.w4a16_device_status() == 0
+    assert_within_bound(y2.cpu(), p.to("cpu"))

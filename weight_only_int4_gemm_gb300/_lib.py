@@ -35,6 +35,7 @@ SIGNATURES = {
     "w4a16_gemm_path": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_dequant_ref": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
     "w4a16_select_path": (_I, [_I, _I, _I]),
+    "w4a16_debug_forced_timeout": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_device_status": (_I, [_I]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -186,6 +187,23 @@ def w4a16_dequant_ref(packed: torch.Tensor, scales: torch.Tensor, has_zeros: boo
         packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0, out.data_ptr(), K, N,
         GROUP, _stream(stream)))
     return out
+
+
+def w4a16_debug_forced_timeout(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                               has_zeros: bool, out: torch.Tensor, wait_ms: int,
+                               workspace: torch.Tensor | None = None, stream=None) -> int:
+    """Run the tensor-core kernel with one wait that must expire (test hook);
+    returns the launch status (the device status word then reads TIMEOUT)."""
+    B, K = x.shape
+    N = scales.shape[1]
+    need = w4a16_workspace_bytes(B, K, N)
+    if workspace is None:
+        workspace = _default_ws.get(need, x.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(load().w4a16_debug_forced_timeout(
+        x.data_ptr(), packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0,
+        out.data_ptr(), B, K, N, GROUP, ws_ptr, ws_bytes, int(wait_ms), _stream(stream)))
 
 
 def w4a16_device_status(clear: bool = True) -> int:

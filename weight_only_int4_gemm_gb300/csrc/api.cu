@@ -72,7 +72,7 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 
 w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, int has_zeros,
                        void* y, int B, int K, int N, int group_size, void* workspace,
-                       size_t ws_bytes, int path, void* stream) {
+                       size_t ws_bytes, int path, void* stream, int forced_timeout_ms = 0) {
     if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
     if (!shape_ok(K, N) || B < 1 || B > kMaxB) return W4A16_ERR_SHAPE;
     if (!x || !packed || !scales || !y) return W4A16_ERR_NULL;
@@ -94,6 +94,10 @@ w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, in
     unsigned int* status = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_device_status) != cudaSuccess)
         return W4A16_ERR_CUDA;
+    if (forced_timeout_ms > 0)
+        return from_cuda(launch_tc_forced_timeout(plan_tc(B, K, N, num_sms()), x, packed, scales,
+                                                  has_zeros != 0, y, B, K, N, workspace, status,
+                                                  forced_timeout_ms, s));
     return from_cuda(launch_tc(plan_tc(B, K, N, num_sms()), x, packed, scales, has_zeros != 0,
                                y, B, K, N, workspace, status, s));
 }
@@ -169,6 +173,15 @@ w4a16_status w4a16_dequant_ref(const void* packed, const void* scales, int has_z
     if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return W4A16_ERR_ALIGN;
     return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_debug_forced_timeout(const void* x, const void* packed, const void* scales,
+                                        int has_zeros, void* y, int B, int K, int N,
+                                        int group_size, void* workspace, size_t ws_bytes,
+                                        int wait_ms, void* stream) {
+    if (wait_ms < 1 || wait_ms > 10000) return W4A16_ERR_UNSUPPORTED;
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     W4A16_PATH_TCGEN05, stream, wait_ms);
 }
 
 int w4a16_select_path(int B, int K, int N) {

@@ -67,6 +67,10 @@ size_t tc_workspace_bytes(const TcPlan& p, int B, int N);
 cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
                       bool has_zeros, void* y, int B, int K, int N, void* workspace,
                       unsigned int* status, cudaStream_t stream);
+cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void* packed,
+                                     const void* scales, bool has_zeros, void* y, int B, int K,
+                                     int N, void* workspace, unsigned int* status, int wait_ms,
+                                     cudaStream_t stream);
 bool tc_available();
 
 }  // namespace w4a16

@@ -512,7 +512,7 @@ size_t tc_workspace_bytes(const TcPlan& p, int B, int N) {
     return split_workspace_bytes(p.split, B, N);
 }
 
-cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
+static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
                            bool has_zeros, void* y, int B, int K, int N, void* workspace,
                            unsigned int* status, int force_timeout_ms, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
@@ -562,6 +562,14 @@ cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const 
                       unsigned int* status, cudaStream_t stream) {
     return launch_tc_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status, 0,
                           stream);
+}
+
+cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void* packed,
+                                     const void* scales, bool has_zeros, void* y, int B, int K,
+                                     int N, void* workspace, unsigned int* status, int wait_ms,
+                                     cudaStream_t stream) {
+    return launch_tc_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
+                          wait_ms, stream);
 }
 
 }  // namespace w4a16
