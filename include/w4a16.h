@@ -56,7 +56,7 @@ extern "C" {
 #endif
 
 #define W4A16_GROUP 128
-#define W4A16_PACKED_LAYOUT 1 /* version tag of the packed blob's layout */
+#define W4A16_PACKED_LAYOUT 2 /* version tag of the packed blob's layout */
 
 typedef enum {
     W4A16_OK = 0,

@@ -71,8 +71,13 @@ def test_gemm_validation(lib):
     assert _gemm(lib, x=FAKE + 8) == ERR_ALIGN
     assert _gemm(lib, scales=FAKE + 2) == ERR_ALIGN
     assert _gemm(lib, path=7) == ERR_UNSUP
-    # the small-batch kernel reduces split-K on chip: it needs no workspace
-    assert lib.w4a16_workspace_bytes(1, 4096, 4096, 128) == 0
+    # a shape that splits K needs workspace: missing / too small / misaligned
+    B, K, N = 1, 4096, 4096
+    need = lib.w4a16_workspace_bytes(B, K, N, 128)
+    assert need > 0
+    assert _gemm(lib, B=B, K=K, N=N, path=0) == ERR_NULL
+    assert _gemm(lib, B=B, K=K, N=N, ws=FAKE, ws_bytes=need - 1, path=0) == ERR_WS
+    assert _gemm(lib, B=B, K=K, N=N, ws=FAKE + 4, ws_bytes=need, path=0) == ERR_ALIGN
     # without a tensor-core device the forced tensor-core path is refused
     assert _gemm(lib, B=64, K=4096, N=4096, path=1) == ERR_UNSUP
     assert lib.w4a16_debug_forced_timeout(FAKE, FAKE, FAKE, 0, FAKE, 64, 4096, 4096, 128,

@@ -45,6 +45,22 @@ DeviceInfo device_info() {
     return info;
 }
 
+// Device address of the status word on the current device (cached per device).
+unsigned int* device_status_word() {
+    static std::mutex mu;
+    static std::unordered_map<int, unsigned int*> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    unsigned int* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_device_status) != cudaSuccess)
+        return nullptr;
+    cache[dev] = p;
+    return p;
+}
+
 int num_sms() {
     const int s = device_info().sms;
     return s > 0 ? s : 152;
@@ -88,12 +104,11 @@ w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, in
         if (ws_bytes < need) return W4A16_ERR_WORKSPACE;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_status_word();
+    if (status == nullptr) return W4A16_ERR_CUDA;
     if (path == W4A16_PATH_SKINNY)
         return from_cuda(launch_skinny(plan_skinny(B, K, N, num_sms()), x, packed, scales,
-                                       has_zeros != 0, y, B, K, N, workspace, s));
-    unsigned int* status = nullptr;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_device_status) != cudaSuccess)
-        return W4A16_ERR_CUDA;
+                                       has_zeros != 0, y, B, K, N, workspace, status, s));
     if (forced_timeout_ms > 0)
         return from_cuda(launch_tc_forced_timeout(plan_tc(B, K, N, num_sms()), x, packed, scales,
                                                   has_zeros != 0, y, B, K, N, workspace, status,

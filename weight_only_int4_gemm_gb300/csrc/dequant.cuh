@@ -9,12 +9,16 @@
 // multiply by the group scale then gives w = RNE_bf16((q - z) * s).  One
 // lop3 builds two such values at once, one in each 16-bit half.
 //
-// Packed layout (version W4A16_PACKED_LAYOUT = 1):
-//   codes: uint32 [K/32][N][4].  The 16 bytes at chunk c, column n hold the
-//   32 codes of rows k = 32c .. 32c+31 of column n; word j holds rows
-//   32c + 8j .. 32c + 8j + 7.  Inside a word, the codes of rows (2i, 2i+1)
-//   (offsets within the word) sit in nibbles i and i + 4, i.e. in the low and
-//   high 16-bit halves at the same bit offset 4i, so
+// Packed layout (version W4A16_PACKED_LAYOUT = 2):
+//   codes: the N columns are cut into tiles of 128 (the last tile holds
+//   w = N - 128*t columns when N is not a multiple of 128).  Tile t starts at
+//   byte 64*K*t; inside it, chunk c (rows 32c .. 32c+31) is w consecutive
+//   16-byte entries, one per column, so every (tile, run of chunks) is one
+//   contiguous block -- a single bulk copy.  The 16 bytes of (chunk c,
+//   column n) hold the 32 codes of rows 32c .. 32c+31 of column n; word j
+//   holds rows 32c + 8j .. 32c + 8j + 7.  Inside a word, the codes of rows
+//   (2i, 2i+1) (offsets within the word) sit in nibbles i and i + 4, i.e. in
+//   the low and high 16-bit halves at the same bit offset 4i, so
 //        (word >> 4i) & 0x000F000F  ==  { code(2i), code(2i+1) }.
 //   zeros (asymmetric format only): the canonical uint32 [K/128][N/8] array,
 //   copied unchanged after the codes.
@@ -24,6 +28,25 @@
 #include <stdint.h>
 
 namespace w4a16 {
+
+constexpr int kPackTileCols = 128;
+
+// Width of column tile t.
+__host__ __device__ inline int packed_tile_width(int N, int t) {
+    return N - kPackTileCols * t < kPackTileCols ? N - kPackTileCols * t : kPackTileCols;
+}
+
+// Byte offset of tile t's block of codes.
+__host__ __device__ inline size_t packed_tile_base(int K, int t) {
+    return (size_t)64 * (size_t)K * (size_t)t;
+}
+
+// Index, in 16-byte units, of (chunk c, column n).
+__host__ __device__ inline size_t packed_index16(int K, int N, int c, int n) {
+    const int t = n / kPackTileCols;
+    return packed_tile_base(K, t) / 16 + (size_t)c * packed_tile_width(N, t) +
+           (size_t)(n - kPackTileCols * t);
+}
 
 // Nibble position of row offset r (0..7) inside a packed word.
 __host__ __device__ constexpr int packed_nibble_of_row(int r) {

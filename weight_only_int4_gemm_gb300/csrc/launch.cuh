@@ -40,19 +40,21 @@ cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K
 cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,
                                int K, int N, cudaStream_t stream);
 
-// ---- small-batch split-K kernel (skinny.cu) ----
+// ---- small-batch streaming kernel (skinny.cu) ----
 struct SkinnyPlan {
-    int nt;            // n8 batch tiles per CTA pass: 1, 2 or 4 (8, 16 or 32 rows)
+    int nt;            // n8 batch tiles per unit: 1, 2 or 4 (8, 16 or 32 rows)
     int batch_chunks;  // ceil(B / (8 * nt))
-    int col_blocks;    // ceil(N / columns per CTA)
+    int col_blocks;    // column tiles of 128
     int gps;           // groups of 128 rows per K split
     int split;         // number of K splits (1 = no workspace)
+    int units;         // batch_chunks * col_blocks * split
+    int grid;          // persistent CTAs
 };
 SkinnyPlan plan_skinny(int B, int K, int N, int num_sms);
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N);
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
                           const void* scales, bool has_zeros, void* y, int B, int K, int N,
-                          void* workspace, cudaStream_t stream);
+                          void* workspace, unsigned int* status, cudaStream_t stream);
 
 // ---- tcgen05 tensor-core kernel (tc_gemm.cu) ----
 struct TcPlan {

@@ -13,7 +13,7 @@ constexpr int kPackThreads = 256;
 // One thread per (chunk c, column n): gathers the four canonical words of rows
 // 32c .. 32c+31 of column n and moves every code to its packed nibble.
 __global__ void __launch_bounds__(kPackThreads)
-repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, int N) {
+repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, int K, int N) {
     const int n = blockIdx.x * kPackThreads + threadIdx.x;
     const int c = blockIdx.y;
     if (n >= N) return;
@@ -26,7 +26,7 @@ repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, 
         for (int r = 0; r < 8; ++r) p |= ((w >> (4 * r)) & 0xFu) << (4 * packed_nibble_of_row(r));
         out[j] = p;
     }
-    packed[(size_t)c * N + n] = make_uint4(out[0], out[1], out[2], out[3]);
+    packed[packed_index16(K, N, c, n)] = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // One thread per (chunk c, column n): decodes 32 weights with the shared
@@ -34,12 +34,12 @@ repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, 
 template <bool kHasZeros>
 __global__ void __launch_bounds__(kPackThreads)
 dequant_ref_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict__ scales,
-                   const uint32_t* __restrict__ zeros, uint16_t* __restrict__ w, int N) {
+                   const uint32_t* __restrict__ zeros, uint16_t* __restrict__ w, int K, int N) {
     const int n = blockIdx.x * kPackThreads + threadIdx.x;
     const int c = blockIdx.y;
     if (n >= N) return;
     const int g = c >> 2;  // 4 chunks of 32 rows per group of 128
-    const uint4 q = packed[(size_t)c * N + n];
+    const uint4 q = packed[packed_index16(K, N, c, n)];
     const uint32_t s2 = scale_pair(__ldg(scales + (size_t)g * N + n));
     const uint32_t z2 = kHasZeros ? zero_pair(load_zero(zeros, N, g, n)) : kSymmetricZeroPair;
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};
@@ -61,7 +61,7 @@ dequant_ref_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict_
 cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K, int N,
                           void* packed, cudaStream_t stream) {
     dim3 grid((N + kPackThreads - 1) / kPackThreads, K / 32);
-    repack_kernel<<<grid, kPackThreads, 0, stream>>>(qweight, static_cast<uint4*>(packed), N);
+    repack_kernel<<<grid, kPackThreads, 0, stream>>>(qweight, static_cast<uint4*>(packed), K, N);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || qzeros == nullptr) return err;
     const size_t zero_bytes = (size_t)(K / 128) * (size_t)(N / 8) * 4;
@@ -78,9 +78,9 @@ cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_
                                                           packed_code_bytes(K, N));
     uint16_t* out = static_cast<uint16_t*>(w);
     if (has_zeros)
-        dequant_ref_kernel<true><<<grid, kPackThreads, 0, stream>>>(p, s, z, out, N);
+        dequant_ref_kernel<true><<<grid, kPackThreads, 0, stream>>>(p, s, z, out, K, N);
     else
-        dequant_ref_kernel<false><<<grid, kPackThreads, 0, stream>>>(p, s, nullptr, out, N);
+        dequant_ref_kernel<false><<<grid, kPackThreads, 0, stream>>>(p, s, nullptr, out, K, N);
     return cudaGetLastError();
 }
 

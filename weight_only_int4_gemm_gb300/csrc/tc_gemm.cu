@@ -281,8 +281,9 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // ---------------- TMA producer
         if (lane == 0) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            const uint32_t raw_chunk = (uint32_t)nvalid * 16;
-            const uint32_t tx = 2 * raw_chunk + (uint32_t)a.bn * kBlockK * 2;
+            const uint32_t raw_block = 2u * (uint32_t)nvalid * 16;  // two 32-row chunks
+            const uint32_t tx = raw_block + (uint32_t)a.bn * kBlockK * 2;
+            const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, col_tile);
             int issued = 0;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % kSlots;
@@ -293,10 +294,8 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 const uint32_t bar = smem_u32(&tail->full_tma[s]);
                 const int kb = kb_begin + i;
                 mbar_arrive_expect_tx(bar, tx);
-                const uint8_t* src0 = a.packed + ((size_t)(2 * kb) * a.N + n0) * 16;
-                const uint8_t* src1 = a.packed + ((size_t)(2 * kb + 1) * a.N + n0) * 16;
-                bulk_g2s(smem_u32(raw_tile(s)), src0, raw_chunk, bar);
-                bulk_g2s(smem_u32(raw_tile(s)) + kTileN * 16, src1, raw_chunk, bar);
+                bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * nvalid * 16,
+                         raw_block, bar);
                 tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, b0, bar);
                 issued = i + 1;
             }
@@ -352,7 +351,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             const bool landed = wait_bounded(smem_u32(&tail->full_tma[s]), (i / kSlots) & 1,
                                              abort, a.status, kTimeoutNs);
             if (!__all_sync(0xffffffffu, landed)) break;  // warp-uniform exit
-            const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * kTileN + r];
+            const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * nvalid + r];
             const uint32_t words[4] = {q.x, q.y, q.z, q.w};
             uint8_t* row = a_tile(s) + r * 128;
 #pragma unroll
