@@ -6,7 +6,7 @@
 #include <mutex>
 #include <unordered_map>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 #include "launch.cuh"
 
 namespace w4a16 {

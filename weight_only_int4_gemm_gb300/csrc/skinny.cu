@@ -21,10 +21,14 @@
 //    free, so each lane's four k values per step are consecutive rows of its
 //    own 32-row chunk; the activations are staged in exactly that fragment
 //    order, which makes each fragment load one 16-byte read;
-//  * work units are (batch chunk, column tile, K split); a K split writes
-//    fp32 partials to the workspace and the last unit of a tile to finish
-//    (arrival counter) sums them in a fixed order -- deterministic, no second
-//    launch, no waiting on other CTAs;
+//  * work units are (batch chunk, column tile, K split), handed out
+//    dynamically (the first unit of each CTA is fixed, later ones come from an
+//    atomic work counter), so slow and fast SMs even out;
+//  * a dedicated epilogue warp takes each finished unit's accumulators from
+//    shared memory and writes y -- or, for a K split, fp32 partials, the last
+//    unit of a tile to finish (arrival counter) summing them in a fixed order
+//    (deterministic, no second launch) -- while the consumers already work on
+//    the next unit;
 //  * programmatic dependent launch: the first ring slots' weight copies are
 //    issued before waiting for the previous kernel on the stream, so
 //    consecutive layers' weight streams overlap.
@@ -41,20 +45,25 @@ namespace w4a16 {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);  // 288
+constexpr int kThreads = 32 * (2 + kConsumerWarps);  // 320
 constexpr int kTileCols = kPackTileCols;             // 128 columns per tile
 constexpr int kSlotGroups = 2;                       // 128-row groups per ring slot
 constexpr uint32_t kSlotCodeBytes = kSlotGroups * 4 * kTileCols * 16;  // 16 KB
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr unsigned int kStatusTimeout = 7;           // W4A16_ERR_TIMEOUT
+constexpr int kWorkCounter = kMaxCounters - 2;       // workspace words used by the scheduler
+constexpr int kDoneCounter = kMaxCounters - 1;
 
-template <int NT> constexpr int ring_slots() { return NT >= 4 ? 6 : 4; }
+template <int NT> constexpr int ring_slots() { return NT == 1 ? 4 : (NT == 2 ? 3 : 5); }
+template <int NT> constexpr int ctas_per_sm_t() { return NT >= 4 ? 1 : 2; }
 template <int NT> constexpr uint32_t slot_x_bytes() { return kSlotGroups * 16 * 8 * NT * 16; }
 constexpr uint32_t kSlotScaleBytes = kSlotGroups * kTileCols * 2;  // 512
 constexpr uint32_t kSlotZeroBytes = kSlotGroups * kTileCols / 2;   // 128
 template <int NT> constexpr uint32_t slot_bytes() {
     return kSlotCodeBytes + slot_x_bytes<NT>() + kSlotScaleBytes + kSlotZeroBytes;
 }
+// accumulators of one unit: [warp][bt][i][lane]
+template <int NT> constexpr uint32_t result_bytes() { return kConsumerWarps * NT * 4 * 32 * 4; }
 
 struct Args {
     const uint16_t* x;
@@ -63,7 +72,7 @@ struct Args {
     const uint32_t* zeros;
     uint16_t* y;
     float* partial;      // [split][B][N]   (split > 1)
-    uint32_t* counters;  // [batch_chunks][tiles] (fixed workspace prefix)
+    uint32_t* counters;  // fixed workspace prefix: per-tile arrivals + scheduler words
     unsigned int* status;
     int B, K, N;
     int tiles, split, gps, units;
@@ -72,8 +81,12 @@ struct Args {
 struct Tail {
     uint64_t full[8];
     uint64_t empty[8];
+    uint64_t res_full[2];
+    uint64_t res_empty[2];
+    int slot_unit[8];    // unit of each ring slot (-1: no more work)
+    int slot_step[8];    // step of the unit held by the slot
+    int res_unit[2];
     int abort;
-    int is_last;
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -100,6 +113,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Bounded wait; false when this CTA is aborting or the wait expired (then it
+// sets the abort flag and the device status word).
 __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                           unsigned int* status) {
     const unsigned long long t0 = globaltimer();
@@ -114,14 +129,24 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// 16- or 4-byte asynchronous copy global -> shared; src_bytes = 0 zero-fills.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
+// warp-uniform bounded wait
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* status) {
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, status));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -138,13 +163,9 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
-__device__ __forceinline__ void consumer_bar() {  // the 8 consumer warps only
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
-}
-
-// Work unit u -> (batch chunk, tile, split index).
+// Work unit u -> (batch chunk, tile, split index) and its extents.
 struct Unit {
-    int bc, tile, sk, g_begin, ng, n0, width, b0, rows;
+    int bc, tile, sk, g_begin, ng, n0, width, b0, rows, nsteps;
 };
 
 template <int NT>
@@ -155,24 +176,26 @@ __device__ __forceinline__ Unit decode_unit(const Args& a, int u) {
     const int rest = u / a.split;
     w.tile = rest % a.tiles;
     w.bc = rest / a.tiles;
-    const int G = a.K / kGroup;
     w.g_begin = w.sk * a.gps;
-    w.ng = min(a.gps, G - w.g_begin);
+    w.ng = min(a.gps, a.K / kGroup - w.g_begin);
     w.n0 = w.tile * kTileCols;
     w.width = packed_tile_width(a.N, w.tile);
     w.b0 = w.bc * kRows;
     w.rows = min(kRows, a.B - w.b0);
+    w.nsteps = (w.ng + kSlotGroups - 1) / kSlotGroups;
     return w;
 }
 
 // ------------------------------------------------------------ kernel
 
 template <int NT, bool kHasZeros>
-__global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm_t<NT>())
+skinny_kernel(const Args a) {
     constexpr int kRows = 8 * NT;
     constexpr int S = ring_slots<NT>();
     extern __shared__ __align__(128) uint8_t smem[];
-    Tail* tail = reinterpret_cast<Tail*>(smem + S * slot_bytes<NT>());
+    float* res = reinterpret_cast<float*>(smem + S * slot_bytes<NT>());
+    Tail* tail = reinterpret_cast<Tail*>(smem + S * slot_bytes<NT>() + 2 * result_bytes<NT>());
     volatile int* abort = &tail->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -192,11 +215,17 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const Args a) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            // lane 0's expect-tx arrive + one cp.async arrive per producer lane
+            // lane 0's arrive (with the expected bytes) + one cp.async arrive per producer lane
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&tail->full[s])),
                          "r"(33));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&tail->empty[s])),
                          "r"(kConsumerWarps));
+        }
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                         ::"r"(smem_u32(&tail->res_full[b])), "r"(kConsumerWarps));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                         ::"r"(smem_u32(&tail->res_empty[b])), "r"(1));
         }
         tail->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -206,219 +235,268 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const Args a) {
 
     if (warp == 0) {
         // ---------------- producer
-        const int G = a.K / kGroup;
-        (void)G;
-        // pass 0: weight copies of the first S slots, before waiting for the
-        // previous kernel; pass 1: everything else.
-        int issued = 0;    // steps whose copies are all issued
-        int w_issued = 0;  // steps whose code copy is issued
-        for (int pass = 0; pass < 2; ++pass) {
-            if (pass == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
-            int step = 0;
-            bool stop = false;
-            for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
-                const Unit w = decode_unit<NT>(a, u);
-                const int nsteps = (w.ng + kSlotGroups - 1) / kSlotGroups;
-                const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, w.tile);
-                for (int st = 0; st < nsteps; ++st, ++step) {
-                    if (pass == 0 && step >= S) {
-                        stop = true;
-                        break;
-                    }
-                    const int s = step % S;
-                    const int g0 = w.g_begin + st * kSlotGroups;
-                    const int ngs = min(kSlotGroups, w.g_begin + w.ng - g0);
-                    const uint32_t full = smem_u32(&tail->full[s]);
-                    const bool weights_now = (pass == 0) || step >= S;
-                    if (pass == 1 && step >= S) {
-                        const bool ok = wait_bounded(smem_u32(&tail->empty[s]),
-                                                     ((step / S) - 1) & 1, abort, a.status);
-                        if (!__all_sync(0xffffffffu, ok)) {
-                            stop = true;
-                            break;
-                        }
-                    }
-                    if (weights_now && lane == 0) {
-                        const uint32_t bytes = (uint32_t)ngs * 4 * w.width * 16;
-                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                                     ::"r"(full), "r"(bytes)
-                                     : "memory");
-                        asm volatile(
-                            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-                            "[%0], [%1], %2, [%3];"
-                            ::"r"(smem_u32(slot_codes(s))),
-                            "l"(tile_codes + (size_t)(4 * g0) * w.width * 16), "r"(bytes),
-                            "r"(full)
-                            : "memory");
-                    }
-                    if (weights_now) w_issued = step + 1;
-                    if (pass == 1) {
-                        // activations in fragment order: piece (gl, r, p) of
-                        // x[b0 + r][128*(g0+gl) + 8p .. +8], zero-filled past B
-                        const uint32_t xbase = smem_u32(slot_x(s));
-                        const int rows_alloc = ((w.rows + 7) / 8) * 8;
-                        const int total = ngs * 16 * rows_alloc;
-                        for (int e = lane; e < total; e += 32) {
-                            const int p = e & 15;
-                            const int r = (e >> 4) % rows_alloc;
-                            const int gl = (e >> 4) / rows_alloc;
-                            const bool valid = r < w.rows;
-                            const uint16_t* src = a.x + (size_t)(w.b0 + (valid ? r : 0)) * a.K +
-                                                  (size_t)kGroup * (g0 + gl) + 8 * p;
-                            cp_async_16(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
-                                        src, valid ? 16u : 0u);
-                        }
-                        // scales: ngs rows of `width` bf16, 16-byte pieces
-                        const int spr = w.width / 8;
-                        for (int e = lane; e < ngs * spr; e += 32) {
-                            const int gl = e / spr, j = e - gl * spr;
-                            cp_async_16(smem_u32(slot_scales(s)) + 2u * (gl * kTileCols + 8 * j),
-                                        a.scales + (size_t)(g0 + gl) * a.N + w.n0 + 8 * j, 16u);
-                        }
-                        if (kHasZeros) {
-                            for (int e = lane; e < ngs * spr; e += 32) {
-                                const int gl = e / spr, j = e - gl * spr;
-                                cp_async_4(smem_u32(slot_zeros(s)) + 4u * (gl * (kTileCols / 8) + j),
-                                           a.zeros + (size_t)(g0 + gl) * (a.N / 8) + w.n0 / 8 + j);
-                            }
-                        }
-                        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
-                                     ::"r"(full)
-                                     : "memory");
-                        issued = step + 1;
-                    }
-                }
+        uint64_t evict_first;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+        int step = 0;        // ring position
+        int issued = 0;      // ring positions fully issued
+        int w_issued = 0;    // ring positions whose code copy is issued
+        bool ok = true;
+        // The first unit is fixed (blockIdx.x): its first slots' code copies go
+        // out before waiting for the previous kernel on the stream.
+        const Unit first = decode_unit<NT>(a, blockIdx.x);
+        const uint8_t* first_codes = a.packed + packed_tile_base(a.K, first.tile);
+        auto issue_codes = [&](const Unit& w, const uint8_t* tile_codes, int st, int pos) {
+            const int s = pos % S;
+            const int g0 = w.g_begin + st * kSlotGroups;
+            const int ngs = min(kSlotGroups, w.g_begin + w.ng - g0);
+            const uint32_t bytes = (uint32_t)ngs * 4 * w.width * 16;
+            const uint32_t full = smem_u32(&tail->full[s]);
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full),
+                         "r"(bytes)
+                         : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+                "[%0], [%1], %2, [%3], %4;"
+                ::"r"(smem_u32(slot_codes(s))), "l"(tile_codes + (size_t)(4 * g0) * w.width * 16),
+                "r"(bytes), "r"(full), "l"(evict_first)
+                : "memory");
+        };
+        const int pre = min(S, first.nsteps);
+        if (lane == 0) {
+            for (int st = 0; st < pre; ++st) {
+                tail->slot_unit[st] = blockIdx.x;
+                tail->slot_step[st] = st;
+                issue_codes(first, first_codes, st, st);
             }
         }
-        // Every copy into the ring must land before the CTA exits.  Steps whose
-        // code copy went out early but whose other copies were never issued
-        // (only after an expired wait) get their missing arrivals here.
+        w_issued = pre;
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+
+        int u = blockIdx.x;
+        uint32_t* work = a.counters + kWorkCounter;
+        while (ok) {
+            const Unit w = decode_unit<NT>(a, u);
+            const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, w.tile);
+            for (int st = 0; st < w.nsteps; ++st, ++step) {
+                const int s = step % S;
+                const uint32_t full = smem_u32(&tail->full[s]);
+                if (step >= w_issued) {
+                    if (step >= S && !warp_wait(smem_u32(&tail->empty[s]), ((step / S) - 1) & 1,
+                                                abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tail->slot_unit[s] = u;
+                        tail->slot_step[s] = st;
+                        issue_codes(w, tile_codes, st, step);
+                    }
+                    w_issued = step + 1;
+                }
+                // activations (valid rows only), scales, zero-points
+                const int g0 = w.g_begin + st * kSlotGroups;
+                const int ngs = min(kSlotGroups, w.g_begin + w.ng - g0);
+                const uint32_t xbase = smem_u32(slot_x(s));
+                const int p = lane & 15;
+                for (int gl = 0; gl < ngs; ++gl)
+                    for (int r = lane >> 4; r < w.rows; r += 2)
+                        cp_async_16(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
+                                    a.x + (size_t)(w.b0 + r) * a.K + (size_t)kGroup * (g0 + gl) + 8 * p);
+                const int gl = lane >> 4;
+                if (gl < ngs && p < w.width / 8) {
+                    cp_async_16(smem_u32(slot_scales(s)) + 2u * (gl * kTileCols + 8 * p),
+                                a.scales + (size_t)(g0 + gl) * a.N + w.n0 + 8 * p);
+                    if (kHasZeros)
+                        cp_async_4(smem_u32(slot_zeros(s)) + 4u * (gl * (kTileCols / 8) + p),
+                                   a.zeros + (size_t)(g0 + gl) * (a.N / 8) + w.n0 / 8 + p);
+                }
+                cp_async_arrive_noinc(full);
+                issued = step + 1;
+            }
+            if (!ok) break;
+            // next unit from the work counter (units [0, grid) are the fixed first ones)
+            int next = 0;
+            if (lane == 0) next = (int)gridDim.x + (int)atomicAdd(work, 1u);
+            next = __shfl_sync(0xffffffffu, next, 0);
+            if (next >= a.units) {
+                if (lane == 0) {
+                    // the last CTA to run out of work resets the scheduler words
+                    const uint32_t done = atomicAdd(a.counters + kDoneCounter, 1u);
+                    if (done == gridDim.x - 1) {
+                        a.counters[kWorkCounter] = 0u;
+                        a.counters[kDoneCounter] = 0u;
+                    }
+                }
+                break;
+            }
+            u = next;
+        }
+        // end marker for the consumers
+        if (ok) {
+            const int s = step % S;
+            if (step < S || warp_wait(smem_u32(&tail->empty[s]), ((step / S) - 1) & 1, abort,
+                                      a.status)) {
+                if (lane == 0) {
+                    tail->slot_unit[s] = -1;
+                    mbar_arrive(smem_u32(&tail->full[s]));
+                }
+                cp_async_arrive_noinc(smem_u32(&tail->full[s]));
+            }
+        }
+        // every copy into the ring must land before the CTA exits
         for (int i = max(0, w_issued - S); i < w_issued; ++i) {
             const uint32_t full = smem_u32(&tail->full[i % S]);
-            if (i >= issued)
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full)
-                             : "memory");
+            if (i >= issued) cp_async_arrive_noinc(full);
             wait_bounded(full, (i / S) & 1, abort, a.status);
         }
-    } else {
+    } else if (warp <= kConsumerWarps) {
         // ---------------- consumers: warp cw owns columns 16cw .. 16cw+15 of the tile
         const int cw = warp - 1;
         const int gid = lane >> 2;  // mma group id: weight column within 8
         const int tig = lane & 3;   // which 32-row chunk of a group
         const int ca = 16 * cw + gid, cb = ca + 8;  // the two columns of this lane
-        int step = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            const Unit w = decode_unit<NT>(a, u);
-            const int nsteps = (w.ng + kSlotGroups - 1) / kSlotGroups;
-            float acc[NT][4];
-#pragma unroll
-            for (int bt = 0; bt < NT; ++bt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[bt][i] = 0.f;
-
-            for (int st = 0; st < nsteps; ++st, ++step) {
-                const int s = step % S;
-                const bool landed =
-                    wait_bounded(smem_u32(&tail->full[s]), (step / S) & 1, abort, a.status);
-                if (!__all_sync(0xffffffffu, landed)) {
-                    ok = false;
+        float acc[NT][4];
+        int nunit = 0;  // units finished by this CTA
+        for (int step = 0;; ++step) {
+            const int s = step % S;
+            if (!warp_wait(smem_u32(&tail->full[s]), (step / S) & 1, abort, a.status)) break;
+            const int u = tail->slot_unit[s];
+            const int st = tail->slot_step[s];
+            const int buf = nunit & 1;
+            if (u < 0) {
+                // no more work: tell the epilogue warp
+                if (nunit >= 2 && !warp_wait(smem_u32(&tail->res_empty[buf]), ((nunit >> 1) - 1) & 1,
+                                             abort, a.status))
                     break;
+                if (lane == 0) {
+                    if (cw == 0) tail->res_unit[buf] = -1;
+                    mbar_arrive(smem_u32(&tail->res_full[buf]));
                 }
-                const int ngs = min(kSlotGroups, w.ng - st * kSlotGroups);
-                const uint4* codes = reinterpret_cast<const uint4*>(slot_codes(s));
-                const uint4* xs = slot_x(s);
-                const uint16_t* sc = slot_scales(s);
-                const uint32_t* zs = slot_zeros(s);
+                break;
+            }
+            const Unit w = decode_unit<NT>(a, u);
+            if (st == 0) {
 #pragma unroll
-                for (int gl = 0; gl < kSlotGroups; ++gl) {
-                    if (gl < ngs) {
-                        const uint4 qa = codes[(4 * gl + tig) * w.width + min(ca, w.width - 1)];
-                        const uint4 qb = codes[(4 * gl + tig) * w.width + min(cb, w.width - 1)];
-                        const uint32_t sa = scale_pair(sc[gl * kTileCols + ca]);
-                        const uint32_t sb = scale_pair(sc[gl * kTileCols + cb]);
-                        uint32_t za = kSymmetricZeroPair, zb = kSymmetricZeroPair;
-                        if (kHasZeros) {
-                            za = zero_pair((zs[gl * (kTileCols / 8) + (ca >> 3)] >> (4 * (ca & 7))) & 0xFu);
-                            zb = zero_pair((zs[gl * (kTileCols / 8) + (cb >> 3)] >> (4 * (cb & 7))) & 0xFu);
-                        }
-                        const uint32_t wA[4] = {qa.x, qa.y, qa.z, qa.w};
-                        const uint32_t wB[4] = {qb.x, qb.y, qb.z, qb.w};
+                for (int bt = 0; bt < NT; ++bt)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 xf[NT];
+                    for (int i = 0; i < 4; ++i) acc[bt][i] = 0.f;
+            }
+            const int ngs = min(kSlotGroups, w.ng - st * kSlotGroups);
+            const uint4* codes = reinterpret_cast<const uint4*>(slot_codes(s));
+            const uint4* xs = slot_x(s);
+            const uint16_t* sc = slot_scales(s);
+            const uint32_t* zs = slot_zeros(s);
+            const int cla = min(ca, w.width - 1), clb = min(cb, w.width - 1);
+#pragma unroll
+            for (int gl = 0; gl < kSlotGroups; ++gl) {
+                if (gl < ngs) {
+                    const uint4 qa = codes[(4 * gl + tig) * w.width + cla];
+                    const uint4 qb = codes[(4 * gl + tig) * w.width + clb];
+                    const uint32_t sa = scale_pair(sc[gl * kTileCols + cla]);
+                    const uint32_t sb = scale_pair(sc[gl * kTileCols + clb]);
+                    uint32_t za = kSymmetricZeroPair, zb = kSymmetricZeroPair;
+                    if (kHasZeros) {
+                        za = zero_pair((zs[gl * (kTileCols / 8) + (cla >> 3)] >> (4 * (cla & 7))) & 0xFu);
+                        zb = zero_pair((zs[gl * (kTileCols / 8) + (clb >> 3)] >> (4 * (clb & 7))) & 0xFu);
+                    }
+                    const uint32_t wA[4] = {qa.x, qa.y, qa.z, qa.w};
+                    const uint32_t wB[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 xf[NT];
+#pragma unroll
+                        for (int bt = 0; bt < NT; ++bt)
+                            xf[bt] = (bt * 8 + gid < w.rows)  // rows past B are never staged
+                                         ? xs[((gl * 4 + j) * kRows + bt * 8 + gid) * 4 + tig]
+                                         : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            // step 2j + h: rows 4(2j+h) .. +3 of each lane's chunk
+                            const uint32_t a0 = dequant_pair(wA[j], 2 * h, za, sa);
+                            const uint32_t a1 = dequant_pair(wB[j], 2 * h, zb, sb);
+                            const uint32_t a2 = dequant_pair(wA[j], 2 * h + 1, za, sa);
+                            const uint32_t a3 = dequant_pair(wB[j], 2 * h + 1, zb, sb);
 #pragma unroll
                             for (int bt = 0; bt < NT; ++bt)
-                                xf[bt] = xs[((gl * 4 + j) * kRows + bt * 8 + gid) * 4 + tig];
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                // step 2j + h: rows 4(2j+h) .. +3 of each lane's chunk
-                                const uint32_t a0 = dequant_pair(wA[j], 2 * h, za, sa);
-                                const uint32_t a1 = dequant_pair(wB[j], 2 * h, zb, sb);
-                                const uint32_t a2 = dequant_pair(wA[j], 2 * h + 1, za, sa);
-                                const uint32_t a3 = dequant_pair(wB[j], 2 * h + 1, zb, sb);
-#pragma unroll
-                                for (int bt = 0; bt < NT; ++bt)
-                                    if (bt * 8 < w.rows)  // warp-uniform: skip padding tiles
-                                        mma_bf16(acc[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
-                                                 h ? xf[bt].w : xf[bt].y);
-                            }
+                                if (bt * 8 < w.rows)  // warp-uniform: skip padding tiles
+                                    mma_bf16(acc[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
+                                             h ? xf[bt].w : xf[bt].y);
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0)
-                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
-                                 ::"r"(smem_u32(&tail->empty[s]))
-                                 : "memory");
             }
-            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tail->empty[s]));
 
-            // unit output: D row (gid or gid+8) = weight column, D column
-            // (2*tig + (i & 1)) = batch row
+            if (st == w.nsteps - 1) {
+                // unit finished: hand the accumulators to the epilogue warp
+                if (nunit >= 2 && !warp_wait(smem_u32(&tail->res_empty[buf]), ((nunit >> 1) - 1) & 1,
+                                             abort, a.status))
+                    break;
+                float* r = res + buf * (result_bytes<NT>() / 4);
 #pragma unroll
-            for (int bt = 0; bt < NT; ++bt)
+                for (int bt = 0; bt < NT; ++bt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = (i & 2) ? cb : ca;
-                    const int b = bt * 8 + 2 * tig + (i & 1);
-                    if (c < w.width && b < w.rows) {
-                        const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c;
-                        if (a.split == 1)
-                            a.y[off] = f32_to_bf16_rn(acc[bt][i]);
-                        else
-                            a.partial[(size_t)w.sk * a.B * a.N + off] = acc[bt][i];
-                    }
+                    for (int i = 0; i < 4; ++i) r[((cw * NT + bt) * 4 + i) * 32 + lane] = acc[bt][i];
+                __syncwarp();
+                if (lane == 0) {
+                    if (cw == 0) tail->res_unit[buf] = u;
+                    mbar_arrive(smem_u32(&tail->res_full[buf]));
                 }
+                ++nunit;
+            }
+        }
+    } else {
+        // ---------------- epilogue warp: y, or split-K partials + ordered reduction
+        for (int k = 0;; ++k) {
+            const int buf = k & 1;
+            if (!warp_wait(smem_u32(&tail->res_full[buf]), (k >> 1) & 1, abort, a.status)) break;
+            const int u = tail->res_unit[buf];
+            if (u < 0) break;
+            const Unit w = decode_unit<NT>(a, u);
+            const float* r = res + buf * (result_bytes<NT>() / 4);
+            // element (column c, row b) of the unit lives at
+            // r[((c/16 * NT + b/8) * 4 + i) * 32 + lane'], i = 2*((c%16)/8) + b%2,
+            // lane' = 4*(c%8) + (b%8)/2
+            for (int b = 0; b < w.rows; ++b) {
+                for (int c = lane; c < w.width; c += 32) {
+                    const int r16 = c & 15;
+                    const int i = ((r16 >> 3) << 1) | (b & 1);
+                    const int ln = (r16 & 7) * 4 + ((b & 7) >> 1);
+                    const float v = r[(((c >> 4) * NT + (b >> 3)) * 4 + i) * 32 + ln];
+                    const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c;
+                    if (a.split == 1)
+                        a.y[off] = f32_to_bf16_rn(v);
+                    else
+                        a.partial[(size_t)w.sk * a.B * a.N + off] = v;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tail->res_empty[buf]));  // buffer free again
             if (a.split > 1) {
                 // the last unit of this tile to finish sums the partials in order
                 __threadfence();
-                consumer_bar();
+                __syncwarp();
                 uint32_t* counter = a.counters + (size_t)w.bc * a.tiles + w.tile;
-                if (threadIdx.x == 32) {
-                    uint32_t prev;
+                uint32_t prev = 0;
+                if (lane == 0)
                     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
                                  : "=r"(prev)
                                  : "l"(counter)
                                  : "memory");
-                    tail->is_last = (prev == (uint32_t)(a.split - 1));
-                }
-                consumer_bar();
-                if (tail->is_last) {
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == (uint32_t)(a.split - 1)) {
                     __threadfence();
-                    const int t = threadIdx.x - 32;
-                    for (int e = t; e < w.rows * w.width; e += 32 * kConsumerWarps) {
-                        const int r = e / w.width;
-                        const int c = e - r * w.width;
-                        const size_t off = (size_t)(w.b0 + r) * a.N + w.n0 + c;
-                        float sum = 0.f;
-                        for (int sk = 0; sk < a.split; ++sk)
-                            sum += __ldcg(a.partial + (size_t)sk * a.B * a.N + off);
-                        a.y[off] = f32_to_bf16_rn(sum);
-                    }
-                    if (t == 0) *counter = 0u;  // ready for the next call
+                    for (int b = 0; b < w.rows; ++b)
+                        for (int c = lane; c < w.width; c += 32) {
+                            const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c;
+                            float sum = 0.f;
+                            for (int sk = 0; sk < a.split; ++sk)
+                                sum += __ldcg(a.partial + (size_t)sk * a.B * a.N + off);
+                            a.y[off] = f32_to_bf16_rn(sum);
+                        }
+                    if (lane == 0) *counter = 0u;  // ready for the next call
                 }
-                consumer_bar();  // is_last is reused by the next unit
             }
         }
     }
@@ -427,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const Args a) {
 
 template <int NT, bool Z>
 cudaError_t launch_t(const SkinnyPlan& p, Args a, cudaStream_t stream) {
-    const size_t smem = (size_t)ring_slots<NT>() * slot_bytes<NT>() + sizeof(Tail);
+    const size_t smem = (size_t)ring_slots<NT>() * slot_bytes<NT>() + 2 * result_bytes<NT>() +
+                        sizeof(Tail);
     const void* kern = reinterpret_cast<const void*>(skinny_kernel<NT, Z>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
@@ -447,38 +526,31 @@ SkinnyPlan plan_skinny(int B, int K, int N, int num_sms) {
     p.col_blocks = (N + kTileCols - 1) / kTileCols;
     const int G = K / kGroup;
     const long long base = (long long)p.col_blocks * p.batch_chunks;
-    const int cps = ctas_per_sm(p.nt);
-    // Choose the K split: estimated time = the busiest SM's groups plus a
-    // fixed cost per unit (and per split, for the reduction).  CTA c takes
-    // units c, c + grid, ...; SM m hosts CTAs m and m + num_sms.
-    double best = 1e300;
-    int best_split = 1;
-    for (int split = 1; split <= std::min(G, 64); ++split) {
-        const int gps = (G + split - 1) / split;
-        if ((G + gps - 1) / gps != split) continue;  // no empty units
-        if (split > 1 && base > kMaxCounters) break;
-        const long long units = base * split;
-        const long long grid = std::min<long long>(units, (long long)num_sms * cps);
-        const long long q = units / grid, r = units % grid;
-        auto n_of = [&](long long c) { return c < grid ? q + (c < r ? 1 : 0) : 0; };
-        const long long sm_units = n_of(0) + (cps > 1 ? n_of(num_sms) : 0);
-        const double per_unit = gps + (split > 1 ? 2.0 : 0.5);
-        const double cost = (double)sm_units * per_unit / cps;
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_split = split;
-        }
-    }
-    p.split = best_split;
-    p.gps = (G + best_split - 1) / best_split;
-    const long long units = base * p.split;
+    const long long slots = (long long)num_sms * ctas_per_sm(p.nt);
+    // Units are handed out dynamically, so only their size matters: the K
+    // split is the smallest that gives every CTA at least one unit (small
+    // layers), and otherwise keeps units of a few ring slots so the tail
+    // (the last units finishing) stays short, without multiplying the
+    // split-K partial traffic.
+    int split = 1;
+    while (split < G && split < 32 && base * split < slots) ++split;
+    while (split < G && split < 32 && base * split < 3 * slots &&
+           (G + split - 1) / split > 8)
+        ++split;
+    if (base > kMaxCounters - 2) split = 1;
+    int gps = (G + split - 1) / split;
+    split = (G + gps - 1) / gps;  // no empty units
+    p.split = split;
+    p.gps = gps;
+    const long long units = base * split;
     p.units = (int)units;
-    p.grid = (int)std::min<long long>(units, (long long)num_sms * cps);
+    p.grid = (int)std::min<long long>(units, slots);
     return p;
 }
 
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N) {
-    return split_workspace_bytes(p.split, B, N);
+    // the scheduler's work counter lives in the counter prefix
+    return p.split > 1 ? split_workspace_bytes(p.split, B, N) : kCounterBytes;
 }
 
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,

@@ -337,16 +337,26 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         const int r = t & (kTileN - 1);                   // weight column within the tile
         const int h = t >> 7;                             // which 32-row chunk of the block
         const int n = min(n0 + r, a.N - 1);
-        int cur_g = -1;
+        // scale / zero-point of the current group, and the next group's
+        // already in flight (two K blocks per group hide the load latency)
+        const int g_last = (kb_begin + nkb - 1) >> 1;
+        int cur_g = kb_begin >> 1;
+        uint16_t s_next = __ldg(a.scales + (size_t)cur_g * a.N + n);
+        uint32_t z_next = kHasZeros ? load_zero(a.zeros, a.N, cur_g, n) : 8u;
         uint32_t s2 = 0, z2 = kSymmetricZeroPair;
+        cur_g -= 1;
         for (int i = 0; i < nkb; ++i) {
             const int s = i % kSlots;
             const int kb = kb_begin + i;
             const int g = kb >> 1;  // two 64-row blocks per group of 128
             if (g != cur_g) {
-                s2 = scale_pair(__ldg(a.scales + (size_t)g * a.N + n));
-                if (kHasZeros) z2 = zero_pair(load_zero(a.zeros, a.N, g, n));
+                s2 = scale_pair(s_next);
+                if (kHasZeros) z2 = zero_pair(z_next);
                 cur_g = g;
+                if (g < g_last) {
+                    s_next = __ldg(a.scales + (size_t)(g + 1) * a.N + n);
+                    if (kHasZeros) z_next = load_zero(a.zeros, a.N, g + 1, n);
+                }
             }
             const bool landed = wait_bounded(smem_u32(&tail->full_tma[s]), (i / kSlots) & 1,
                                              abort, a.status, kTimeoutNs);
