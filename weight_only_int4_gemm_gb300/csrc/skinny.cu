@@ -343,8 +343,11 @@ skinny_kernel(const Args a) {
                 cp_async_arrive_noinc(smem_u32(&tail->full[s]));
             }
         }
-        // every copy into the ring must land before the CTA exits
-        for (int i = max(0, w_issued - S); i < w_issued; ++i) {
+        // After an expired wait, every copy still in flight into the ring must
+        // land before the CTA exits.  (On the normal path the consumers have
+        // waited for every slot, and the end marker may already reuse a slot,
+        // so there is nothing to drain.)
+        for (int i = max(0, w_issued - S); !ok && i < w_issued; ++i) {
             const uint32_t full = smem_u32(&tail->full[i % S]);
             if (i >= issued) cp_async_arrive_noinc(full);
             wait_bounded(full, (i / S) & 1, abort, a.status);
