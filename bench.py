@@ -42,13 +42,14 @@ L2_BYTES = 129 * 1024 * 1024
 
 # --------------------------------------------------------------- workloads
 
-def workload(name: str, batch: int | None):
+def workload(name: str, batch: int | None, shape: str | None = None):
     """List of (label, B, K, N, zero_points, outlier_frac) GEMMs forming one step."""
     if name == "decode_layer":
         return [(f"{lbl}_B{B}", B, K, N, False, 0.0)
                 for B in (1, 2, 4, 8, 16) for lbl, K, N in LAYER]
     if name == "single":
-        return [("linear_4096", batch or 1, 4096, 4096, False, 0.0)]
+        K, N = (int(v) for v in (shape or "4096x4096").split("x"))
+        return [(f"linear_{K}x{N}", batch or 1, K, N, False, 0.0)]
     if name == "decode_step":
         B = batch or 1
         return [(f"{lbl}_L{i}", B, K, N, False, 0.0) for i in range(32) for lbl, K, N in LAYER] + \
@@ -425,6 +426,7 @@ def main():
     ap.add_argument("--workload", default="decode_layer",
                     choices=["decode_layer", "single", "decode_step", "prefill", "zp70b"])
     ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--shape", default=None, help="KxN for --workload single (default 4096x4096)")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -437,7 +439,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    gemms = workload(args.workload, args.batch)
+    gemms = workload(args.workload, args.batch, args.shape)
     sbytes, sflops = step_bytes_flops(gemms)
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
 

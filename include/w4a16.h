@@ -82,10 +82,13 @@ typedef enum {
 size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros);
 
 /* Bytes of device workspace w4a16_gemm needs for this shape (0 if none).
- * The workspace holds fp32 split-K partial sums and arrival counters.  It
- * must be zero-filled once before its first use; every call leaves the
- * counters at zero again, so it can be reused by later calls on the same
- * stream.  Calls that run concurrently must use different workspaces.
+ * The workspace holds arrival counters, the small-batch kernel's work
+ * scheduler and an fp32 accumulator for split-K sums.  It must be
+ * zero-filled once before its first use; every call leaves it all-zero
+ * again, so later calls of any shape on the same stream can reuse it.
+ * Calls that run concurrently must use different workspaces.  (Split-K sums
+ * are accumulated in arrival order, so outputs may differ in the last bit
+ * between calls; every one is within the error bound.)
  * Returns (size_t)-1 for invalid shapes. */
 size_t w4a16_workspace_bytes(int B, int K, int N, int group_size);
 

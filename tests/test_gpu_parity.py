@@ -161,14 +161,32 @@ def test_zero_point_70b_shapes_sampled(K, N, B):
 
 # ------------------------------------------------------------ behaviour
 
-def test_repeated_calls_are_deterministic_and_reuse_workspace():
-    p = inputs.make_problem(4, 4096, 4096, seed=3).to("cuda")
-    packed = w.w4a16_pack(p.qweight)
-    ys = [w.w4a16_gemm(p.x, packed, p.scales, False).clone() for _ in range(3)]
-    # interleave another shape on the same workspace, then repeat
-    q = inputs.make_problem(2, 14336, 4096, seed=4).to("cuda")
+def test_repeated_calls_reuse_workspace_across_shapes():
+    """One workspace shared by calls of different shapes and paths: every call
+    leaves it zeroed, so every result stays within the bound."""
+    p = inputs.make_problem(4, 4096, 4096, seed=3)
+    g = p.to("cuda")
+    packed = w.w4a16_pack(g.qweight)
+    ys = [w.w4a16_gemm(g.x, packed, g.scales, False).clone() for _ in range(3)]
+    q = inputs.make_problem(64, 4096, 4096, seed=4).to("cuda")         # tensor-core split-K
     w.w4a16_gemm(q.x, w.w4a16_pack(q.qweight), q.scales, False)
-    ys.append(w.w4a16_gemm(p.x, packed, p.scales, False))
+    r = inputs.make_problem(2, 14336, 4096, seed=5).to("cuda")         # small-batch split-K
+    w.w4a16_gemm(r.x, w.w4a16_pack(r.qweight), r.scales, False)
+    ys.append(w.w4a16_gemm(g.x, packed, g.scales, False))
+    torch.cuda.synchronize()
+    assert w.w4a16_device_status() == 0
+    for y in ys:
+        assert_within_bound(y.cpu(), p)
+
+
+def test_without_split_k_results_are_bit_identical():
+    """A shape that needs no K split has one summation order: repeated calls
+    are bit-identical."""
+    B, K, N = 8, 1024, 128256
+    assert w.w4a16_workspace_bytes(B, K, N) <= 65536   # counters only, no accumulator
+    g = inputs.make_problem(B, K, N, seed=6).to("cuda")
+    packed = w.w4a16_pack(g.qweight)
+    ys = [w.w4a16_gemm(g.x, packed, g.scales, False).clone() for _ in range(3)]
     torch.cuda.synchronize()
     for y in ys[1:]:
         assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))

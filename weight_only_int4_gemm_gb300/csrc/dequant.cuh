@@ -91,6 +91,13 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int i, uint32_t 
     return bf16x2_mul(bf16x2_sub(magic, zero2), scale2);
 }
 
+// Pair i (0..3) of a packed word as the exact integers (q - z), bf16x2: the
+// magic OR and the exact subtraction, without the scale.  Kernels that apply
+// the group scale to an fp32 sum over the group use this.
+__device__ __forceinline__ uint32_t code_pair(uint32_t word, int i, uint32_t zero2) {
+    return bf16x2_sub(lop3_and_or(word >> (4 * i), 0x000F000Fu, 0x43004300u), zero2);
+}
+
 // All 8 rows of a packed word, out[i] = rows (2i, 2i+1).
 __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t zero2, uint32_t scale2,
                                              uint32_t out[4]) {

@@ -13,16 +13,14 @@ inline size_t packed_code_bytes(int K, int N) { return (size_t)K * (size_t)N / 2
 inline size_t packed_zero_bytes(int K, int N) { return (size_t)(K / kGroup) * (size_t)(N / 8) * 4; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace layout shared by every split-K kernel: a fixed prefix of arrival
-// counters (zero-filled once by the caller, left at zero by every call) and,
-// after it, the fp32 partial sums (no initialisation needed).  The prefix
-// does not depend on the shape, so calls of different shapes can share one
-// workspace.  Shapes with more output tiles than counters never split K.
+// Workspace layout shared by every kernel: a fixed prefix of counters
+// (per-tile arrival counters and the small-batch kernel's work-scheduler
+// words) and, after it, one fp32 accumulator [B][N] that split-K kernels add
+// their partial sums into.  The caller zero-fills the workspace once; every
+// call leaves all of it at zero again (the last CTA of a tile clears what it
+// converted), so calls of different shapes can share one workspace.
 constexpr int kMaxCounters = 16384;
 constexpr size_t kCounterBytes = kMaxCounters * sizeof(uint32_t);
-inline size_t split_workspace_bytes(int split, int B, int N) {
-    return split <= 1 ? 0 : kCounterBytes + (size_t)split * B * N * sizeof(float);
-}
 inline uint32_t* ws_counters(void* ws) { return static_cast<uint32_t*>(ws); }
 inline float* ws_partials(void* ws) {
     return ws == nullptr ? nullptr
@@ -63,6 +61,7 @@ struct TcPlan {
     int col_tiles;   // ceil(N / 128)
     int kb_per_split;// 64-row K blocks per split
     int split;       // K splits (1 = no workspace)
+    int grid;        // persistent CTAs
 };
 TcPlan plan_tc(int B, int K, int N, int num_sms);
 size_t tc_workspace_bytes(const TcPlan& p, int B, int N);

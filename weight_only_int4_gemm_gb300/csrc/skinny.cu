@@ -13,11 +13,15 @@
 //    lanes copy the matching activations, scales and zero-points with
 //    cp.async and attach them to the slot's mbarrier (arrive.noinc);
 //  * each consumer warp owns 16 columns of the tile: it reads its codes from
-//    the slot (one conflict-free 16-byte load per lane per chunk), decodes
-//    them with the shared lop3 magic-number routine and feeds the bf16 pairs
-//    as the A operand of warp-level m16n8k16 tensor-core products in which
-//    the 16 rows are weight columns and the 8 columns batch rows (operands
-//    swapped, so the batch pads only to 8).  The k order inside an mma is
+//    the slot (one conflict-free 16-byte load per lane per chunk), turns them
+//    into the exact integers (q - z) with the shared magic-number OR and an
+//    exact bf16 subtraction, and feeds those as the A operand of warp-level
+//    m16n8k16 tensor-core products in which the 16 rows are weight columns
+//    and the 8 columns batch rows (operands swapped, so the batch pads only to
+//    8).  The products (q - z)*x are exact; each 128-row group is summed in
+//    fp32 and multiplied by its scale once (acc += s * sum), which removes the
+//    per-weight bf16 multiply from the CUDA cores -- at decode batch sizes the
+//    issue slots, not the tensor cores, bound the kernel.  The k order inside an mma is
 //    free, so each lane's four k values per step are consecutive rows of its
 //    own 32-row chunk; the activations are staged in exactly that fragment
 //    order, which makes each fragment load one 16-byte read;
@@ -25,9 +29,11 @@
 //    dynamically (the first unit of each CTA is fixed, later ones come from an
 //    atomic work counter), so slow and fast SMs even out;
 //  * a dedicated epilogue warp takes each finished unit's accumulators from
-//    shared memory and writes y -- or, for a K split, fp32 partials, the last
-//    unit of a tile to finish (arrival counter) summing them in a fixed order
-//    (deterministic, no second launch) -- while the consumers already work on
+//    shared memory and writes y -- or, for a K split, adds them into an fp32
+//    accumulator with vector reductions (red.global.add.v4.f32), the last
+//    unit of a tile to arrive (arrival counter) converting the sum to bf16
+//    and clearing the accumulator; the order of the fp32 additions across
+//    K splits follows arrival order -- while the consumers already work on
 //    the next unit;
 //  * programmatic dependent launch: the first ring slots' weight copies are
 //    issued before waiting for the previous kernel on the stream, so
@@ -71,7 +77,7 @@ struct Args {
     const uint16_t* scales;
     const uint32_t* zeros;
     uint16_t* y;
-    float* partial;      // [split][B][N]   (split > 1)
+    float* partial;      // fp32 accumulator [B][N], zero between calls (split > 1)
     uint32_t* counters;  // fixed workspace prefix: per-tile arrivals + scheduler words
     unsigned int* status;
     int B, K, N;
@@ -141,6 +147,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// 16-byte asynchronous copy that reads src_bytes (0 or 16) and zero-fills the rest.
+__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
 }
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
@@ -298,10 +310,15 @@ skinny_kernel(const Args a) {
                 const int ngs = min(kSlotGroups, w.g_begin + w.ng - g0);
                 const uint32_t xbase = smem_u32(slot_x(s));
                 const int p = lane & 15;
+                const int rows8 = (w.rows + 7) & ~7;  // rows read by the mma tiles in use
                 for (int gl = 0; gl < ngs; ++gl)
-                    for (int r = lane >> 4; r < w.rows; r += 2)
-                        cp_async_16(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
-                                    a.x + (size_t)(w.b0 + r) * a.K + (size_t)kGroup * (g0 + gl) + 8 * p);
+                    for (int r = lane >> 4; r < rows8; r += 2) {
+                        const bool valid = r < w.rows;  // padding rows are zero-filled
+                        cp_async_16z(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
+                                     a.x + (size_t)(w.b0 + (valid ? r : 0)) * a.K +
+                                         (size_t)kGroup * (g0 + gl) + 8 * p,
+                                     valid ? 16u : 0u);
+                    }
                 const int gl = lane >> 4;
                 if (gl < ngs && p < w.width / 8) {
                     cp_async_16(smem_u32(slot_scales(s)) + 2u * (gl * kTileCols + 8 * p),
@@ -390,13 +407,14 @@ skinny_kernel(const Args a) {
             const uint16_t* sc = slot_scales(s);
             const uint32_t* zs = slot_zeros(s);
             const int cla = min(ca, w.width - 1), clb = min(cb, w.width - 1);
+            const uint4* xq = xs + gid * 4 + tig;  // this lane's fragment column
 #pragma unroll
             for (int gl = 0; gl < kSlotGroups; ++gl) {
                 if (gl < ngs) {
                     const uint4 qa = codes[(4 * gl + tig) * w.width + cla];
                     const uint4 qb = codes[(4 * gl + tig) * w.width + clb];
-                    const uint32_t sa = scale_pair(sc[gl * kTileCols + cla]);
-                    const uint32_t sb = scale_pair(sc[gl * kTileCols + clb]);
+                    const float sa = __uint_as_float((uint32_t)sc[gl * kTileCols + cla] << 16);
+                    const float sb = __uint_as_float((uint32_t)sc[gl * kTileCols + clb] << 16);
                     uint32_t za = kSymmetricZeroPair, zb = kSymmetricZeroPair;
                     if (kHasZeros) {
                         za = zero_pair((zs[gl * (kTileCols / 8) + (cla >> 3)] >> (4 * (cla & 7))) & 0xFu);
@@ -404,27 +422,37 @@ skinny_kernel(const Args a) {
                     }
                     const uint32_t wA[4] = {qa.x, qa.y, qa.z, qa.w};
                     const uint32_t wB[4] = {qb.x, qb.y, qb.z, qb.w};
+                    float t[NT][4];  // this group's fp32 sums of (q - z) * x
+#pragma unroll
+                    for (int bt = 0; bt < NT; ++bt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) t[bt][i] = 0.f;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint4 xf[NT];
 #pragma unroll
                         for (int bt = 0; bt < NT; ++bt)
-                            xf[bt] = (bt * 8 + gid < w.rows)  // rows past B are never staged
-                                         ? xs[((gl * 4 + j) * kRows + bt * 8 + gid) * 4 + tig]
-                                         : make_uint4(0u, 0u, 0u, 0u);
+                            xf[bt] = xq[((gl * 4 + j) * kRows + bt * 8) * 4];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             // step 2j + h: rows 4(2j+h) .. +3 of each lane's chunk
-                            const uint32_t a0 = dequant_pair(wA[j], 2 * h, za, sa);
-                            const uint32_t a1 = dequant_pair(wB[j], 2 * h, zb, sb);
-                            const uint32_t a2 = dequant_pair(wA[j], 2 * h + 1, za, sa);
-                            const uint32_t a3 = dequant_pair(wB[j], 2 * h + 1, zb, sb);
+                            const uint32_t a0 = code_pair(wA[j], 2 * h, za);
+                            const uint32_t a1 = code_pair(wB[j], 2 * h, zb);
+                            const uint32_t a2 = code_pair(wA[j], 2 * h + 1, za);
+                            const uint32_t a3 = code_pair(wB[j], 2 * h + 1, zb);
 #pragma unroll
                             for (int bt = 0; bt < NT; ++bt)
                                 if (bt * 8 < w.rows)  // warp-uniform: skip padding tiles
-                                    mma_bf16(acc[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
+                                    mma_bf16(t[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
                                              h ? xf[bt].w : xf[bt].y);
                         }
+                    }
+#pragma unroll
+                    for (int bt = 0; bt < NT; ++bt) {
+                        acc[bt][0] = fmaf(sa, t[bt][0], acc[bt][0]);
+                        acc[bt][1] = fmaf(sa, t[bt][1], acc[bt][1]);
+                        acc[bt][2] = fmaf(sb, t[bt][2], acc[bt][2]);
+                        acc[bt][3] = fmaf(sb, t[bt][3], acc[bt][3]);
                     }
                 }
             }
@@ -450,7 +478,9 @@ skinny_kernel(const Args a) {
             }
         }
     } else {
-        // ---------------- epilogue warp: y, or split-K partials + ordered reduction
+        // ---------------- epilogue warp: y, or split-K accumulation + conversion
+        // Lane l owns columns 4l .. 4l+3 of the tile.
+        const int c4 = 4 * lane;
         for (int k = 0;; ++k) {
             const int buf = k & 1;
             if (!warp_wait(smem_u32(&tail->res_full[buf]), (k >> 1) & 1, abort, a.status)) break;
@@ -458,26 +488,35 @@ skinny_kernel(const Args a) {
             if (u < 0) break;
             const Unit w = decode_unit<NT>(a, u);
             const float* r = res + buf * (result_bytes<NT>() / 4);
+            const bool mine = c4 < w.width;
             // element (column c, row b) of the unit lives at
             // r[((c/16 * NT + b/8) * 4 + i) * 32 + lane'], i = 2*((c%16)/8) + b%2,
             // lane' = 4*(c%8) + (b%8)/2
-            for (int b = 0; b < w.rows; ++b) {
-                for (int c = lane; c < w.width; c += 32) {
-                    const int r16 = c & 15;
-                    const int i = ((r16 >> 3) << 1) | (b & 1);
-                    const int ln = (r16 & 7) * 4 + ((b & 7) >> 1);
-                    const float v = r[(((c >> 4) * NT + (b >> 3)) * 4 + i) * 32 + ln];
-                    const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c;
-                    if (a.split == 1)
-                        a.y[off] = f32_to_bf16_rn(v);
-                    else
-                        a.partial[(size_t)w.sk * a.B * a.N + off] = v;
+            auto elem = [&](int c, int b) {
+                const int r16 = c & 15;
+                const int i = ((r16 >> 3) << 1) | (b & 1);
+                const int ln = (r16 & 7) * 4 + ((b & 7) >> 1);
+                return r[(((c >> 4) * NT + (b >> 3)) * 4 + i) * 32 + ln];
+            };
+            for (int b = 0; b < w.rows && mine; ++b) {
+                const float v0 = elem(c4, b), v1 = elem(c4 + 1, b), v2 = elem(c4 + 2, b),
+                            v3 = elem(c4 + 3, b);
+                const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c4;
+                if (a.split == 1) {
+                    const uint32_t lo = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
+                    const uint32_t hi = (uint32_t)f32_to_bf16_rn(v2) | ((uint32_t)f32_to_bf16_rn(v3) << 16);
+                    *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                } else {
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                                 ::"l"(a.partial + off), "f"(v0), "f"(v1), "f"(v2), "f"(v3)
+                                 : "memory");
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tail->res_empty[buf]));  // buffer free again
             if (a.split > 1) {
-                // the last unit of this tile to finish sums the partials in order
+                // the last unit of this tile to arrive converts the fp32 sum to
+                // bf16 and clears the accumulator for the next call
                 __threadfence();
                 __syncwarp();
                 uint32_t* counter = a.counters + (size_t)w.bc * a.tiles + w.tile;
@@ -490,14 +529,27 @@ skinny_kernel(const Args a) {
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 if (prev == (uint32_t)(a.split - 1)) {
                     __threadfence();
-                    for (int b = 0; b < w.rows; ++b)
-                        for (int c = lane; c < w.width; c += 32) {
-                            const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c;
-                            float sum = 0.f;
-                            for (int sk = 0; sk < a.split; ++sk)
-                                sum += __ldcg(a.partial + (size_t)sk * a.B * a.N + off);
-                            a.y[off] = f32_to_bf16_rn(sum);
+                    for (int b0 = 0; b0 < w.rows && mine; b0 += 8) {
+                        float4 v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (b0 + j < w.rows)
+                                v[j] = __ldcg(reinterpret_cast<const float4*>(
+                                    a.partial + (size_t)(w.b0 + b0 + j) * a.N + w.n0 + c4));
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (b0 + j < w.rows) {
+                                const size_t off = (size_t)(w.b0 + b0 + j) * a.N + w.n0 + c4;
+                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[j].x) |
+                                                    ((uint32_t)f32_to_bf16_rn(v[j].y) << 16);
+                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[j].z) |
+                                                    ((uint32_t)f32_to_bf16_rn(v[j].w) << 16);
+                                *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                                __stcg(reinterpret_cast<float4*>(a.partial + off),
+                                       make_float4(0.f, 0.f, 0.f, 0.f));
+                            }
                         }
+                    }
                     if (lane == 0) *counter = 0u;  // ready for the next call
                 }
             }
@@ -552,8 +604,8 @@ SkinnyPlan plan_skinny(int B, int K, int N, int num_sms) {
 }
 
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N) {
-    // the scheduler's work counter lives in the counter prefix
-    return p.split > 1 ? split_workspace_bytes(p.split, B, N) : kCounterBytes;
+    // counter prefix (also holds the scheduler's words) + one fp32 accumulator
+    return p.split > 1 ? kCounterBytes + (size_t)B * N * sizeof(float) : kCounterBytes;
 }
 
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,

@@ -14,19 +14,22 @@
 //   D[128 weight columns][bn batch rows] (fp32, TMEM)
 //     += W^T[128][64 k] (bf16, smem, dequantised by producer warps)
 //      . X^T[64 k][bn]  (bf16, smem, TMA from x[B][K])
-// Warp roles (one CTA per tile, K streamed in 64-row blocks through a ring of
-// kSlots shared-memory slots):
-//   warp 0     : TMA thread -- bulk-copies the packed codes of the block and
-//                tensor-copies the x block (128-byte swizzle), one mbarrier
-//                with the expected byte count per slot;
-//   warp 1     : TMEM allocator + the single MMA-issuing thread
-//                (tcgen05.mma kind::f16, 4 x K=16 per block, commit to the
-//                slot's "empty" barrier);
-//   warps 2..9 : dequant producers -- packed codes (smem) -> lop3 magic
-//                decode -> bf16 (q - z) * s -> 128-byte-swizzled K-major
-//                rows of the weight tile; proxy fence; arrive;
-//   warps 4..7 : after the K loop, the epilogue (tcgen05.ld 32 lanes x 16
-//                columns -> bf16 y, or fp32 split-K partials).
+// Persistent CTAs (one per SM) take work items (column tile, batch tile, K
+// split) round robin and stream K in 64-row blocks through a ring of kSlots
+// shared-memory slots.  Warp roles:
+//   warp 0      : TMA thread -- bulk-copies the packed codes of the block (one
+//                 contiguous copy) and tensor-copies the x block (128-byte
+//                 swizzle), one mbarrier with the expected byte count per slot;
+//   warp 1      : TMEM allocator + the single MMA-issuing thread
+//                 (tcgen05.mma kind::f16, 4 x K=16 per block, commit per slot
+//                 to "empty" and per item to the accumulator's "full");
+//   warps 2..9  : dequant producers -- packed codes (smem) -> lop3 magic
+//                 decode -> bf16 (q - z) * s -> 128-byte-swizzled K-major
+//                 rows of the weight tile; proxy fence; arrive;
+//   warps 10..13: epilogue (tcgen05.ld 32 lanes x 16 columns -> bf16 y, or
+//                 fp32 split-K reductions), one TMEM lane quadrant each.
+// Two TMEM accumulators alternate between items, so the epilogue of one item
+// overlaps the main loop of the next.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT in the device status word, drains and returns.
 #include <cuda.h>
@@ -42,13 +45,13 @@ namespace w4a16 {
 namespace {
 
 constexpr int kBlockK = 64;                  // K rows per pipeline slot
-constexpr int kTileN = 128;                  // weight columns per CTA (MMA M)
+constexpr int kTileN = 128;                  // weight columns per tile (MMA M)
 constexpr int kSlots = 4;
-constexpr int kNumWarps = 10;
-constexpr int kThreads = 32 * kNumWarps;
 constexpr int kDequantWarp0 = 2;
 constexpr int kDequantWarps = 8;
-constexpr int kEpilogueWarp0 = 4;            // warps 4..7 = TMEM lane quadrants 0..3
+constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantWarps;  // warps 10..13
+constexpr int kNumWarps = kEpilogueWarp0 + 4;
+constexpr int kThreads = 32 * kNumWarps;     // 448
 constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
 constexpr uint32_t kRawBytes = kTileN * kBlockK / 2;     // 4 KB of packed codes
 constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
@@ -59,7 +62,7 @@ struct Args {
     const uint16_t* scales;
     const uint32_t* zeros;
     uint16_t* y;
-    float* partial;
+    float* partial;      // fp32 accumulator [B][N], zero between calls (split > 1)
     uint32_t* counters;
     unsigned int* status;
     int B, K, N;
@@ -67,7 +70,8 @@ struct Args {
     int kb_per_split;   // K blocks per split
     int split;
     int nkb;            // total K blocks (K / 64)
-    uint32_t tmem_cols; // power of two >= max(32, bn)
+    int col_tiles, batch_tiles, items;
+    uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= max(32, bn))
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
 };
 
@@ -213,15 +217,37 @@ struct SharedTail {
     uint64_t full_tma[kSlots];   // TMA bytes landed (codes + x)
     uint64_t full_ops[kSlots];   // weight tile dequantised (8 warp arrivals)
     uint64_t empty[kSlots];      // MMAs reading the slot finished (commit)
-    uint64_t accum;              // all MMAs finished (commit)
+    uint64_t tmem_full[2];       // accumulator complete (commit)
+    uint64_t tmem_empty[2];      // accumulator drained by the epilogue (4 warps)
     uint64_t never;              // test hook: nobody arrives here
     uint32_t tmem_base;
     int abort;
-    int is_last;
 };
 
 __host__ __device__ constexpr uint32_t slot_bytes(int bn) {
     return kATileBytes + (uint32_t)bn * kBlockK * 2 + kRawBytes;
+}
+
+struct Item {
+    int col_tile, batch_tile, split_idx, n0, b0, nvalid, kb_begin, nkb;
+};
+
+__device__ __forceinline__ Item decode_item(const Args& a, int it) {
+    Item t;
+    t.col_tile = it % a.col_tiles;
+    const int rest = it / a.col_tiles;
+    t.batch_tile = rest % a.batch_tiles;
+    t.split_idx = rest / a.batch_tiles;
+    t.n0 = t.col_tile * kTileN;
+    t.b0 = t.batch_tile * a.bn;
+    t.nvalid = min(kTileN, a.N - t.n0);
+    t.kb_begin = t.split_idx * a.kb_per_split;
+    t.nkb = min(a.kb_per_split, a.nkb - t.kb_begin);
+    return t;
+}
+
+__device__ __forceinline__ void epilogue_bar() {  // the 4 epilogue warps only
+    asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
 template <bool kHasZeros>
@@ -235,14 +261,6 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int col_tile = blockIdx.x;
-    const int batch_tile = blockIdx.y;
-    const int split_idx = blockIdx.z;
-    const int n0 = col_tile * kTileN;
-    const int b0 = batch_tile * a.bn;
-    const int nvalid = min(kTileN, a.N - n0);
-    const int kb_begin = split_idx * a.kb_per_split;
-    const int nkb = min(a.kb_per_split, a.nkb - kb_begin);
     volatile int* abort = &tail->abort;
 
     auto a_tile = [&](int s) { return smem + s * sbytes; };
@@ -255,23 +273,25 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             mbar_init(smem_u32(&tail->full_ops[s]), kDequantWarps);
             mbar_init(smem_u32(&tail->empty[s]), 1);
         }
-        mbar_init(smem_u32(&tail->accum), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tail->tmem_full[b]), 1);
+            mbar_init(smem_u32(&tail->tmem_empty[b]), 4);
+        }
         mbar_init(smem_u32(&tail->never), 1);
         tail->abort = 0;
-        tail->is_last = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(&tail->tmem_base)), "r"(a.tmem_cols)
+                     ::"r"(smem_u32(&tail->tmem_base)), "r"(2 * a.acc_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_d = tail->tmem_base;
+    const uint32_t tmem_base = tail->tmem_base;
     // the next kernel on the stream may start now; this one reads x and writes
     // y / workspace only after the previous kernel has finished (the TMA
     // thread waits; everything else is ordered after it through mbarriers)
@@ -281,26 +301,32 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // ---------------- TMA producer
         if (lane == 0) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            const uint32_t raw_block = 2u * (uint32_t)nvalid * 16;  // two 32-row chunks
-            const uint32_t tx = raw_block + (uint32_t)a.bn * kBlockK * 2;
-            const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, col_tile);
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % kSlots;
-                if (i >= kSlots &&
-                    !wait_bounded(smem_u32(&tail->empty[s]), ((i / kSlots) - 1) & 1, abort,
-                                  a.status, kTimeoutNs))
-                    break;
-                const uint32_t bar = smem_u32(&tail->full_tma[s]);
-                const int kb = kb_begin + i;
-                mbar_arrive_expect_tx(bar, tx);
-                bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * nvalid * 16,
-                         raw_block, bar);
-                tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, b0, bar);
-                issued = i + 1;
+            int stage = 0, issued = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
+                const Item t = decode_item(a, it);
+                const uint32_t raw_block = 2u * (uint32_t)t.nvalid * 16;  // two 32-row chunks
+                const uint32_t tx = raw_block + (uint32_t)a.bn * kBlockK * 2;
+                const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, t.col_tile);
+                for (int i = 0; i < t.nkb; ++i, ++stage) {
+                    const int s = stage % kSlots;
+                    if (stage >= kSlots &&
+                        !wait_bounded(smem_u32(&tail->empty[s]), ((stage / kSlots) - 1) & 1, abort,
+                                      a.status, kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_u32(&tail->full_tma[s]);
+                    const int kb = t.kb_begin + i;
+                    mbar_arrive_expect_tx(bar, tx);
+                    bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * t.nvalid * 16,
+                             raw_block, bar);
+                    tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, t.b0, bar);
+                    issued = stage + 1;
+                }
             }
-            // drain: the copies of the last slots must land before the CTA exits
-            for (int i = max(0, issued - kSlots); i < issued; ++i)
+            // after an expired wait, the copies in flight must land before exit
+            for (int i = max(0, issued - kSlots); !ok && i < issued; ++i)
                 wait_bounded(smem_u32(&tail->full_tma[i % kSlots]), (i / kSlots) & 1, abort,
                              a.status, kTimeoutNs);
         }
@@ -312,133 +338,197 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             if (a.force_timeout)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
                                   (unsigned long long)a.force_timeout * 1000000ull);
-            for (int i = 0; ok && i < nkb; ++i) {
-                const int s = i % kSlots;
-                const uint32_t ph = (i / kSlots) & 1;
-                if (!wait_bounded(smem_u32(&tail->full_tma[s]), ph, abort, a.status, kTimeoutNs) ||
-                    !wait_bounded(smem_u32(&tail->full_ops[s]), ph, abort, a.status, kTimeoutNs)) {
+            int stage = 0, j = 0;
+            for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x, ++j) {
+                const Item t = decode_item(a, it);
+                const int acc = j & 1;
+                if (j >= 2 && !wait_bounded(smem_u32(&tail->tmem_empty[acc]), ((j >> 1) - 1) & 1,
+                                            abort, a.status, kTimeoutNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t abase = smem_u32(a_tile(s));
-                const uint32_t xbase = smem_u32(x_tile(s));
+                const uint32_t tmem_d = tmem_base + acc * a.acc_cols;
+                for (int i = 0; i < t.nkb; ++i, ++stage) {
+                    const int s = stage % kSlots;
+                    const uint32_t ph = (stage / kSlots) & 1;
+                    if (!wait_bounded(smem_u32(&tail->full_tma[s]), ph, abort, a.status, kTimeoutNs) ||
+                        !wait_bounded(smem_u32(&tail->full_ops[s]), ph, abort, a.status, kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t abase = smem_u32(a_tile(s));
+                    const uint32_t xbase = smem_u32(x_tile(s));
 #pragma unroll
-                for (int kk = 0; kk < kBlockK / 16; ++kk)
-                    mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
-                                smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
-                mma_commit(smem_u32(&tail->empty[s]));
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
+                                    smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
+                    mma_commit(smem_u32(&tail->empty[s]));
+                }
+                mma_commit(smem_u32(&tail->tmem_full[acc]));  // fires once this item's MMAs are done
             }
-            mma_commit(smem_u32(&tail->accum));  // fires once every issued MMA is done
+            if (!ok) {
+                // let the epilogue drain: both accumulators "complete" once
+                // every issued MMA has finished
+                mma_commit(smem_u32(&tail->tmem_full[0]));
+                mma_commit(smem_u32(&tail->tmem_full[1]));
+            }
+        }
+    } else if (warp < kEpilogueWarp0) {
+        // ---------------- dequant producers (warps 2..9)
+        const int t256 = threadIdx.x - 32 * kDequantWarp0;  // 0..255
+        const int r = t256 & (kTileN - 1);                   // weight column within the tile
+        const int h = t256 >> 7;                             // which 32-row chunk of the block
+        int stage = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
+            const Item t = decode_item(a, it);
+            const int n = min(t.n0 + r, a.N - 1);
+            // scale / zero-point of the current group, and the next group's
+            // already in flight (two K blocks per group hide the load latency)
+            const int g_last = (t.kb_begin + t.nkb - 1) >> 1;
+            int cur_g = t.kb_begin >> 1;
+            uint16_t s_next = __ldg(a.scales + (size_t)cur_g * a.N + n);
+            uint32_t z_next = kHasZeros ? load_zero(a.zeros, a.N, cur_g, n) : 8u;
+            uint32_t s2 = 0, z2 = kSymmetricZeroPair;
+            cur_g -= 1;
+            for (int i = 0; i < t.nkb; ++i, ++stage) {
+                const int s = stage % kSlots;
+                const int kb = t.kb_begin + i;
+                const int g = kb >> 1;  // two 64-row blocks per group of 128
+                if (g != cur_g) {
+                    s2 = scale_pair(s_next);
+                    if (kHasZeros) z2 = zero_pair(z_next);
+                    cur_g = g;
+                    if (g < g_last) {
+                        s_next = __ldg(a.scales + (size_t)(g + 1) * a.N + n);
+                        if (kHasZeros) z_next = load_zero(a.zeros, a.N, g + 1, n);
+                    }
+                }
+                const bool landed = wait_bounded(smem_u32(&tail->full_tma[s]), (stage / kSlots) & 1,
+                                                 abort, a.status, kTimeoutNs);
+                if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
+                    ok = false;
+                    break;
+                }
+                const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * t.nvalid + min(r, t.nvalid - 1)];
+                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                uint8_t* row = a_tile(s) + r * 128;
+#pragma unroll
+                for (int jw = 0; jw < 4; ++jw) {
+                    uint32_t p[4];
+                    dequant_word(words[jw], z2, s2, p);
+                    const int chunk = (4 * h + jw) ^ (r & 7);  // 128-byte swizzle
+                    *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(p[0], p[1], p[2], p[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tail->full_ops[s]));
+            }
         }
     } else {
-        // ---------------- dequant producers (warps 2..9)
-        const int t = threadIdx.x - 32 * kDequantWarp0;  // 0..255
-        const int r = t & (kTileN - 1);                   // weight column within the tile
-        const int h = t >> 7;                             // which 32-row chunk of the block
-        const int n = min(n0 + r, a.N - 1);
-        // scale / zero-point of the current group, and the next group's
-        // already in flight (two K blocks per group hide the load latency)
-        const int g_last = (kb_begin + nkb - 1) >> 1;
-        int cur_g = kb_begin >> 1;
-        uint16_t s_next = __ldg(a.scales + (size_t)cur_g * a.N + n);
-        uint32_t z_next = kHasZeros ? load_zero(a.zeros, a.N, cur_g, n) : 8u;
-        uint32_t s2 = 0, z2 = kSymmetricZeroPair;
-        cur_g -= 1;
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % kSlots;
-            const int kb = kb_begin + i;
-            const int g = kb >> 1;  // two 64-row blocks per group of 128
-            if (g != cur_g) {
-                s2 = scale_pair(s_next);
-                if (kHasZeros) z2 = zero_pair(z_next);
-                cur_g = g;
-                if (g < g_last) {
-                    s_next = __ldg(a.scales + (size_t)(g + 1) * a.N + n);
-                    if (kHasZeros) z_next = load_zero(a.zeros, a.N, g + 1, n);
-                }
-            }
-            const bool landed = wait_bounded(smem_u32(&tail->full_tma[s]), (i / kSlots) & 1,
-                                             abort, a.status, kTimeoutNs);
-            if (!__all_sync(0xffffffffu, landed)) break;  // warp-uniform exit
-            const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * nvalid + r];
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-            uint8_t* row = a_tile(s) + r * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t p[4];
-                dequant_word(words[j], z2, s2, p);
-                const int chunk = (4 * h + j) ^ (r & 7);  // 128-byte swizzle
-                *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(p[0], p[1], p[2], p[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tail->full_ops[s]));
-        }
-
-        // ---------------- epilogue (warps 4..7 = lane quadrants 0..3)
-        if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
-            const int quad = warp - kEpilogueWarp0;
-            const bool done = wait_bounded(smem_u32(&tail->accum), 0, abort, a.status, kTimeoutNs);
+        // ---------------- epilogue (warps 10..13; TMEM lane quadrant = warp % 4)
+        const int quad = warp & 3;
+        int j = 0;
+        for (int it = blockIdx.x; it < a.items; it += gridDim.x, ++j) {
+            const Item t = decode_item(a, it);
+            const int acc = j & 1;
+            const bool done = wait_bounded(smem_u32(&tail->tmem_full[acc]), (j >> 1) & 1, abort,
+                                           a.status, kTimeoutNs);
             tc_fence_after();
-            if (__all_sync(0xffffffffu, done && !*abort)) {  // tcgen05.ld is warp-collective
-                const int nn = n0 + quad * 32 + lane;
-                const uint32_t taddr = tmem_d + ((uint32_t)(quad * 32) << 16);
+            const bool live = __all_sync(0xffffffffu, done && !*abort);
+            if (live) {  // tcgen05.ld is warp-collective
+                const int nn = t.n0 + quad * 32 + lane;
+                const uint32_t taddr = tmem_base + acc * a.acc_cols + ((uint32_t)(quad * 32) << 16);
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
                     tmem_ld_16(taddr + c0, v);
                     if (nn < a.N) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int b = b0 + c0 + j;
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int b = t.b0 + c0 + jj;
                             if (b < a.B) {
                                 if (a.split == 1)
-                                    a.y[(size_t)b * a.N + nn] = f32_to_bf16_rn(v[j]);
+                                    a.y[(size_t)b * a.N + nn] = f32_to_bf16_rn(v[jj]);
                                 else
-                                    a.partial[((size_t)split_idx * a.B + b) * a.N + nn] = v[j];
+                                    asm volatile("red.global.add.f32 [%0], %1;"
+                                                 ::"l"(a.partial + (size_t)b * a.N + nn), "f"(v[jj])
+                                                 : "memory");
                             }
                         }
                     }
                 }
             }
             tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tail->tmem_empty[acc]));
+            if (!live) break;
+            if (a.split > 1) {
+                // the last CTA of this tile to arrive converts the fp32 sum to
+                // bf16 and clears the accumulator for the next call
+                __threadfence();
+                epilogue_bar();
+                uint32_t* counter = a.counters + (size_t)t.batch_tile * a.col_tiles + t.col_tile;
+                __shared__ int s_last;
+                if (warp == kEpilogueWarp0 && lane == 0) {
+                    uint32_t prev;
+                    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                                 : "=r"(prev)
+                                 : "l"(counter)
+                                 : "memory");
+                    s_last = (prev == (uint32_t)(a.split - 1));
+                }
+                epilogue_bar();
+                if (s_last) {
+                    __threadfence();
+                    // 4 columns per thread and 8 loads in flight: the sums come
+                    // back from L2, so latency, not bandwidth, sets the pace
+                    const int rows = min(a.bn, a.B - t.b0);
+                    const int c4n = t.nvalid / 4;
+                    const int total = rows * c4n;
+                    const int et = threadIdx.x - 32 * kEpilogueWarp0;
+                    for (int e0 = et; e0 < total; e0 += 128 * 8) {
+                        float4 v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int e = e0 + 128 * j;
+                            if (e < total) {
+                                const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
+                                v[j] = __ldcg(reinterpret_cast<const float4*>(
+                                    a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int e = e0 + 128 * j;
+                            if (e < total) {
+                                const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
+                                const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
+                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[j].x) |
+                                                    ((uint32_t)f32_to_bf16_rn(v[j].y) << 16);
+                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[j].z) |
+                                                    ((uint32_t)f32_to_bf16_rn(v[j].w) << 16);
+                                *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                                __stcg(reinterpret_cast<float4*>(a.partial + off),
+                                       make_float4(0.f, 0.f, 0.f, 0.f));
+                            }
+                        }
+                    }
+                    if (et == 0) *counter = 0u;
+                }
+                epilogue_bar();  // s_last is reused by the next item
+            }
         }
     }
 
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
-                     "r"(a.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(2 * a.acc_cols)
                      : "memory");
     }
-    if (a.split == 1 || *abort) return;
-
-    // ---------------- split-K: the last CTA of this tile sums the partials in order
-    __threadfence();
-    __syncthreads();
-    uint32_t* counter = a.counters + (size_t)batch_tile * gridDim.x + col_tile;
-    if (threadIdx.x == 0) {
-        uint32_t prev;
-        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                     : "=r"(prev)
-                     : "l"(counter)
-                     : "memory");
-        tail->is_last = (prev == (uint32_t)(a.split - 1));
-    }
-    __syncthreads();
-    if (!tail->is_last) return;
-    __threadfence();
-    const int rows = min(a.bn, a.B - b0);
-    for (int e = threadIdx.x; e < rows * nvalid; e += kThreads) {
-        const int rr = e / nvalid;
-        const int cc = e - rr * nvalid;
-        const size_t off = (size_t)(b0 + rr) * a.N + n0 + cc;
-        float sum = 0.f;
-        for (int sk = 0; sk < a.split; ++sk) sum += __ldcg(a.partial + (size_t)sk * a.B * a.N + off);
-        a.y[off] = f32_to_bf16_rn(sum);
-    }
-    if (threadIdx.x == 0) *counter = 0u;
 }
 
 // ------------------------------------------------------------ host side
@@ -464,7 +554,7 @@ EncodeTiledFn encode_fn() {
 
 size_t smem_bytes(int bn) { return (size_t)kSlots * slot_bytes(bn) + sizeof(SharedTail) + 1024; }
 
-uint32_t tmem_cols_for(int bn) {
+uint32_t acc_cols_for(int bn) {
     uint32_t c = 32;
     while (c < (uint32_t)bn) c <<= 1;
     return c;
@@ -496,16 +586,18 @@ TcPlan plan_tc(int B, int K, int N, int num_sms) {
     p.col_tiles = (N + kTileN - 1) / kTileN;
     const int nkb = K / kBlockK;
     const long long tiles = (long long)p.col_tiles * p.batch_tiles;
-    // K split that minimises (waves x blocks per CTA), a little cost per split
+    // persistent CTAs (one per SM) take items round robin; choose the K split
+    // minimising the busiest CTA's K blocks plus a fixed cost per item and a
+    // small cost per split (accumulator traffic)
     double best = 1e300;
     int best_split = 1, best_kbps = nkb;
     for (int split = 1; split <= std::min(16, nkb); ++split) {
         const int kbps = (nkb + split - 1) / split;
         if (split > 1 && (kbps < 8 || tiles > kMaxCounters)) break;
         const int s = (nkb + kbps - 1) / kbps;
-        const long long ctas = tiles * s;
-        const long long waves = (ctas + num_sms - 1) / num_sms;
-        const double cost = (double)waves * (kbps + 6) * (1.0 + 0.02 * (s - 1));
+        const long long items = tiles * s;
+        const long long per_cta = (items + num_sms - 1) / num_sms;
+        const double cost = (double)per_cta * (kbps + 4) * (1.0 + 0.02 * (s - 1));
         if (cost < best - 1e-9) {
             best = cost;
             best_split = s;
@@ -514,11 +606,12 @@ TcPlan plan_tc(int B, int K, int N, int num_sms) {
     }
     p.split = best_split;
     p.kb_per_split = best_kbps;
+    p.grid = (int)std::min<long long>(tiles * p.split, num_sms);
     return p;
 }
 
 size_t tc_workspace_bytes(const TcPlan& p, int B, int N) {
-    return split_workspace_bytes(p.split, B, N);
+    return p.split > 1 ? kCounterBytes + (size_t)B * N * sizeof(float) : 0;
 }
 
 static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
@@ -552,7 +645,10 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     a.kb_per_split = p.kb_per_split;
     a.split = p.split;
     a.nkb = K / kBlockK;
-    a.tmem_cols = tmem_cols_for(p.bn);
+    a.col_tiles = p.col_tiles;
+    a.batch_tiles = p.batch_tiles;
+    a.items = p.col_tiles * p.batch_tiles * p.split;
+    a.acc_cols = acc_cols_for(p.bn);
     a.force_timeout = force_timeout_ms;
 
     const size_t smem = smem_bytes(p.bn);
@@ -562,8 +658,8 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     void* args[] = {&xmap, &a};
-    return launch_with_pdl(kern, dim3(p.col_tiles, p.batch_tiles, p.split), dim3(kThreads), smem,
-                           stream, args);
+    const int grid = std::min(a.items, p.grid);
+    return launch_with_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, args);
 }
 
 cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
