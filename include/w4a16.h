@@ -142,6 +142,24 @@ int w4a16_select_path(int B, int K, int N);
  * itself fails. */
 w4a16_status w4a16_device_status(int clear);
 
+/* w4a16_gemm for callers that cannot allocate device memory (the pages have
+ * no counterpart; this is a deployment convenience).  Same arguments,
+ * layouts and result as w4a16_gemm, but without a workspace argument: the
+ * split-K scratch is a 4 MiB device array compiled into the library
+ * (every GPU that loads the library holds it until the process exits).
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - The first call on a device looks the array's device address up for
+ *    that device; make that first call before any stream capture.
+ *  - Every call shares the one array and clears its arrival counters on
+ *    `stream` first; calls that may overlap on the GPU (different streams,
+ *    or different host threads) race on it and must be serialised by the
+ *    caller.
+ *  - Returns W4A16_ERR_WORKSPACE when the shape needs more scratch than the
+ *    array holds (w4a16_workspace_bytes() tells how much it needs). */
+w4a16_status w4a16_gemm_static_scratch(const void *x, const void *packed, const void *scales,
+                                       int has_zeros, void *y, int B, int K, int N,
+                                       int group_size, void *stream);
+
 /* Test hook for the bounded waits of the tensor-core kernel (no counterpart
  * on the pages).  Launches the tensor-core kernel on a valid problem (same
  * arguments and rules as w4a16_gemm_path with W4A16_PATH_TCGEN05), but its

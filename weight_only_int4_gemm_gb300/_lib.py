@@ -34,6 +34,7 @@ SIGNATURES = {
     "w4a16_gemm": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
     "w4a16_gemm_path": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_dequant_ref": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
+    "w4a16_gemm_static_scratch": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),
     "w4a16_select_path": (_I, [_I, _I, _I]),
     "w4a16_debug_forced_timeout": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_device_status": (_I, [_I]),

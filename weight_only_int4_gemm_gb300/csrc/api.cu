@@ -119,6 +119,18 @@ w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, in
 
 }  // namespace
 
+int gemm_entry(const void* x, const void* packed, const void* scales, int has_zeros, void* y,
+               int B, int K, int N, int group_size, void* workspace, size_t ws_bytes, int path,
+               void* stream) {
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     path, stream);
+}
+
+size_t auto_workspace_bytes(int B, int K, int N, int group_size) {
+    if (group_size != kGroup || !shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
+    return path_workspace(choose_path(B, K, N), B, K, N);
+}
+
 cudaError_t launch_with_pdl(const void* func, dim3 grid, dim3 block, size_t smem,
                             cudaStream_t stream, void** args) {
     cudaLaunchConfig_t cfg = {};

@@ -74,4 +74,12 @@ cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void*
                                      cudaStream_t stream);
 bool tc_available();
 
+// Validation + dispatch + launch shared by the C entry points (api.cu).
+// Returns a w4a16_status value.
+int gemm_entry(const void* x, const void* packed, const void* scales, int has_zeros, void* y,
+               int B, int K, int N, int group_size, void* workspace, size_t ws_bytes, int path,
+               void* stream);
+// Workspace the automatic path needs for this shape (SIZE_MAX for invalid shapes).
+size_t auto_workspace_bytes(int B, int K, int N, int group_size);
+
 }  // namespace w4a16
