@@ -38,6 +38,7 @@ LAYER = [("qkv", 4096, 6144), ("o_proj", 4096, 4096), ("gate_up", 4096, 28672),
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
+FORCE = -1  # kernel path forced from the command line (-1: the library's choice)
 
 
 # --------------------------------------------------------------- workloads
@@ -222,7 +223,7 @@ def run_gpu(args, gemms, rank, world, device):
     ws = torch.zeros(max(w.w4a16_workspace_bytes(B, K, N) for _, B, K, N, _, _ in gemms) + 256,
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device)
-    paths = [w.w4a16_select_path(B, K, N) for _, B, K, N, _, _ in gemms]
+    paths = [w.w4a16_select_path(B, K, N) if FORCE < 0 else FORCE for _, B, K, N, _, _ in gemms]
 
     counter = {"i": 0}
     pick = copy_index(gemms, uses, n_copies)
@@ -232,7 +233,7 @@ def run_gpu(args, gemms, rank, world, device):
         for i, (label, B, K, N, zp, _) in enumerate(gemms):
             packed, sc = layers[(K, N, zp)][pick(counter["i"], i, (K, N, zp))]
             x, y = acts[i]
-            w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream)
+            w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream, path=FORCE)
         counter["i"] += 1
 
     # capture one CUDA graph per copy rotation so launch overhead stays off the clock
@@ -277,13 +278,13 @@ def run_gpu(args, gemms, rank, world, device):
     assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
 
     if args.per_gemm:
-        per_gemm_table(gemms, layers, ws, stream, device, load_peaks()[0])
+        per_gemm_table(gemms, layers, ws, stream, device, load_peaks()[0], path=FORCE)
     # end to end through the public API with host buffers
     e2e = run_e2e(args, gemms, layers, device, ws, pick)
     return ms, clk.summary(), paths, n_copies, e2e
 
 
-def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200):
+def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200, path=-1):
     """Each distinct (B, K, N) alone, in a CUDA graph of `reps` launches that
     rotate over the weight copies; prints one line per GEMM to stderr."""
     import torch
@@ -302,13 +303,13 @@ def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200):
         with torch.cuda.stream(stream):
             for r in range(3):
                 packed, sc = reps_list[r % len(reps_list)]
-                w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream)
+                w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream, path=path)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r in range(reps):
                 packed, sc = reps_list[r % len(reps_list)]
-                w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream)
+                w.w4a16_gemm(x, packed, sc, zp, N, out=y, workspace=ws, stream=stream, path=path)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             for _ in range(2):
@@ -320,7 +321,8 @@ def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200):
         us = e0.elapsed_time(e1) * 1e3 / reps
         byts = model.linear_bytes(B, K, N, zp)
         fl = model.linear_flops(B, K, N)
-        print(f"per-gemm B={B:5d} K={K:6d} N={N:6d} zp={int(zp)} path={w.PATH_NAMES[w.w4a16_select_path(B, K, N)]:8s} "
+        pname = w.PATH_NAMES[w.w4a16_select_path(B, K, N) if path < 0 else path]
+        print(f"per-gemm B={B:5d} K={K:6d} N={N:6d} zp={int(zp)} path={pname:8s} "
               f"{us:9.2f} us  {byts / us / 1e3:8.1f} GB/s ({byts / us / 1e3 / hbm_gbs * 100:5.1f}% hbm)  "
               f"{fl / us / 1e6:8.1f} TFLOP/s", file=sys.stderr, flush=True)
 
@@ -430,9 +432,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--force-path", choices=["skinny", "tcgen05"], default=None,
+                    help="force one kernel path (ablations; default: the library's choice)")
     ap.add_argument("--per-gemm", action="store_true",
                     help="also time each distinct GEMM alone (table on stderr)")
     args = ap.parse_args()
+    global FORCE
+    FORCE = {"skinny": 0, "tcgen05": 1}.get(args.force_path, -1)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
@@ -518,7 +524,9 @@ def main():
         launch_s = t_step * len(dom_idx) / len(gemms) / len(dom_idx)  # apportioned
     per_launch_bytes = dom_bytes / len(dom_idx)
     per_launch_flops = dom_flops / len(dom_idx)
-    if dom_name == "skinny":
+    # the bound is whichever side of the roofline the work sits on, not the kernel
+    memory_bound = per_launch_bytes / (hbm * 1e9) >= per_launch_flops / (tf_sust * 1e12)
+    if memory_bound:
         achieved = per_launch_bytes / launch_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs"}

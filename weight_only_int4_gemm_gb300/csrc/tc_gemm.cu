@@ -15,18 +15,21 @@
 //     += W^T[128][64 k] (bf16, smem, dequantised by producer warps)
 //      . X^T[64 k][bn]  (bf16, smem, TMA from x[B][K])
 // Persistent CTAs (one per SM) take work items (column tile, batch tile, K
-// split) round robin and stream K in 64-row blocks through a ring of kSlots
-// shared-memory slots.  Warp roles:
+// split) round robin and stream K in 64-row blocks through two rings: a deep
+// ring of packed-code + x stages (as deep as shared memory allows: ~27 stages
+// at bn = 16, enough bytes in flight to stream weights at HBM speed when the
+// batch is small) and a ring of 4 dequantised weight tiles.  Warp roles:
 //   warp 0      : TMA thread -- bulk-copies the packed codes of the block (one
 //                 contiguous copy) and tensor-copies the x block (128-byte
 //                 swizzle), one mbarrier with the expected byte count per slot;
 //   warp 1      : TMEM allocator + the single MMA-issuing thread
 //                 (tcgen05.mma kind::f16, 4 x K=16 per block, commit per slot
 //                 to "empty" and per item to the accumulator's "full");
-//   warps 2..9  : dequant producers -- packed codes (smem) -> lop3 magic
-//                 decode -> bf16 (q - z) * s -> 128-byte-swizzled K-major
-//                 rows of the weight tile; proxy fence; arrive;
-//   warps 10..13: epilogue (tcgen05.ld 32 lanes x 16 columns -> bf16 y, or
+//   warps 2..17 : dequant producers, two groups of 8 warps taking alternate
+//                 stages -- packed codes (smem) -> lop3 magic decode -> bf16
+//                 (q - z) * s -> 128-byte-swizzled K-major rows of the weight
+//                 tile; proxy fence; arrive;
+//   warps 18..21: epilogue (tcgen05.ld 32 lanes x 16 columns -> bf16 y, or
 //                 fp32 split-K reductions), one TMEM lane quadrant each.
 // Two TMEM accumulators alternate between items, so the epilogue of one item
 // overlaps the main loop of the next.
@@ -44,14 +47,17 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kBlockK = 64;                  // K rows per pipeline slot
+constexpr int kBlockK = 64;                  // K rows per pipeline stage
 constexpr int kTileN = 128;                  // weight columns per tile (MMA M)
-constexpr int kSlots = 4;
+constexpr int kASlots = 4;                   // ring of dequantised weight tiles
+constexpr int kMaxRawSlots = 32;             // ring of packed codes + x tiles
+constexpr size_t kSmemBudget = 227 * 1024;
 constexpr int kDequantWarp0 = 2;
-constexpr int kDequantWarps = 8;
-constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantWarps;  // warps 10..13
+constexpr int kDequantGroups = 2;            // groups of 8 warps take alternate stages
+constexpr int kDequantWarps = 8;             // warps per group (one weight tile each)
+constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;  // 18..21
 constexpr int kNumWarps = kEpilogueWarp0 + 4;
-constexpr int kThreads = 32 * kNumWarps;     // 448
+constexpr int kThreads = 32 * kNumWarps;     // 704
 constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
 constexpr uint32_t kRawBytes = kTileN * kBlockK / 2;     // 4 KB of packed codes
 constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
@@ -72,6 +78,7 @@ struct Args {
     int nkb;            // total K blocks (K / 64)
     int col_tiles, batch_tiles, items;
     uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= max(32, bn))
+    int raw_slots;      // depth of the codes + x ring
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
 };
 
@@ -127,6 +134,14 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+
+// Inline fast path: one try_wait, the bounded loop only if the phase is not
+// complete yet.
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* status, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, abort, status, limit_ns);
 }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -214,18 +229,21 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 // ------------------------------------------------------------ kernel
 
 struct SharedTail {
-    uint64_t full_tma[kSlots];   // TMA bytes landed (codes + x)
-    uint64_t full_ops[kSlots];   // weight tile dequantised (8 warp arrivals)
-    uint64_t empty[kSlots];      // MMAs reading the slot finished (commit)
-    uint64_t tmem_full[2];       // accumulator complete (commit)
-    uint64_t tmem_empty[2];      // accumulator drained by the epilogue (4 warps)
-    uint64_t never;              // test hook: nobody arrives here
+    uint64_t raw_full[kMaxRawSlots];   // TMA bytes landed (codes + x)
+    uint64_t raw_empty[kMaxRawSlots];  // MMAs of the stage finished (commit)
+    uint64_t a_full[kASlots];          // weight tile dequantised (8 warp arrivals)
+    uint64_t a_empty[kASlots];         // MMAs reading the weight tile finished (commit)
+    uint64_t tmem_full[2];             // accumulator complete (commit)
+    uint64_t tmem_empty[2];            // accumulator drained by the epilogue (4 warps)
+    uint64_t never;                    // test hook: nobody arrives here
     uint32_t tmem_base;
     int abort;
 };
 
-__host__ __device__ constexpr uint32_t slot_bytes(int bn) {
-    return kATileBytes + (uint32_t)bn * kBlockK * 2 + kRawBytes;
+// Shared memory: [kASlots weight tiles of 16 KB][raw_slots x (x tile bn*128 B,
+// packed codes 4 KB)][tail]; every operand tile starts on a 1024-byte boundary.
+__host__ __device__ constexpr uint32_t raw_slot_bytes(int bn) {
+    return (uint32_t)bn * kBlockK * 2 + kRawBytes;
 }
 
 struct Item {
@@ -256,22 +274,27 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const uint32_t sbytes = slot_bytes(a.bn);
-    SharedTail* tail = reinterpret_cast<SharedTail*>(smem + kSlots * sbytes);
+    const int R = a.raw_slots;
+    const uint32_t rbytes = raw_slot_bytes(a.bn);
+    uint8_t* raw_base = smem + kASlots * kATileBytes;
+    SharedTail* tail = reinterpret_cast<SharedTail*>(raw_base + R * rbytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = &tail->abort;
 
-    auto a_tile = [&](int s) { return smem + s * sbytes; };
-    auto x_tile = [&](int s) { return smem + s * sbytes + kATileBytes; };
-    auto raw_tile = [&](int s) { return smem + s * sbytes + kATileBytes + a.bn * kBlockK * 2; };
+    auto a_tile = [&](int sa) { return smem + sa * kATileBytes; };
+    auto x_tile = [&](int s) { return raw_base + s * rbytes; };
+    auto raw_tile = [&](int s) { return raw_base + s * rbytes + a.bn * kBlockK * 2; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(smem_u32(&tail->full_tma[s]), 1);
-            mbar_init(smem_u32(&tail->full_ops[s]), kDequantWarps);
-            mbar_init(smem_u32(&tail->empty[s]), 1);
+        for (int s = 0; s < R; ++s) {
+            mbar_init(smem_u32(&tail->raw_full[s]), 1);
+            mbar_init(smem_u32(&tail->raw_empty[s]), 1);
+        }
+        for (int s = 0; s < kASlots; ++s) {
+            mbar_init(smem_u32(&tail->a_full[s]), kDequantWarps);
+            mbar_init(smem_u32(&tail->a_empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tail->tmem_full[b]), 1);
@@ -292,43 +315,66 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tail->tmem_base;
-    // the next kernel on the stream may start now; this one reads x and writes
-    // y / workspace only after the previous kernel has finished (the TMA
-    // thread waits; everything else is ordered after it through mbarriers)
+    // The next kernel on the stream may start now.  This one writes y and the
+    // workspace, and reads x, only after the previous kernel has finished: the
+    // TMA thread waits before its first x copy, and everything else is ordered
+    // after that through mbarriers.  The packed codes do not depend on the
+    // previous kernel, so the first stages' code copies go out before.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ---------------- TMA producer
         if (lane == 0) {
+            const uint32_t xbytes = (uint32_t)a.bn * kBlockK * 2;
+            const Item first = decode_item(a, blockIdx.x);
+            const int pre = min(R, first.nkb);
+            for (int i = 0; i < pre; ++i) {
+                const uint32_t bar = smem_u32(&tail->raw_full[i]);
+                const uint32_t cb = 2u * (uint32_t)first.nvalid * 16;  // two 32-row chunks
+                mbar_arrive_expect_tx(bar, cb + xbytes);
+                bulk_g2s(smem_u32(raw_tile(i)),
+                         a.packed + packed_tile_base(a.K, first.col_tile) +
+                             (size_t)(2 * (first.kb_begin + i)) * first.nvalid * 16,
+                         cb, bar);
+            }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             int stage = 0, issued = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
                 const Item t = decode_item(a, it);
-                const uint32_t raw_block = 2u * (uint32_t)t.nvalid * 16;  // two 32-row chunks
-                const uint32_t tx = raw_block + (uint32_t)a.bn * kBlockK * 2;
+                const uint32_t cb = 2u * (uint32_t)t.nvalid * 16;
                 const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, t.col_tile);
                 for (int i = 0; i < t.nkb; ++i, ++stage) {
-                    const int s = stage % kSlots;
-                    if (stage >= kSlots &&
-                        !wait_bounded(smem_u32(&tail->empty[s]), ((stage / kSlots) - 1) & 1, abort,
-                                      a.status, kTimeoutNs)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t bar = smem_u32(&tail->full_tma[s]);
+                    const int s = stage % R;
+                    const uint32_t bar = smem_u32(&tail->raw_full[s]);
                     const int kb = t.kb_begin + i;
-                    mbar_arrive_expect_tx(bar, tx);
-                    bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * t.nvalid * 16,
-                             raw_block, bar);
+                    if (stage >= pre) {
+                        if (stage >= R &&
+                            !wait_bounded(smem_u32(&tail->raw_empty[s]), ((stage / R) - 1) & 1,
+                                          abort, a.status, kTimeoutNs)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar, cb + xbytes);
+                        bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * t.nvalid * 16,
+                                 cb, bar);
+                    }
                     tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, t.b0, bar);
                     issued = stage + 1;
                 }
             }
-            // after an expired wait, the copies in flight must land before exit
-            for (int i = max(0, issued - kSlots); !ok && i < issued; ++i)
-                wait_bounded(smem_u32(&tail->full_tma[i % kSlots]), (i / kSlots) & 1, abort,
-                             a.status, kTimeoutNs);
+            // After an expired wait, every copy in flight must land before the
+            // CTA exits; stages whose code copy went out early still need their
+            // x copy for the barrier to complete.
+            if (!ok) {
+                for (int i = issued; i < pre; ++i)
+                    tma_load_2d(smem_u32(x_tile(i)), &xmap, (first.kb_begin + i) * kBlockK, first.b0,
+                                smem_u32(&tail->raw_full[i]));
+                const int last = max(issued, pre);
+                for (int i = max(0, last - R); i < last; ++i)
+                    wait_bounded(smem_u32(&tail->raw_full[i % R]), (i / R) & 1, abort, a.status,
+                                 kTimeoutNs);
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
@@ -350,21 +396,24 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 tc_fence_after();
                 const uint32_t tmem_d = tmem_base + acc * a.acc_cols;
                 for (int i = 0; i < t.nkb; ++i, ++stage) {
-                    const int s = stage % kSlots;
-                    const uint32_t ph = (stage / kSlots) & 1;
-                    if (!wait_bounded(smem_u32(&tail->full_tma[s]), ph, abort, a.status, kTimeoutNs) ||
-                        !wait_bounded(smem_u32(&tail->full_ops[s]), ph, abort, a.status, kTimeoutNs)) {
+                    const int s = stage % R;
+                    const int sa = stage % kASlots;
+                    if (!wait_fast(smem_u32(&tail->raw_full[s]), (stage / R) & 1, abort, a.status,
+                                   kTimeoutNs) ||
+                        !wait_fast(smem_u32(&tail->a_full[sa]), (stage / kASlots) & 1, abort,
+                                   a.status, kTimeoutNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t abase = smem_u32(a_tile(s));
+                    const uint32_t abase = smem_u32(a_tile(sa));
                     const uint32_t xbase = smem_u32(x_tile(s));
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk)
                         mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
                                     smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
-                    mma_commit(smem_u32(&tail->empty[s]));
+                    mma_commit(smem_u32(&tail->a_empty[sa]));
+                    mma_commit(smem_u32(&tail->raw_empty[s]));
                 }
                 mma_commit(smem_u32(&tail->tmem_full[acc]));  // fires once this item's MMAs are done
             }
@@ -376,8 +425,11 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             }
         }
     } else if (warp < kEpilogueWarp0) {
-        // ---------------- dequant producers (warps 2..9)
-        const int t256 = threadIdx.x - 32 * kDequantWarp0;  // 0..255
+        // ---------------- dequant producers (warps 2..17): two groups of 8 warps
+        // take alternate stages, so two weight tiles are decoded at a time
+        const int dw = warp - kDequantWarp0;
+        const int grp = dw / kDequantWarps;                  // stage parity handled
+        const int t256 = (dw % kDequantWarps) * 32 + lane;   // 0..255 within the group
         const int r = t256 & (kTileN - 1);                   // weight column within the tile
         const int h = t256 >> 7;                             // which 32-row chunk of the block
         int stage = 0;
@@ -385,36 +437,26 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
             const Item t = decode_item(a, it);
             const int n = min(t.n0 + r, a.N - 1);
-            // scale / zero-point of the current group, and the next group's
-            // already in flight (two K blocks per group hide the load latency)
-            const int g_last = (t.kb_begin + t.nkb - 1) >> 1;
-            int cur_g = t.kb_begin >> 1;
-            uint16_t s_next = __ldg(a.scales + (size_t)cur_g * a.N + n);
-            uint32_t z_next = kHasZeros ? load_zero(a.zeros, a.N, cur_g, n) : 8u;
-            uint32_t s2 = 0, z2 = kSymmetricZeroPair;
-            cur_g -= 1;
             for (int i = 0; i < t.nkb; ++i, ++stage) {
-                const int s = stage % kSlots;
-                const int kb = t.kb_begin + i;
-                const int g = kb >> 1;  // two 64-row blocks per group of 128
-                if (g != cur_g) {
-                    s2 = scale_pair(s_next);
-                    if (kHasZeros) z2 = zero_pair(z_next);
-                    cur_g = g;
-                    if (g < g_last) {
-                        s_next = __ldg(a.scales + (size_t)(g + 1) * a.N + n);
-                        if (kHasZeros) z_next = load_zero(a.zeros, a.N, g + 1, n);
-                    }
-                }
-                const bool landed = wait_bounded(smem_u32(&tail->full_tma[s]), (stage / kSlots) & 1,
-                                                 abort, a.status, kTimeoutNs);
+                if ((stage & 1) != grp) continue;
+                const int s = stage % R;
+                const int sa = stage % kASlots;
+                const int g = (t.kb_begin + i) >> 1;  // two 64-row blocks per group of 128
+                const uint32_t s2 = scale_pair(__ldg(a.scales + (size_t)g * a.N + n));
+                const uint32_t z2 = kHasZeros ? zero_pair(load_zero(a.zeros, a.N, g, n))
+                                              : kSymmetricZeroPair;
+                bool landed = wait_fast(smem_u32(&tail->raw_full[s]), (stage / R) & 1, abort,
+                                        a.status, kTimeoutNs);
+                if (landed && stage >= kASlots)
+                    landed = wait_fast(smem_u32(&tail->a_empty[sa]), ((stage / kASlots) - 1) & 1,
+                                       abort, a.status, kTimeoutNs);
                 if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
                     ok = false;
                     break;
                 }
                 const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * t.nvalid + min(r, t.nvalid - 1)];
                 const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-                uint8_t* row = a_tile(s) + r * 128;
+                uint8_t* row = a_tile(sa) + r * 128;
 #pragma unroll
                 for (int jw = 0; jw < 4; ++jw) {
                     uint32_t p[4];
@@ -424,7 +466,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&tail->full_ops[s]));
+                if (lane == 0) mbar_arrive(smem_u32(&tail->a_full[sa]));
             }
         }
     } else {
@@ -552,7 +594,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-size_t smem_bytes(int bn) { return (size_t)kSlots * slot_bytes(bn) + sizeof(SharedTail) + 1024; }
+int raw_slots_for(int bn) {
+    const size_t avail = kSmemBudget - 1024 - sizeof(SharedTail) - (size_t)kASlots * kATileBytes;
+    return (int)std::min<size_t>(kMaxRawSlots, avail / raw_slot_bytes(bn));
+}
+
+size_t smem_bytes(int bn) {
+    return (size_t)kASlots * kATileBytes + (size_t)raw_slots_for(bn) * raw_slot_bytes(bn) +
+           sizeof(SharedTail) + 1024;
+}
 
 uint32_t acc_cols_for(int bn) {
     uint32_t c = 32;
@@ -649,6 +699,7 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     a.batch_tiles = p.batch_tiles;
     a.items = p.col_tiles * p.batch_tiles * p.split;
     a.acc_cols = acc_cols_for(p.bn);
+    a.raw_slots = raw_slots_for(p.bn);
     a.force_timeout = force_timeout_ms;
 
     const size_t smem = smem_bytes(p.bn);
