@@ -383,7 +383,7 @@ class OracleSampler:
             return t.view(__import__("torch").int16).numpy().view(np.uint16) \
                 if str(t.dtype) == "torch.bfloat16" else t.numpy().view(np.uint32)
 
-        self.MAX_COLS = 4096
+        self.MAX_COLS = 16384
         self.np, self.oracle, self.gemms = np, oracle, gemms
         self.probs = []
         for i, (label, B, K, N, zp, outl) in enumerate(gemms):
@@ -402,7 +402,7 @@ class OracleSampler:
         return est
 
     def calibrate(self, seconds_per_step: float):
-        """Grow the column sample (1 .. 4096) until one sampled step costs about
+        """Grow the column sample (1 .. 16384) until one sampled step costs about
         ``seconds_per_step`` of CPU time."""
         while self.cols < self.MAX_COLS:
             t0 = time.perf_counter()
@@ -415,6 +415,23 @@ class OracleSampler:
         return (f"{self.cols} column(s) of each of the {len(self.gemms)} GEMMs of one step "
                 f"(all rows, all K), timed and scaled by N/columns; {steps} sampled step(s), "
                 f"{seconds:.1f} s of CPU work")
+
+
+def reduce_times_over_ranks(ms: float, e2e_step_ms: float, world: int, device=None):
+    """Replicas run independently; the job takes as long as the slowest rank,
+    so both timings are reduced with MAX over ranks (no data-path collective)."""
+    if world <= 1:
+        return ms, e2e_step_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, e2e_step_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0]), float(t[1])
+
+
+def aggregate_value(bytes_per_step: int, world: int, step_s: float) -> float:
+    """Whole-job TB/s: every replica streams its own step's bytes."""
+    return bytes_per_step * world / step_s / 1e12
 
 
 # --------------------------------------------------------------- main
@@ -500,15 +517,10 @@ def main():
 
     import weight_only_int4_gemm_gb300 as w
     ms, clocks, paths, n_copies, (e2e_ms, e2e_steps, h2d, d2h) = run_gpu(args, gemms, rank, world, device)
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms / e2e_steps], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_step_ms = float(t[0]), float(t[1])
-    else:
-        e2e_step_ms = e2e_ms / e2e_steps
+    ms, e2e_step_ms = reduce_times_over_ranks(ms, e2e_ms / e2e_steps, world, device)
 
     t_step = ms / 1e3 / args.steps
-    value = sbytes * world / t_step / 1e12
+    value = aggregate_value(sbytes, world, t_step)
     # roofline for the dominant kernel: every launch of the step is one GEMM;
     # the graph replays them back to back, so the mean launch time is the
     # timed region over the launches
@@ -557,8 +569,13 @@ def main():
         oracle.build()
         sampler = OracleSampler(gemms)
         sampler.calibrate(args.cpu_budget / 5)
+        # at the column cap one sampled step may cost well under the budget:
+        # repeat it until about cpu_budget seconds of oracle work are done
         t0 = time.perf_counter()
-        runs = [sampler.step() for _ in range(5)]
+        runs = [sampler.step()]
+        per = time.perf_counter() - t0
+        n_runs = max(5, min(500, int(args.cpu_budget / max(per, 1e-3))))
+        runs += [sampler.step() for _ in range(n_runs - 1)]
         t_cpu = statistics.median(runs)
         sample = sampler.describe(len(runs), time.perf_counter() - t0)
         line["cpu_baseline"] = {"value": sbytes / t_cpu / 1e12, "unit": "TB/s",
