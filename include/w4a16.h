@@ -56,7 +56,7 @@ extern "C" {
 #endif
 
 #define W4A16_GROUP 128
-#define W4A16_PACKED_LAYOUT 2 /* version tag of the packed blob's layout */
+#define W4A16_PACKED_LAYOUT 3 /* version tag of the packed blob's layout */
 
 typedef enum {
     W4A16_OK = 0,
@@ -73,12 +73,15 @@ typedef enum {
 /* Kernel paths the dispatcher chooses from (w4a16_select_path, forcing). */
 typedef enum {
     W4A16_PATH_AUTO = -1,
-    W4A16_PATH_SKINNY = 0,  /* memory-bound small-batch split-K kernel */
-    W4A16_PATH_TCGEN05 = 1  /* compute-bound tcgen05/TMEM tensor-core kernel */
+    W4A16_PATH_SKINNY = 0,  /* small-batch split-K kernel (mma.sync), B <= 16 */
+    W4A16_PATH_TCGEN05 = 1  /* tcgen05 tensor-core kernels (weight tile in TMEM up to
+                               128 batch rows, in shared memory above) */
 } w4a16_path;
 
 /* Bytes of the packed blob for a K x N layer (codes, plus zero-points when
- * has_zeros != 0): K*N/2 [+ (K/128)*(N/8)*4].  Returns 0 for invalid shapes. */
+ * has_zeros != 0): K*N/2 [+ (K/128)*R*4], where R = N/8 rounded up to a
+ * multiple of 4 (each group's row of zero-point words is padded to 16 bytes).
+ * Returns 0 for invalid shapes. */
 size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros);
 
 /* Bytes of device workspace w4a16_gemm needs for this shape (0 if none).

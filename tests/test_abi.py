@@ -40,6 +40,9 @@ def test_every_declared_symbol_is_exported(lib):
 def test_packed_bytes():
     assert w.w4a16_packed_bytes(4096, 4096, False) == 4096 * 4096 // 2
     assert w.w4a16_packed_bytes(4096, 4096, True) == 4096 * 4096 // 2 + 32 * 512 * 4
+    # zero-point rows are padded to a multiple of 4 words (16 bytes)
+    assert w.w4a16_packed_bytes(128, 8, True) == 128 * 8 // 2 + 1 * 4 * 4
+    assert w.w4a16_packed_bytes(256, 4104, True) == 256 * 4104 // 2 + 2 * 516 * 4
     lib = _lib.load()
     assert lib.w4a16_packed_bytes(100, 4096, 128, 0) == 0
     assert lib.w4a16_packed_bytes(128, 12, 128, 0) == 0

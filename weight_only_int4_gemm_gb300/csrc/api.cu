@@ -67,9 +67,11 @@ int num_sms() {
 }
 
 // Batch above which the tensor-core kernel takes over from the split-K
-// kernel (the split-K kernel pads the batch to 8/16/32 rows and re-streams
-// the weights for every further 32 rows).
-constexpr int kSkinnyMaxB = 32;
+// kernel.  Measured on GB300 (decoder-layer shapes): the mma.sync kernel is
+// faster up to 8 rows, the two are even at 16, and from 17 rows (where the
+// mma.sync kernel needs 32-row batch tiles) the tensor-core kernel is 1.7x
+// faster.
+constexpr int kSkinnyMaxB = 16;
 
 int choose_path(int B, int K, int N) {
     (void)K;

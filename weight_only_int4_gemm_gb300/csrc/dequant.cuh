@@ -9,7 +9,7 @@
 // multiply by the group scale then gives w = RNE_bf16((q - z) * s).  One
 // lop3 builds two such values at once, one in each 16-bit half.
 //
-// Packed layout (version W4A16_PACKED_LAYOUT = 2):
+// Packed layout (version W4A16_PACKED_LAYOUT = 3):
 //   codes: the N columns are cut into tiles of 128 (the last tile holds
 //   w = N - 128*t columns when N is not a multiple of 128).  Tile t starts at
 //   byte 64*K*t; inside it, chunk c (rows 32c .. 32c+31) is w consecutive
@@ -20,8 +20,10 @@
 //   (2i, 2i+1) (offsets within the word) sit in nibbles i and i + 4, i.e. in
 //   the low and high 16-bit halves at the same bit offset 4i, so
 //        (word >> 4i) & 0x000F000F  ==  { code(2i), code(2i+1) }.
-//   zeros (asymmetric format only): the canonical uint32 [K/128][N/8] array,
-//   copied unchanged after the codes.
+//   zeros (asymmetric format only): the canonical uint32 [K/128][N/8] words,
+//   after the codes, one group per row, each row padded with zero words to a
+//   multiple of 4 words (16 bytes), so the zero-points of any 128-column tile
+//   of a group are one 16-byte-aligned block a bulk copy can fetch.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -105,9 +107,12 @@ __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t zero2, uint
     for (int i = 0; i < 4; ++i) out[i] = dequant_pair(word, i, zero2, scale2);
 }
 
-// Zero-point nibble of column n, group g, from the canonical zeros array.
+// Words per group row of the packed zero-points (N/8 rounded up to 4).
+__host__ __device__ inline int packed_zero_row_words(int N) { return ((N >> 3) + 3) & ~3; }
+
+// Zero-point nibble of column n, group g, from the packed zero-points.
 __device__ __forceinline__ uint32_t load_zero(const uint32_t* zeros, int N, int g, int n) {
-    const uint32_t w = __ldg(zeros + (size_t)g * (N >> 3) + (n >> 3));
+    const uint32_t w = __ldg(zeros + (size_t)g * packed_zero_row_words(N) + (n >> 3));
     return (w >> (4 * (n & 7))) & 0xFu;
 }
 

@@ -10,7 +10,10 @@ namespace w4a16 {
 constexpr int kGroup = 128;
 
 inline size_t packed_code_bytes(int K, int N) { return (size_t)K * (size_t)N / 2; }
-inline size_t packed_zero_bytes(int K, int N) { return (size_t)(K / kGroup) * (size_t)(N / 8) * 4; }
+// Zero-point rows: N/8 words padded to a multiple of 4 (dequant.cuh).
+inline size_t packed_zero_bytes(int K, int N) {
+    return (size_t)(K / kGroup) * (size_t)(((N / 8) + 3) & ~3) * 4;
+}
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace layout shared by every kernel: a fixed prefix of counters
@@ -62,6 +65,11 @@ struct TcPlan {
     int kb_per_split;// 64-row K blocks per split
     int split;       // K splits (1 = no workspace)
     int grid;        // persistent CTAs
+    int issuers;     // MMA-issuing threads, each with its own accumulator (1, 2, 4)
+    int bufs;        // accumulator sets alternating between items (1, 2)
+    int a_slots;     // dequantised weight tiles held in TMEM
+    int nsub;        // 64-row K blocks per copy stage
+    bool wide;       // more than 128 batch rows: the single-issuer kernel (tc_wide.cu)
 };
 TcPlan plan_tc(int B, int K, int N, int num_sms);
 size_t tc_workspace_bytes(const TcPlan& p, int B, int N);
@@ -73,6 +81,12 @@ cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void*
                                      int N, void* workspace, unsigned int* status, int wait_ms,
                                      cudaStream_t stream);
 bool tc_available();
+// wide batches (tc_wide.cu); plan_tc() routes there and launch_tc() follows the plan
+TcPlan plan_tc_wide(int B, int K, int N, int num_sms);
+cudaError_t launch_tc_wide(const TcPlan& p, const void* x, const void* packed,
+                           const void* scales, bool has_zeros, void* y, int B, int K, int N,
+                           void* workspace, unsigned int* status, int force_timeout_ms,
+                           cudaStream_t stream);
 
 // Validation + dispatch + launch shared by the C entry points (api.cu).
 // Returns a w4a16_status value.

@@ -64,9 +64,13 @@ cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K
     repack_kernel<<<grid, kPackThreads, 0, stream>>>(qweight, static_cast<uint4*>(packed), K, N);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || qzeros == nullptr) return err;
-    const size_t zero_bytes = (size_t)(K / 128) * (size_t)(N / 8) * 4;
-    return cudaMemcpyAsync(static_cast<char*>(packed) + packed_code_bytes(K, N), qzeros,
-                           zero_bytes, cudaMemcpyDeviceToDevice, stream);
+    // zero-points: one group per row, rows padded with zero words to 16 bytes
+    char* zdst = static_cast<char*>(packed) + packed_code_bytes(K, N);
+    err = cudaMemsetAsync(zdst, 0, packed_zero_bytes(K, N), stream);
+    if (err != cudaSuccess) return err;
+    const size_t row_bytes = (size_t)(N / 8) * 4;
+    return cudaMemcpy2DAsync(zdst, (size_t)packed_zero_row_words(N) * 4, qzeros, row_bytes,
+                             row_bytes, (size_t)(K / 128), cudaMemcpyDeviceToDevice, stream);
 }
 
 cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,

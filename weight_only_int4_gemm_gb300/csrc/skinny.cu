@@ -325,7 +325,7 @@ skinny_kernel(const Args a) {
                                 a.scales + (size_t)(g0 + gl) * a.N + w.n0 + 8 * p);
                     if (kHasZeros)
                         cp_async_4(smem_u32(slot_zeros(s)) + 4u * (gl * (kTileCols / 8) + p),
-                                   a.zeros + (size_t)(g0 + gl) * (a.N / 8) + w.n0 / 8 + p);
+                                   a.zeros + (size_t)(g0 + gl) * packed_zero_row_words(a.N) + w.n0 / 8 + p);
                 }
                 cp_async_arrive_noinc(full);
                 issued = step + 1;

@@ -1,39 +1,49 @@
-// tc_gemm.cu -- compute-bound W4A16 GEMM on the 5th-generation tensor cores
-// (tcgen05 MMA with TMEM accumulators, TMA-fed operands), for large batches.
+// tc_gemm.cu -- W4A16 GEMM on the 5th-generation tensor cores (tcgen05 MMA,
+// TMA-fed activations), with the dequantised weight tile held in tensor memory.
 //
 // "Give Me BF16 or Give Me Death" (summary), "Inference with W4A16": the
 // 4-bit weights are rebuilt to 16-bit values inside the matrix
 // multiplication and multiplied on 16-bit tensor cores with higher-precision
-// accumulation; at large batch the layer is compute-bound.  "When
-// quantization pays -- and when it does not" (model of a decode step): the
-// dequantisation runs on the CUDA cores and is only free while another pipe is
-// longer -- so here it runs in dedicated producer warps, overlapped with the
-// asynchronous tensor pipe.
+// accumulation.  "When quantization pays -- and when it does not" (model of a
+// decode step): the dequantisation runs on the CUDA cores and is only free
+// while another pipe is longer -- so here it runs in dedicated warps,
+// overlapped with the asynchronous copy and tensor pipes.
 //
 // Tile (operands swapped so the weight tile is the 128-row MMA operand):
 //   D[128 weight columns][bn batch rows] (fp32, TMEM)
-//     += W^T[128][64 k] (bf16, smem, dequantised by producer warps)
-//      . X^T[64 k][bn]  (bf16, smem, TMA from x[B][K])
+//     += W^T[128][64 k] (bf16, TMEM: lane = weight column, 32-bit column j =
+//                        the k pair (2j, 2j+1), even k in the low half)
+//      . X^T[64 k][bn]  (bf16, smem, 128-byte swizzle, TMA from x[B][K])
+// The weight operand never touches shared memory: each dequant thread owns
+// one weight column (one TMEM lane), decodes its 64 codes of a block into 32
+// bf16 pairs and writes them with two tcgen05.st.
+//
+// Copies: a TMA operation costs a few hundred cycles of the SM's copy engine
+// whatever its size, so the K loop is fed in copy stages of nsub 64-row blocks
+// (nsub = 4 at small bn: 16 KB of packed codes per stage), each stage one bulk
+// copy of codes, one tensor copy of the group scales (and one of the
+// zero-points) and one 3-D tensor copy of all its x blocks; two producer
+// threads take the stages in turn.  Codes and x travel in two rings: a code
+// slot is free as soon as the dequant warps have read it, an x slot once the
+// stage's MMAs finished, so the HBM stream of codes is not held up by the
+// (slow to issue) MMAs.  Dequantisation and MMAs stay per 64-row block,
+// through a ring of weight tiles in TMEM.
+//
 // Persistent CTAs (one per SM) take work items (column tile, batch tile, K
-// split) round robin and stream K in 64-row blocks through two rings: a deep
-// ring of packed-code + x stages (as deep as shared memory allows: ~27 stages
-// at bn = 16, enough bytes in flight to stream weights at HBM speed when the
-// batch is small) and a ring of 4 dequantised weight tiles.  Warp roles:
-//   warp 0      : TMA thread -- bulk-copies the packed codes of the block (one
-//                 contiguous copy) and tensor-copies the x block (128-byte
-//                 swizzle), one mbarrier with the expected byte count per slot;
-//   warp 1      : TMEM allocator + the single MMA-issuing thread
-//                 (tcgen05.mma kind::f16, 4 x K=16 per block, commit per slot
-//                 to "empty" and per item to the accumulator's "full");
-//   warps 2..17 : dequant producers, two groups of 8 warps taking alternate
-//                 stages -- packed codes (smem) -> lop3 magic decode -> bf16
-//                 (q - z) * s -> 128-byte-swizzled K-major rows of the weight
-//                 tile; proxy fence; arrive;
-//   warps 18..21: epilogue (tcgen05.ld 32 lanes x 16 columns -> bf16 y, or
-//                 fp32 split-K reductions), one TMEM lane quadrant each.
-// Two TMEM accumulators alternate between items, so the epilogue of one item
-// overlaps the main loop of the next.
-// Every mbarrier wait is bounded; on expiry the kernel records
+// split) round robin.  Up to four MMA-issuing threads take the copy stages of
+// an item in turn, each into its own accumulator: MMAs issued by one thread
+// run one after another, so at small bn (short MMAs) several issuers keep the
+// tensor pipe busy; the epilogue adds the accumulators.  Warp roles:
+//   warps 0, 25     : TMA producers (copy stages alternate between them);
+//   warps 1-3, 24   : MMA issuers 0-3 (warp 1 also allocates TMEM);
+//   warps 4-7       : epilogue, TMEM lane quadrant = warp % 4;
+//   warps 8-23      : dequant, four groups of four warps taking 64-row blocks
+//                     in turn; warp % 4 is the TMEM lane quadrant it writes.
+// Every role keeps its ring positions as counters stepped once per stage: a
+// role runs on one thread, where a division's dependent chain would cost as
+// much as a stage's MMAs.  Accumulators are double-buffered between items when
+// TMEM has room, so the epilogue of one item overlaps the main loop of the
+// next.  Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT in the device status word, drains and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,39 +57,55 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kBlockK = 64;                  // K rows per pipeline stage
+constexpr int kBlockK = 64;                  // K rows per block (4 MMAs of K = 16)
 constexpr int kTileN = 128;                  // weight columns per tile (MMA M)
-constexpr int kASlots = 4;                   // ring of dequantised weight tiles
-constexpr int kMaxRawSlots = 32;             // ring of packed codes + x tiles
+constexpr int kMaxCodeSlots = 16;            // ring of packed codes + scales + zero-points
+constexpr int kMaxXSlots = 16;               // ring of x tiles
+constexpr int kMaxASlots = 12;               // ring of weight tiles in TMEM
+constexpr int kTmemCols = 512;               // the whole of TMEM (one CTA per SM)
+constexpr int kACols = kBlockK / 2;          // TMEM columns per weight tile
+constexpr int kMaxIssuers = 4;
+constexpr int kMaxTmemBatch = 128;           // wider batches go to tc_wide.cu
+constexpr int kEpilogueWarp0 = 4;            // 4..7
+constexpr int kDequantWarp0 = 8;             // 8..23
+constexpr int kDequantGroups = 4;            // groups of 4 warps (one per quadrant)
+constexpr int kIssuer3Warp = kDequantWarp0 + 4 * kDequantGroups;  // 24
+constexpr int kProducer1Warp = kIssuer3Warp + 1;                  // 25
+constexpr int kNumWarps = kProducer1Warp + 1;
+constexpr int kThreads = 32 * kNumWarps;     // 832
 constexpr size_t kSmemBudget = 227 * 1024;
-constexpr int kDequantWarp0 = 2;
-constexpr int kDequantGroups = 2;            // groups of 8 warps take alternate stages
-constexpr int kDequantWarps = 8;             // warps per group (one weight tile each)
-constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;  // 18..21
-constexpr int kNumWarps = kEpilogueWarp0 + 4;
-constexpr int kThreads = 32 * kNumWarps;     // 704
-constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
-constexpr uint32_t kRawBytes = kTileN * kBlockK / 2;     // 4 KB of packed codes
-constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
-constexpr unsigned int kStatusTimeout = 7;               // W4A16_ERR_TIMEOUT
+constexpr uint32_t kCodeBlockBytes = kTileN * kBlockK / 2;  // 4 KB of codes per block
+constexpr uint32_t kScaleRowBytes = kTileN * 2;             // one group's scales of a tile
+constexpr uint32_t kZeroRowBytes = kTileN / 2;              // one group's zero-points
+constexpr unsigned long long kTimeoutNs = 2000000000ull;    // 2 s per wait
+constexpr unsigned int kStatusTimeout = 7;                  // W4A16_ERR_TIMEOUT
+
+static_assert(kDequantWarp0 % 4 == 0 && kEpilogueWarp0 % 4 == 0,
+              "TMEM lane quadrant of a warp is warp % 4");
 
 struct Args {
     const uint8_t* packed;
-    const uint16_t* scales;
-    const uint32_t* zeros;
     uint16_t* y;
-    float* partial;      // fp32 accumulator [B][N], zero between calls (split > 1)
+    float* partial;        // fp32 accumulator [B][N], zero between calls (split > 1)
     uint32_t* counters;
     unsigned int* status;
     int B, K, N;
-    int bn;             // MMA N (batch rows per tile), multiple of 16
-    int kb_per_split;   // K blocks per split
+    int bn;                // MMA N (batch rows per tile), multiple of 16
+    int nsub;              // 64-row blocks per copy stage (2 or 4)
+    int kb_per_split;      // K blocks per split (multiple of nsub)
     int split;
-    int nkb;            // total K blocks (K / 64)
+    int nkb;               // total K blocks (K / 64)
     int col_tiles, batch_tiles, items;
-    uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= max(32, bn))
-    int raw_slots;      // depth of the codes + x ring
-    int force_timeout;  // test hook: wait on a barrier nobody arrives at
+    int issuers;           // MMA-issuing threads (1, 2 or 4)
+    int bufs;              // accumulator sets (1 or 2)
+    int a_slots;           // weight tiles in TMEM
+    int code_slots;        // code ring depth (even)
+    int x_slots;           // x ring depth (even)
+    uint32_t code_slot_bytes, x_slot_bytes;
+    uint32_t code_base;    // code ring offset (the x ring starts the shared memory)
+    uint32_t scale_off, zero_off;  // offsets inside a code slot (codes at 0)
+    int x3d;               // x of a stage is one 3-D box (else one 2-D box per block)
+    int force_timeout;     // test hook: wait on a barrier nobody arrives at
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -139,9 +165,9 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
 // Inline fast path: one try_wait, the bounded loop only if the phase is not
 // complete yet.
 __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status, unsigned long long limit_ns) {
+                                          unsigned int* status) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_bounded(bar, parity, abort, status, limit_ns);
+    return wait_bounded(bar, parity, abort, status, kTimeoutNs);
 }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -161,8 +187,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -191,13 +222,14 @@ __device__ __forceinline__ uint32_t instr_desc_bf16(int n) {
            ((uint32_t)(kTileN >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+// D (TMEM) += A (TMEM) . B (smem descriptor)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -207,8 +239,23 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 lanes x 16 columns of 32 bits: this thread's 16 registers to its lane.
+__device__ __forceinline__ void tmem_st_16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+          "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+          "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 16 columns of 32 bits, no wait (pair with tmem_ld_wait).
+__device__ __forceinline__ void tmem_ld_16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -216,9 +263,10 @@ __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, float (&v)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
@@ -229,25 +277,24 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 // ------------------------------------------------------------ kernel
 
 struct SharedTail {
-    uint64_t raw_full[kMaxRawSlots];   // TMA bytes landed (codes + x)
-    uint64_t raw_empty[kMaxRawSlots];  // MMAs of the stage finished (commit)
-    uint64_t a_full[kASlots];          // weight tile dequantised (8 warp arrivals)
-    uint64_t a_empty[kASlots];         // MMAs reading the weight tile finished (commit)
-    uint64_t tmem_full[2];             // accumulator complete (commit)
-    uint64_t tmem_empty[2];            // accumulator drained by the epilogue (4 warps)
-    uint64_t never;                    // test hook: nobody arrives here
+    uint64_t code_full[kMaxCodeSlots];      // codes, scales, zero-points of the stage landed
+    uint64_t code_free[kMaxCodeSlots];      // read by the dequant warps (4 per block)
+    uint64_t x_full[kMaxXSlots];            // x blocks of the stage landed
+    uint64_t x_free[kMaxXSlots];            // MMAs of the stage finished (commit)
+    uint64_t a_full[kMaxASlots];            // weight tile in TMEM (4 warp arrivals)
+    uint64_t a_free[kMaxASlots];            // MMAs reading the weight tile finished (commit)
+    uint64_t tmem_full[2];                  // accumulator set complete (one commit per issuer)
+    uint64_t tmem_empty[2];                 // accumulator set drained (4 epilogue warps)
+    uint64_t mma_done[kMaxIssuers];         // final drain of each issuer's MMAs
+    uint64_t never;                         // test hook: nobody arrives here
     uint32_t tmem_base;
     int abort;
+    int s_last;
+    int turn;                               // next copy stage whose waits may start
 };
 
-// Shared memory: [kASlots weight tiles of 16 KB][raw_slots x (x tile bn*128 B,
-// packed codes 4 KB)][tail]; every operand tile starts on a 1024-byte boundary.
-__host__ __device__ constexpr uint32_t raw_slot_bytes(int bn) {
-    return (uint32_t)bn * kBlockK * 2 + kRawBytes;
-}
-
 struct Item {
-    int col_tile, batch_tile, split_idx, n0, b0, nvalid, kb_begin, nkb;
+    int col_tile, batch_tile, n0, b0, nvalid, kb_begin, nkb, ncs;
 };
 
 __device__ __forceinline__ Item decode_item(const Args& a, int it) {
@@ -255,59 +302,125 @@ __device__ __forceinline__ Item decode_item(const Args& a, int it) {
     t.col_tile = it % a.col_tiles;
     const int rest = it / a.col_tiles;
     t.batch_tile = rest % a.batch_tiles;
-    t.split_idx = rest / a.batch_tiles;
+    const int split_idx = rest / a.batch_tiles;
     t.n0 = t.col_tile * kTileN;
     t.b0 = t.batch_tile * a.bn;
     t.nvalid = min(kTileN, a.N - t.n0);
-    t.kb_begin = t.split_idx * a.kb_per_split;
+    t.kb_begin = split_idx * a.kb_per_split;
     t.nkb = min(a.kb_per_split, a.nkb - t.kb_begin);
+    t.ncs = (t.nkb + a.nsub - 1) / a.nsub;
     return t;
 }
+
+// Ring position (slot, parity of the slot's current use), stepped without
+// divisions.
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
 
 __device__ __forceinline__ void epilogue_bar() {  // the 4 epilogue warps only
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
+__device__ __forceinline__ int issuer_of_warp(int warp) {
+    return (warp >= 1 && warp <= 3) ? warp - 1 : (warp == kIssuer3Warp ? 3 : -1);
+}
+
+// Weight copies of copy stage c of item t into a code slot: one bulk copy of
+// the packed codes of its blocks (contiguous in the packed layout), one tensor
+// copy of the scale rows of its groups and, for the asymmetric format, one of
+// the zero-point rows.
+template <bool kHasZeros>
+__device__ __forceinline__ void issue_weight_copies(const Args& a, const CUtensorMap* smap,
+                                                    const CUtensorMap* zmap, const Item& t,
+                                                    int c, uint8_t* slot, uint32_t bar) {
+    const int kb0 = t.kb_begin + c * a.nsub;
+    const int ng = a.nsub > 1 ? a.nsub >> 1 : 1;
+    const uint32_t cb = (uint32_t)a.nsub * 2u * (uint32_t)t.nvalid * 16u;
+    const uint32_t zbytes = kHasZeros ? (uint32_t)ng * kZeroRowBytes : 0u;
+    mbar_arrive_expect_tx(bar, cb + (uint32_t)ng * kScaleRowBytes + zbytes);
+    bulk_g2s(smem_u32(slot),
+             a.packed + packed_tile_base(a.K, t.col_tile) + (size_t)(2 * kb0) * t.nvalid * 16, cb,
+             bar);
+    tma_load_2d(smem_u32(slot + a.scale_off), smap, t.n0, kb0 >> 1, bar);
+    if (kHasZeros) tma_load_2d(smem_u32(slot + a.zero_off), zmap, t.n0 >> 3, kb0 >> 1, bar);
+}
+
+// The x blocks of copy stage c into an x slot.
+__device__ __forceinline__ void issue_x_copies(const Args& a, const CUtensorMap* xmap,
+                                               const Item& t, int c, uint8_t* slot,
+                                               uint32_t bar) {
+    const int kb0 = t.kb_begin + c * a.nsub;
+    mbar_arrive_expect_tx(bar, a.x_slot_bytes);
+    if (a.x3d) {
+        tma_load_3d(smem_u32(slot), xmap, 0, t.b0, kb0, bar);
+    } else {
+        for (int j = 0; j < a.nsub; ++j)
+            tma_load_2d(smem_u32(slot + (size_t)j * a.bn * kBlockK * 2), xmap,
+                        (kb0 + j) * kBlockK, t.b0, bar);
+    }
+}
+
 template <bool kHasZeros>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
+          const __grid_constant__ CUtensorMap zmap, const Args a) {
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled operand tiles
+    // 1024-byte alignment for the swizzled x tiles
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const int R = a.raw_slots;
-    const uint32_t rbytes = raw_slot_bytes(a.bn);
-    uint8_t* raw_base = smem + kASlots * kATileBytes;
-    SharedTail* tail = reinterpret_cast<SharedTail*>(raw_base + R * rbytes);
+    const int RC = a.code_slots;
+    const int RX = a.x_slots;
+    const int SA = a.a_slots;
+    const int I = a.issuers;
+    SharedTail* tail = reinterpret_cast<SharedTail*>(smem + a.code_base +
+                                                     (size_t)RC * a.code_slot_bytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = &tail->abort;
-
-    auto a_tile = [&](int sa) { return smem + sa * kATileBytes; };
-    auto x_tile = [&](int s) { return raw_base + s * rbytes; };
-    auto raw_tile = [&](int s) { return raw_base + s * rbytes + a.bn * kBlockK * 2; };
+    auto x_slot = [&](int s) { return smem + (size_t)s * a.x_slot_bytes; };
+    auto code_slot = [&](int s) { return smem + a.code_base + (size_t)s * a.code_slot_bytes; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < R; ++s) {
-            mbar_init(smem_u32(&tail->raw_full[s]), 1);
-            mbar_init(smem_u32(&tail->raw_empty[s]), 1);
+        for (int s = 0; s < RC; ++s) {
+            mbar_init(smem_u32(&tail->code_full[s]), 1);
+            mbar_init(smem_u32(&tail->code_free[s]), 4 * a.nsub);
         }
-        for (int s = 0; s < kASlots; ++s) {
-            mbar_init(smem_u32(&tail->a_full[s]), kDequantWarps);
-            mbar_init(smem_u32(&tail->a_empty[s]), 1);
+        for (int s = 0; s < RX; ++s) {
+            mbar_init(smem_u32(&tail->x_full[s]), 1);
+            mbar_init(smem_u32(&tail->x_free[s]), 1);
+        }
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(smem_u32(&tail->a_full[s]), 4);
+            mbar_init(smem_u32(&tail->a_free[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&tail->tmem_full[b]), 1);
+            mbar_init(smem_u32(&tail->tmem_full[b]), I);
             mbar_init(smem_u32(&tail->tmem_empty[b]), 4);
         }
+        for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(&tail->mma_done[i]), 1);
         mbar_init(smem_u32(&tail->never), 1);
         tail->abort = 0;
+        tail->turn = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&smap)) : "memory");
+        if (kHasZeros)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&zmap))
+                         : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(&tail->tmem_base)), "r"(2 * a.acc_cols)
+                     ::"r"(smem_u32(&tail->tmem_base)), "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -315,177 +428,287 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tail->tmem_base;
+    const uint32_t a_col0 = (uint32_t)(a.bufs * I * a.bn);  // weight tiles after the accumulators
+    const uint32_t xblock_bytes = (uint32_t)a.bn * kBlockK * 2;
     // The next kernel on the stream may start now.  This one writes y and the
     // workspace, and reads x, only after the previous kernel has finished: the
-    // TMA thread waits before its first x copy, and everything else is ordered
-    // after that through mbarriers.  The packed codes do not depend on the
-    // previous kernel, so the first stages' code copies go out before.
+    // producers wait before their first x copy, and everything else is ordered
+    // after that through mbarriers.  The weights (codes, scales, zero-points)
+    // do not depend on the previous kernel, so the first stages' weight copies
+    // go out before.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        // ---------------- TMA producer
+    const int issuer = issuer_of_warp(warp);
+    if (warp == 0 || warp == kProducer1Warp) {
+        // ---------------- TMA producers: producer pr takes copy stages pr, pr+2, ...
+        const int pr = warp == 0 ? 0 : 1;
         if (lane == 0) {
-            const uint32_t xbytes = (uint32_t)a.bn * kBlockK * 2;
             const Item first = decode_item(a, blockIdx.x);
-            const int pre = min(R, first.nkb);
-            for (int i = 0; i < pre; ++i) {
-                const uint32_t bar = smem_u32(&tail->raw_full[i]);
-                const uint32_t cb = 2u * (uint32_t)first.nvalid * 16;  // two 32-row chunks
-                mbar_arrive_expect_tx(bar, cb + xbytes);
-                bulk_g2s(smem_u32(raw_tile(i)),
-                         a.packed + packed_tile_base(a.K, first.col_tile) +
-                             (size_t)(2 * (first.kb_begin + i)) * first.nvalid * 16,
-                         cb, bar);
-            }
+            const int pre = min(RC, first.ncs);
+            for (int c = pr; c < pre; c += 2)
+                issue_weight_copies<kHasZeros>(a, &smap, &zmap, first, c, code_slot(c),
+                                               smem_u32(&tail->code_full[c]));
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            int stage = 0, issued = 0;
+            int gcs = 0, done_c = 0, done_x = 0;  // stages walked; own stages issued (+1)
+            Ring qc, qx;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
                 const Item t = decode_item(a, it);
-                const uint32_t cb = 2u * (uint32_t)t.nvalid * 16;
-                const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, t.col_tile);
-                for (int i = 0; i < t.nkb; ++i, ++stage) {
-                    const int s = stage % R;
-                    const uint32_t bar = smem_u32(&tail->raw_full[s]);
-                    const int kb = t.kb_begin + i;
-                    if (stage >= pre) {
-                        if (stage >= R &&
-                            !wait_bounded(smem_u32(&tail->raw_empty[s]), ((stage / R) - 1) & 1,
-                                          abort, a.status, kTimeoutNs)) {
+                for (int c = 0; c < t.ncs; ++c, ++gcs, qc.next(RC), qx.next(RX)) {
+                    if ((gcs & 1) != pr) continue;
+                    if (gcs >= pre) {
+                        // a code slot is free once the dequant warps read the stage RC back
+                        if (gcs >= RC && !wait_fast(smem_u32(&tail->code_free[qc.s]), qc.ph ^ 1u,
+                                                    abort, a.status)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(bar, cb + xbytes);
-                        bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * t.nvalid * 16,
-                                 cb, bar);
+                        issue_weight_copies<kHasZeros>(a, &smap, &zmap, t, c, code_slot(qc.s),
+                                                       smem_u32(&tail->code_full[qc.s]));
+                        done_c = gcs + 1;
                     }
-                    tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, t.b0, bar);
-                    issued = stage + 1;
+                    // an x slot is free once the MMAs of the stage RX back finished
+                    if (gcs >= RX && !wait_fast(smem_u32(&tail->x_free[qx.s]), qx.ph ^ 1u, abort,
+                                                a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_x_copies(a, &xmap, t, c, x_slot(qx.s), smem_u32(&tail->x_full[qx.s]));
+                    done_x = gcs + 1;
                 }
             }
             // After an expired wait, every copy in flight must land before the
-            // CTA exits; stages whose code copy went out early still need their
-            // x copy for the barrier to complete.
+            // CTA exits: wait for the latest use of every slot this producer filled.
             if (!ok) {
-                for (int i = issued; i < pre; ++i)
-                    tma_load_2d(smem_u32(x_tile(i)), &xmap, (first.kb_begin + i) * kBlockK, first.b0,
-                                smem_u32(&tail->raw_full[i]));
-                const int last = max(issued, pre);
-                for (int i = max(0, last - R); i < last; ++i)
-                    wait_bounded(smem_u32(&tail->raw_full[i % R]), (i / R) & 1, abort, a.status,
-                                 kTimeoutNs);
+                const int last_c = max(done_c, pre);
+                for (int c = max(0, last_c - RC); c < last_c; ++c)
+                    if ((c & 1) == pr)
+                        wait_bounded(smem_u32(&tail->code_full[c % RC]), (c / RC) & 1, abort,
+                                     a.status, kTimeoutNs);
+                for (int c = max(0, done_x - RX); c < done_x; ++c)
+                    if ((c & 1) == pr)
+                        wait_bounded(smem_u32(&tail->x_full[c % RX]), (c / RX) & 1, abort,
+                                     a.status, kTimeoutNs);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+    } else if (issuer >= 0) {
+        // ---------------- MMA issuers: issuer i takes copy stages i, i+I, ... (counted
+        // over all items of the CTA).  mbarrier waits test only the parity of a
+        // phase, so a barrier's uses must be waited for in order: an issuer starts
+        // the waits of its stage only after the previous stage's waits are done
+        // (the turn counter), although the MMAs of consecutive stages overlap.
+        if (lane == 0 && issuer < I) {
             const uint32_t idesc = instr_desc_bf16(a.bn);
             bool ok = true;
-            if (a.force_timeout)
+            if (a.force_timeout && issuer == 0)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
                                   (unsigned long long)a.force_timeout * 1000000ull);
-            int stage = 0, j = 0;
-            for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x, ++j) {
+            // descriptor of slot 0's first x block; slot, block and K step add
+            // to its start-address field (16-byte units, no carry out of it)
+            const uint64_t desc0 = smem_desc_sw128(smem_u32(smem));
+            const uint32_t slot16 = a.x_slot_bytes >> 4;
+            const uint32_t xblock16 = xblock_bytes >> 4;
+            volatile int* turn = &tail->turn;
+            Ring q, qa;
+            int buf = 0, use = 0;
+            int gcs = 0, own = 0;  // copy stages walked, and that count modulo I
+            for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
                 const Item t = decode_item(a, it);
-                const int acc = j & 1;
-                if (j >= 2 && !wait_bounded(smem_u32(&tail->tmem_empty[acc]), ((j >> 1) - 1) & 1,
-                                            abort, a.status, kTimeoutNs)) {
+                if (use >= 1 && !wait_bounded(smem_u32(&tail->tmem_empty[buf]), (use - 1) & 1,
+                                              abort, a.status, kTimeoutNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tmem_d = tmem_base + acc * a.acc_cols;
-                for (int i = 0; i < t.nkb; ++i, ++stage) {
-                    const int s = stage % R;
-                    const int sa = stage % kASlots;
-                    if (!wait_fast(smem_u32(&tail->raw_full[s]), (stage / R) & 1, abort, a.status,
-                                   kTimeoutNs) ||
-                        !wait_fast(smem_u32(&tail->a_full[sa]), (stage / kASlots) & 1, abort,
-                                   a.status, kTimeoutNs)) {
+                const uint32_t tmem_d = tmem_base + (uint32_t)((buf * I + issuer) * a.bn);
+                bool first = true;
+                for (int c = 0; ok && c < t.ncs; ++c, ++gcs, q.next(RX)) {
+                    const int nblk = a.nsub;
+                    const bool mine = own == issuer;
+                    if (++own == I) own = 0;
+                    if (!mine) {
+                        for (int j = 0; j < nblk; ++j) qa.next(SA);
+                        continue;
+                    }
+                    if (I > 1) {
+                        const unsigned long long t0 = globaltimer();
+                        while (*turn != gcs) {
+                            if (*abort) {
+                                ok = false;
+                                break;
+                            }
+                            if (globaltimer() - t0 > kTimeoutNs) {
+                                *abort = 1;
+                                atomicExch(a.status, kStatusTimeout);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                    }
+                    if (!wait_fast(smem_u32(&tail->x_full[q.s]), q.ph, abort, a.status)) {
                         ok = false;
                         break;
                     }
+                    // all of the stage's weight tiles, then the next stage's issuer may
+                    // start its waits while this one issues MMAs (one thread issues
+                    // them slowly; several issuers overlap)
+                    {
+                        Ring qb = qa;
+                        for (int j = 0; ok && j < nblk; ++j, qb.next(SA))
+                            ok = wait_fast(smem_u32(&tail->a_full[qb.s]), qb.ph, abort, a.status);
+                        if (!ok) break;
+                    }
+                    if (I > 1) *turn = gcs + 1;
                     tc_fence_after();
-                    const uint32_t abase = smem_u32(a_tile(sa));
-                    const uint32_t xbase = smem_u32(x_tile(s));
+                    const uint64_t sdesc = desc0 + (uint64_t)((uint32_t)q.s * slot16);
+                    for (int j = 0; j < nblk; ++j, qa.next(SA)) {
+                        const uint32_t tmem_a = tmem_base + a_col0 + (uint32_t)(qa.s * kACols);
+                        const uint64_t bdesc = sdesc + (uint64_t)((uint32_t)j * xblock16);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
-                                    smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
-                    mma_commit(smem_u32(&tail->a_empty[sa]));
-                    mma_commit(smem_u32(&tail->raw_empty[s]));
+                        for (int kk = 0; kk < kBlockK / 16; ++kk)
+                            mma_bf16_ts(tmem_d, tmem_a + 8 * kk, bdesc + (uint64_t)(2 * kk),
+                                        idesc, (first && kk == 0) ? 0u : 1u);
+                        first = false;
+                        mma_commit(smem_u32(&tail->a_free[qa.s]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&tail->x_free[q.s]));
                 }
-                mma_commit(smem_u32(&tail->tmem_full[acc]));  // fires once this item's MMAs are done
+                if (!ok) break;
+                mma_commit(smem_u32(&tail->tmem_full[buf]));  // fires once these MMAs are done
+                if (++buf == a.bufs) {
+                    buf = 0;
+                    ++use;
+                }
             }
             if (!ok) {
-                // let the epilogue drain: both accumulators "complete" once
+                // let the epilogue drain: the accumulator sets "complete" once
                 // every issued MMA has finished
                 mma_commit(smem_u32(&tail->tmem_full[0]));
                 mma_commit(smem_u32(&tail->tmem_full[1]));
             }
+            // every MMA of this thread has finished before TMEM is released, also
+            // after an abort (issued MMAs wait on nothing, so this wait is short)
+            mma_commit(smem_u32(&tail->mma_done[issuer]));
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&tail->mma_done[issuer]), 0) &&
+                   globaltimer() - t0 < kTimeoutNs) {
+            }
         }
-    } else if (warp < kEpilogueWarp0) {
-        // ---------------- dequant producers (warps 2..17): two groups of 8 warps
-        // take alternate stages, so two weight tiles are decoded at a time
+    } else if (warp >= kDequantWarp0) {
+        // ---------------- dequant: group grp takes blocks grp, grp+4, ...; each
+        // thread owns one weight column of the tile = one TMEM lane.  Waits on
+        // a code slot stay in order: with nsub = 4 every group reads every
+        // stage, with nsub = 2 a pair of groups reads every other stage and
+        // the code ring depth is even.
         const int dw = warp - kDequantWarp0;
-        const int grp = dw / kDequantWarps;                  // stage parity handled
-        const int t256 = (dw % kDequantWarps) * 32 + lane;   // 0..255 within the group
-        const int r = t256 & (kTileN - 1);                   // weight column within the tile
-        const int h = t256 >> 7;                             // which 32-row chunk of the block
-        int stage = 0;
+        const int grp = dw >> 2;
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + a_col0;
+        int gb = 0, g4 = 0;  // blocks walked, and that count modulo the group count
+        Ring q, qa;
         bool ok = true;
         for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
             const Item t = decode_item(a, it);
-            const int n = min(t.n0 + r, a.N - 1);
-            for (int i = 0; i < t.nkb; ++i, ++stage) {
-                if ((stage & 1) != grp) continue;
-                const int s = stage % R;
-                const int sa = stage % kASlots;
-                const int g = (t.kb_begin + i) >> 1;  // two 64-row blocks per group of 128
-                const uint32_t s2 = scale_pair(__ldg(a.scales + (size_t)g * a.N + n));
-                const uint32_t z2 = kHasZeros ? zero_pair(load_zero(a.zeros, a.N, g, n))
-                                              : kSymmetricZeroPair;
-                bool landed = wait_fast(smem_u32(&tail->raw_full[s]), (stage / R) & 1, abort,
-                                        a.status, kTimeoutNs);
-                if (landed && stage >= kASlots)
-                    landed = wait_fast(smem_u32(&tail->a_empty[sa]), ((stage / kASlots) - 1) & 1,
-                                       abort, a.status, kTimeoutNs);
-                if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
-                    ok = false;
-                    break;
-                }
-                const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * t.nvalid + min(r, t.nvalid - 1)];
-                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-                uint8_t* row = a_tile(sa) + r * 128;
+            const int rr = min(r, t.nvalid - 1);  // lanes past a ragged edge repeat a column
+            for (int c = 0; ok && c < t.ncs; ++c, q.next(RC)) {
+                const int nblk = a.nsub;
+                for (int j = 0; j < nblk; ++j, ++gb, qa.next(SA)) {
+                    const bool mine = g4 == grp;
+                    if (++g4 == kDequantGroups) g4 = 0;
+                    if (!mine) continue;
+                    bool landed = wait_fast(smem_u32(&tail->code_full[q.s]), q.ph, abort, a.status);
+                    // the weight-tile slot is free once the block SA back finished
+                    if (landed && gb >= SA)
+                        landed = wait_fast(smem_u32(&tail->a_free[qa.s]), qa.ph ^ 1u, abort,
+                                           a.status);
+                    if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* slot = code_slot(q.s);
+                    const uint4* codes = reinterpret_cast<const uint4*>(slot) +
+                                         (size_t)(2 * j) * t.nvalid;
+                    const uint4 q0 = codes[rr];
+                    const uint4 q1 = codes[t.nvalid + rr];
+                    const int kb0 = t.kb_begin + c * a.nsub;
+                    const int grow = ((kb0 + j) >> 1) - (kb0 >> 1);  // group row inside the stage
+                    const uint32_t s2 = scale_pair(reinterpret_cast<const uint16_t*>(
+                        slot + a.scale_off + grow * kScaleRowBytes)[rr]);
+                    uint32_t z2 = kSymmetricZeroPair;
+                    if (kHasZeros) {
+                        const uint32_t zw = reinterpret_cast<const uint32_t*>(
+                            slot + a.zero_off + grow * kZeroRowBytes)[rr >> 3];
+                        z2 = zero_pair((zw >> (4 * (rr & 7))) & 0xFu);
+                    }
+                    // chunk h (rows 32h .. 32h+31 of the block) -> TMEM columns 16h .. 16h+15
+                    const uint32_t col = lane_addr + (uint32_t)(qa.s * kACols);
+                    {
+                        const uint32_t words[4] = {q0.x, q0.y, q0.z, q0.w};
+                        uint32_t v[16];
 #pragma unroll
-                for (int jw = 0; jw < 4; ++jw) {
-                    uint32_t p[4];
-                    dequant_word(words[jw], z2, s2, p);
-                    const int chunk = (4 * h + jw) ^ (r & 7);  // 128-byte swizzle
-                    *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(p[0], p[1], p[2], p[3]);
+                        for (int jw = 0; jw < 4; ++jw)
+#pragma unroll
+                            for (int pp = 0; pp < 4; ++pp)
+                                v[4 * jw + pp] = dequant_pair(words[jw], pp, z2, s2);
+                        tmem_st_16(col, v);
+                    }
+                    {
+                        const uint32_t words[4] = {q1.x, q1.y, q1.z, q1.w};
+                        uint32_t v[16];
+#pragma unroll
+                        for (int jw = 0; jw < 4; ++jw)
+#pragma unroll
+                            for (int pp = 0; pp < 4; ++pp)
+                                v[4 * jw + pp] = dequant_pair(words[jw], pp, z2, s2);
+                        tmem_st_16(col + 16, v);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&tail->a_full[qa.s]));
+                        mbar_arrive(smem_u32(&tail->code_free[q.s]));  // codes read
+                    }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&tail->a_full[sa]));
             }
         }
-    } else {
-        // ---------------- epilogue (warps 10..13; TMEM lane quadrant = warp % 4)
+    } else if (warp >= kEpilogueWarp0) {
+        // ---------------- epilogue (TMEM lane quadrant = warp % 4)
         const int quad = warp & 3;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
         int j = 0;
+        int g0 = 0;  // first copy stage of the item (counted over the CTA's items) modulo I
         for (int it = blockIdx.x; it < a.items; it += gridDim.x, ++j) {
             const Item t = decode_item(a, it);
-            const int acc = j & 1;
-            const bool done = wait_bounded(smem_u32(&tail->tmem_full[acc]), (j >> 1) & 1, abort,
+            const int buf = a.bufs == 2 ? (j & 1) : 0;
+            const int use = a.bufs == 2 ? (j >> 1) : j;
+            const bool done = wait_bounded(smem_u32(&tail->tmem_full[buf]), use & 1, abort,
                                            a.status, kTimeoutNs);
             tc_fence_after();
             const bool live = __all_sync(0xffffffffu, done && !*abort);
             if (live) {  // tcgen05.ld is warp-collective
                 const int nn = t.n0 + quad * 32 + lane;
-                const uint32_t taddr = tmem_base + acc * a.acc_cols + ((uint32_t)(quad * 32) << 16);
+                // issuer i received stages of this item iff (i - g0) mod I < ncs;
+                // the item's first stage went to issuer g0
+                const uint32_t acc0 = lane_base + (uint32_t)(buf * I * a.bn);
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
-                    tmem_ld_16(taddr + c0, v);
+                    uint32_t r[16];
+                    tmem_ld_16(acc0 + (uint32_t)(g0 * a.bn) + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(r[jj]);
+                    for (int k = 1; k < min(I, t.ncs); ++k) {
+                        const int i = g0 + k < I ? g0 + k : g0 + k - I;
+                        tmem_ld_16(acc0 + (uint32_t)(i * a.bn) + c0, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) v[jj] += __uint_as_float(r[jj]);
+                    }
                     if (nn < a.N) {
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
@@ -504,53 +727,53 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tail->tmem_empty[acc]));
+            if (lane == 0) mbar_arrive(smem_u32(&tail->tmem_empty[buf]));
             if (!live) break;
+            g0 = (g0 + t.ncs) % I;
             if (a.split > 1) {
                 // the last CTA of this tile to arrive converts the fp32 sum to
                 // bf16 and clears the accumulator for the next call
                 __threadfence();
                 epilogue_bar();
                 uint32_t* counter = a.counters + (size_t)t.batch_tile * a.col_tiles + t.col_tile;
-                __shared__ int s_last;
                 if (warp == kEpilogueWarp0 && lane == 0) {
                     uint32_t prev;
                     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
                                  : "=r"(prev)
                                  : "l"(counter)
                                  : "memory");
-                    s_last = (prev == (uint32_t)(a.split - 1));
+                    tail->s_last = (prev == (uint32_t)(a.split - 1));
                 }
                 epilogue_bar();
-                if (s_last) {
+                if (tail->s_last) {
                     __threadfence();
-                    // 4 columns per thread and 8 loads in flight: the sums come
+                    // 4 columns per thread and 4 loads in flight: the sums come
                     // back from L2, so latency, not bandwidth, sets the pace
                     const int rows = min(a.bn, a.B - t.b0);
                     const int c4n = t.nvalid / 4;
                     const int total = rows * c4n;
                     const int et = threadIdx.x - 32 * kEpilogueWarp0;
-                    for (int e0 = et; e0 < total; e0 += 128 * 8) {
-                        float4 v[8];
+                    for (int e0 = et; e0 < total; e0 += 128 * 4) {
+                        float4 v[4];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int e = e0 + 128 * j;
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int e = e0 + 128 * jj;
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
-                                v[j] = __ldcg(reinterpret_cast<const float4*>(
+                                v[jj] = __ldcg(reinterpret_cast<const float4*>(
                                     a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
                             }
                         }
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int e = e0 + 128 * j;
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int e = e0 + 128 * jj;
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
                                 const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
-                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[j].x) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[j].y) << 16);
-                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[j].z) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[j].w) << 16);
+                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[jj].x) |
+                                                    ((uint32_t)f32_to_bf16_rn(v[jj].y) << 16);
+                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[jj].z) |
+                                                    ((uint32_t)f32_to_bf16_rn(v[jj].w) << 16);
                                 *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
@@ -564,11 +787,12 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         }
     }
 
+    tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(2 * a.acc_cols)
+                     "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -594,20 +818,43 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-int raw_slots_for(int bn) {
-    const size_t avail = kSmemBudget - 1024 - sizeof(SharedTail) - (size_t)kASlots * kATileBytes;
-    return (int)std::min<size_t>(kMaxRawSlots, avail / raw_slot_bytes(bn));
-}
+// Shared memory: [x ring: x_slots x (nsub x tiles of bn x 128 B)]
+// [code ring: code_slots x (codes nsub x 4 KB, scale rows, zero-point rows)][tail].
+// Both ring depths are even: consecutive uses of a slot fall to the same
+// producer, and (nsub = 2) to the same pair of dequant groups, so every
+// waiter's waits on a slot stay in order.
+struct RingLayout {
+    uint32_t x_slot_bytes, code_slot_bytes, scale_off, zero_off, code_base;
+    int x_slots, code_slots;
+    size_t smem;
+};
 
-size_t smem_bytes(int bn) {
-    return (size_t)kASlots * kATileBytes + (size_t)raw_slots_for(bn) * raw_slot_bytes(bn) +
-           sizeof(SharedTail) + 1024;
-}
-
-uint32_t acc_cols_for(int bn) {
-    uint32_t c = 32;
-    while (c < (uint32_t)bn) c <<= 1;
-    return c;
+RingLayout ring_layout(int bn, int nsub) {
+    RingLayout l;
+    const int ng = nsub > 1 ? nsub / 2 : 1;
+    l.x_slot_bytes = (uint32_t)nsub * (uint32_t)bn * kBlockK * 2;  // multiple of 1024
+    l.scale_off = (uint32_t)nsub * kCodeBlockBytes;
+    l.zero_off = l.scale_off + (uint32_t)ng * kScaleRowBytes;
+    l.code_slot_bytes = (l.zero_off + (uint32_t)ng * kZeroRowBytes + 127u) & ~127u;
+    const size_t avail = kSmemBudget - 1024 - sizeof(SharedTail);
+    // the deepest balanced pair of rings (then the most slots) that fits
+    int best_c = 0, best_x = 0;
+    for (int c = 2; c <= kMaxCodeSlots; c += 2) {
+        if ((size_t)c * l.code_slot_bytes > avail) break;
+        int x = (int)std::min<size_t>(kMaxXSlots, (avail - (size_t)c * l.code_slot_bytes) /
+                                                      l.x_slot_bytes) & ~1;
+        if (x < 2) continue;
+        const int m = std::min(c, x), bm = std::min(best_c, best_x);
+        if (m > bm || (m == bm && c + x > best_c + best_x)) {
+            best_c = c;
+            best_x = x;
+        }
+    }
+    l.code_slots = best_c;
+    l.x_slots = best_x;
+    l.code_base = (uint32_t)best_x * l.x_slot_bytes;
+    l.smem = (size_t)l.code_base + (size_t)best_c * l.code_slot_bytes + sizeof(SharedTail) + 1024;
+    return l;
 }
 
 }  // namespace
@@ -629,20 +876,48 @@ bool tc_available() {
 }
 
 TcPlan plan_tc(int B, int K, int N, int num_sms) {
+    if (B > kMaxTmemBatch) {
+        TcPlan w = plan_tc_wide(B, K, N, num_sms);
+        w.wide = true;
+        return w;
+    }
     TcPlan p{};
     p.batch_tiles = (B + 255) / 256;
     const int per = (B + p.batch_tiles - 1) / p.batch_tiles;
     p.bn = std::min(256, (per + 15) / 16 * 16);
+    // MMAs of one thread run in order and a short MMA (small bn) costs about as
+    // long as a long one, so small tiles spread their copy stages over several
+    // issuers; TMEM (512 columns) holds bufs x issuers accumulators of bn
+    // columns plus the ring of weight tiles (32 columns each).
+    if (p.bn <= 32) {
+        p.issuers = 4;
+        p.bufs = 2;
+    } else if (p.bn <= 64) {
+        p.issuers = 4;
+        p.bufs = 1;
+    } else if (p.bn <= 128) {
+        p.issuers = 2;
+        p.bufs = 1;
+    } else {
+        p.issuers = 1;
+        p.bufs = 1;
+    }
+    // a multiple of the dequant group count, so a tile slot's consecutive uses
+    // fall to the same group (its waits on the slot stay in order)
+    p.a_slots = std::min(kMaxASlots, (kTmemCols - p.bufs * p.issuers * p.bn) / kACols) / 4 * 4;
+    // copy stages of 256 K rows (16 KB of codes) while the x blocks are small,
+    // else 128 rows; every stage is whole (nsub divides the K blocks)
     p.col_tiles = (N + kTileN - 1) / kTileN;
     const int nkb = K / kBlockK;
+    p.nsub = (p.bn <= 32 && nkb % 4 == 0) ? 4 : 2;
     const long long tiles = (long long)p.col_tiles * p.batch_tiles;
     // persistent CTAs (one per SM) take items round robin; choose the K split
-    // minimising the busiest CTA's K blocks plus a fixed cost per item and a
-    // small cost per split (accumulator traffic)
+    // (whole copy stages per split) minimising the busiest CTA's K blocks plus
+    // a fixed cost per item and a small cost per split (accumulator traffic)
     double best = 1e300;
-    int best_split = 1, best_kbps = nkb;
+    int best_split = 1, best_kbps = (nkb + p.nsub - 1) / p.nsub * p.nsub;
     for (int split = 1; split <= std::min(16, nkb); ++split) {
-        const int kbps = (nkb + split - 1) / split;
+        const int kbps = ((nkb + split - 1) / split + p.nsub - 1) / p.nsub * p.nsub;
         if (split > 1 && (kbps < 8 || tiles > kMaxCounters)) break;
         const int s = (nkb + kbps - 1) / kbps;
         const long long items = tiles * s;
@@ -664,26 +939,69 @@ size_t tc_workspace_bytes(const TcPlan& p, int B, int N) {
     return p.split > 1 ? kCounterBytes + (size_t)B * N * sizeof(float) : 0;
 }
 
-static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
-                           bool has_zeros, void* y, int B, int K, int N, void* workspace,
-                           unsigned int* status, int force_timeout_ms, cudaStream_t stream) {
+static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed,
+                                  const void* scales, bool has_zeros, void* y, int B, int K,
+                                  int N, void* workspace, unsigned int* status,
+                                  int force_timeout_ms, cudaStream_t stream) {
+    if (p.wide)
+        return launch_tc_wide(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
+                              force_timeout_ms, stream);
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
+    const int ng = p.nsub > 1 ? p.nsub / 2 : 1;
+    const cuuint32_t e1[3] = {1, 1, 1};
+    // x: 3-D view (k within a block, row, block) so one box brings a stage's
+    // nsub blocks, each a 1024-byte-aligned bn x 128-byte swizzled tile; if the
+    // encoder refuses the view, one 2-D box per block
     CUtensorMap xmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)B};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)p.bn};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    int x3d = 1;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kBlockK, (cuuint64_t)B, (cuuint64_t)(K / kBlockK)};
+        const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kBlockK * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)p.bn, (cuuint32_t)p.nsub};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides,
+                box, e1, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            x3d = 0;
+            const cuuint64_t dims2[2] = {(cuuint64_t)K, (cuuint64_t)B};
+            const cuuint64_t strides2[1] = {(cuuint64_t)K * 2};
+            const cuuint32_t box2[2] = {(cuuint32_t)kBlockK, (cuuint32_t)p.bn};
+            if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims2,
+                    strides2, box2, e1, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
+    }
+    // scales bf16 [K/128][N]: box of 128 columns x ng group rows
+    CUtensorMap smap;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)(K / kGroup)};
+        const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)ng};
+        if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(scales), dims,
+                strides, box, e1, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // zero-points: padded uint32 rows after the codes; box of 16 words x ng rows
+    CUtensorMap zmap = smap;
+    if (has_zeros) {
+        const int row_words = packed_zero_row_words(N);
+        const cuuint64_t dims[2] = {(cuuint64_t)row_words, (cuuint64_t)(K / kGroup)};
+        const cuuint64_t strides[1] = {(cuuint64_t)row_words * 4};
+        const cuuint32_t box[2] = {(cuuint32_t)(kTileN / 8), (cuuint32_t)ng};
+        void* zbase = static_cast<char*>(const_cast<void*>(packed)) + packed_code_bytes(K, N);
+        if (enc(&zmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, zbase, dims, strides, box, e1,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
 
+    const RingLayout lay = ring_layout(p.bn, p.nsub);
     Args a;
     a.packed = static_cast<const uint8_t*>(packed);
-    a.scales = static_cast<const uint16_t*>(scales);
-    a.zeros = reinterpret_cast<const uint32_t*>(static_cast<const char*>(packed) +
-                                                packed_code_bytes(K, N));
     a.y = static_cast<uint16_t*>(y);
     a.partial = ws_partials(workspace);
     a.counters = ws_counters(workspace);
@@ -692,23 +1010,34 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     a.K = K;
     a.N = N;
     a.bn = p.bn;
+    a.nsub = p.nsub;
     a.kb_per_split = p.kb_per_split;
     a.split = p.split;
     a.nkb = K / kBlockK;
     a.col_tiles = p.col_tiles;
     a.batch_tiles = p.batch_tiles;
     a.items = p.col_tiles * p.batch_tiles * p.split;
-    a.acc_cols = acc_cols_for(p.bn);
-    a.raw_slots = raw_slots_for(p.bn);
+    a.issuers = p.issuers;
+    a.bufs = p.bufs;
+    a.a_slots = p.a_slots;
+    a.code_slots = lay.code_slots;
+    a.x_slots = lay.x_slots;
+    a.code_slot_bytes = lay.code_slot_bytes;
+    a.x_slot_bytes = lay.x_slot_bytes;
+    a.code_base = lay.code_base;
+    a.scale_off = lay.scale_off;
+    a.zero_off = lay.zero_off;
+    a.x3d = x3d;
     a.force_timeout = force_timeout_ms;
+    if (a.a_slots < 4 || a.code_slots < 2 || a.x_slots < 2) return cudaErrorInvalidConfiguration;
 
-    const size_t smem = smem_bytes(p.bn);
+    const size_t smem = lay.smem;
     const void* kern = has_zeros ? reinterpret_cast<const void*>(tc_kernel<true>)
                                  : reinterpret_cast<const void*>(tc_kernel<false>);
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    void* args[] = {&xmap, &a};
+    void* args[] = {&xmap, &smap, &zmap, &a};
     const int grid = std::min(a.items, p.grid);
     return launch_with_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, args);
 }
