@@ -30,10 +30,10 @@
 // through a ring of weight tiles in TMEM.
 //
 // Persistent CTAs (one per SM) take work items (column tile, batch tile, K
-// split) round robin.  Up to four MMA-issuing threads take the copy stages of
-// an item in turn, each into its own accumulator: MMAs issued by one thread
-// run one after another, so at small bn (short MMAs) several issuers keep the
-// tensor pipe busy; the epilogue adds the accumulators.  Warp roles:
+// split) round robin.  Up to four MMA-issuing threads take the 64-row blocks
+// in turn, each into its own accumulator: MMAs issued by one thread run one
+// after another, so at small bn (short MMAs) several issuers keep the tensor
+// pipe busy; the epilogue adds the accumulators.  Warp roles:
 //   warps 0, 25     : TMA producers (copy stages alternate between them);
 //   warps 1-3, 24   : MMA issuers 0-3 (warp 1 also allocates TMEM);
 //   warps 4-7       : epilogue, TMEM lane quadrant = warp % 4;
@@ -290,7 +290,6 @@ struct SharedTail {
     uint32_t tmem_base;
     int abort;
     int s_last;
-    int turn;                               // next copy stage whose waits may start
 };
 
 struct Item {
@@ -395,7 +394,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
         }
         for (int s = 0; s < RX; ++s) {
             mbar_init(smem_u32(&tail->x_full[s]), 1);
-            mbar_init(smem_u32(&tail->x_free[s]), 1);
+            mbar_init(smem_u32(&tail->x_free[s]), a.nsub);  // one commit per block
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(smem_u32(&tail->a_full[s]), 4);
@@ -408,7 +407,6 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
         for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(&tail->mma_done[i]), 1);
         mbar_init(smem_u32(&tail->never), 1);
         tail->abort = 0;
-        tail->turn = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
@@ -492,26 +490,30 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
             }
         }
     } else if (issuer >= 0) {
-        // ---------------- MMA issuers: issuer i takes copy stages i, i+I, ... (counted
-        // over all items of the CTA).  mbarrier waits test only the parity of a
-        // phase, so a barrier's uses must be waited for in order: an issuer starts
-        // the waits of its stage only after the previous stage's waits are done
-        // (the turn counter), although the MMAs of consecutive stages overlap.
+        // ---------------- MMA issuers: issuer i takes 64-row blocks i, i+I, ... (counted
+        // over all items of the CTA; I divides the 4 dequant groups, so all blocks
+        // of a group go to one issuer).  mbarrier waits test only the parity of a
+        // phase, so every waiter must wait for a barrier's uses in order: each
+        // dequant group has its own sub-ring of weight tiles, read by one issuer,
+        // and every issuer reads every x slot it waits for in order (the x ring
+        // depth times the blocks per stage is a multiple of I).
         if (lane == 0 && issuer < I) {
             const uint32_t idesc = instr_desc_bf16(a.bn);
             bool ok = true;
             if (a.force_timeout && issuer == 0)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
                                   (unsigned long long)a.force_timeout * 1000000ull);
-            // descriptor of slot 0's first x block; slot, block and K step add
+            // descriptor of x slot 0's first block; slot, block and K step add
             // to its start-address field (16-byte units, no carry out of it)
             const uint64_t desc0 = smem_desc_sw128(smem_u32(smem));
             const uint32_t slot16 = a.x_slot_bytes >> 4;
             const uint32_t xblock16 = xblock_bytes >> 4;
-            volatile int* turn = &tail->turn;
-            Ring q, qa;
+            const int SAg = SA >> 2;  // tiles per dequant group
+            // block 4k + g is group g's k-th block: all groups' sub-rings are at the
+            // same position, stepped once every 4 blocks
+            Ring qx, qk;
             int buf = 0, use = 0;
-            int gcs = 0, own = 0;  // copy stages walked, and that count modulo I
+            int gb = 0;  // blocks walked
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
                 const Item t = decode_item(a, it);
                 if (use >= 1 && !wait_bounded(smem_u32(&tail->tmem_empty[buf]), (use - 1) & 1,
@@ -522,58 +524,30 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                 tc_fence_after();
                 const uint32_t tmem_d = tmem_base + (uint32_t)((buf * I + issuer) * a.bn);
                 bool first = true;
-                for (int c = 0; ok && c < t.ncs; ++c, ++gcs, q.next(RX)) {
-                    const int nblk = a.nsub;
-                    const bool mine = own == issuer;
-                    if (++own == I) own = 0;
-                    if (!mine) {
-                        for (int j = 0; j < nblk; ++j) qa.next(SA);
-                        continue;
-                    }
-                    if (I > 1) {
-                        const unsigned long long t0 = globaltimer();
-                        while (*turn != gcs) {
-                            if (*abort) {
-                                ok = false;
-                                break;
-                            }
-                            if (globaltimer() - t0 > kTimeoutNs) {
-                                *abort = 1;
-                                atomicExch(a.status, kStatusTimeout);
-                                ok = false;
-                                break;
-                            }
+                for (int c = 0; ok && c < t.ncs; ++c, qx.next(RX)) {
+                    const uint64_t sdesc = desc0 + (uint64_t)((uint32_t)qx.s * slot16);
+                    for (int j = 0; j < a.nsub; ++j, ++gb) {
+                        const int g = gb & (kDequantGroups - 1);
+                        const int sa = g * SAg + qk.s;
+                        const uint32_t pha = qk.ph;
+                        if (g == kDequantGroups - 1) qk.next(SAg);
+                        if ((gb & (I - 1)) != issuer) continue;
+                        if (!wait_fast(smem_u32(&tail->x_full[qx.s]), qx.ph, abort, a.status) ||
+                            !wait_fast(smem_u32(&tail->a_full[sa]), pha, abort, a.status)) {
+                            ok = false;
+                            break;
                         }
-                        if (!ok) break;
-                    }
-                    if (!wait_fast(smem_u32(&tail->x_full[q.s]), q.ph, abort, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    // all of the stage's weight tiles, then the next stage's issuer may
-                    // start its waits while this one issues MMAs (one thread issues
-                    // them slowly; several issuers overlap)
-                    {
-                        Ring qb = qa;
-                        for (int j = 0; ok && j < nblk; ++j, qb.next(SA))
-                            ok = wait_fast(smem_u32(&tail->a_full[qb.s]), qb.ph, abort, a.status);
-                        if (!ok) break;
-                    }
-                    if (I > 1) *turn = gcs + 1;
-                    tc_fence_after();
-                    const uint64_t sdesc = desc0 + (uint64_t)((uint32_t)q.s * slot16);
-                    for (int j = 0; j < nblk; ++j, qa.next(SA)) {
-                        const uint32_t tmem_a = tmem_base + a_col0 + (uint32_t)(qa.s * kACols);
+                        tc_fence_after();
+                        const uint32_t tmem_a = tmem_base + a_col0 + (uint32_t)(sa * kACols);
                         const uint64_t bdesc = sdesc + (uint64_t)((uint32_t)j * xblock16);
 #pragma unroll
                         for (int kk = 0; kk < kBlockK / 16; ++kk)
                             mma_bf16_ts(tmem_d, tmem_a + 8 * kk, bdesc + (uint64_t)(2 * kk),
                                         idesc, (first && kk == 0) ? 0u : 1u);
                         first = false;
-                        mma_commit(smem_u32(&tail->a_free[qa.s]));
+                        mma_commit(smem_u32(&tail->a_free[sa]));
+                        mma_commit(smem_u32(&tail->x_free[qx.s]));  // one of nsub per stage
                     }
-                    if (!ok) break;
-                    mma_commit(smem_u32(&tail->x_free[q.s]));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&tail->tmem_full[buf]));  // fires once these MMAs are done
@@ -597,32 +571,35 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
             }
         }
     } else if (warp >= kDequantWarp0) {
-        // ---------------- dequant: group grp takes blocks grp, grp+4, ...; each
-        // thread owns one weight column of the tile = one TMEM lane.  Waits on
-        // a code slot stay in order: with nsub = 4 every group reads every
-        // stage, with nsub = 2 a pair of groups reads every other stage and
-        // the code ring depth is even.
+        // ---------------- dequant: group grp takes blocks grp, grp+4, ... into its own
+        // sub-ring of weight tiles; each thread owns one weight column of the
+        // tile = one TMEM lane.  Waits on a code slot stay in order: with
+        // nsub = 4 every group reads every stage, with nsub = 2 a pair of groups
+        // reads every other stage and the code ring depth is even.
         const int dw = warp - kDequantWarp0;
         const int grp = dw >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + a_col0;
-        int gb = 0, g4 = 0;  // blocks walked, and that count modulo the group count
-        Ring q, qa;
+        int g4 = 0;  // blocks walked, modulo the group count
+        const int SAg = SA >> 2;
+        Ring q, qa;  // code ring; this group's sub-ring of weight tiles
+        int own = 0;  // blocks of this group so far
         bool ok = true;
         for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
             const Item t = decode_item(a, it);
             const int rr = min(r, t.nvalid - 1);  // lanes past a ragged edge repeat a column
             for (int c = 0; ok && c < t.ncs; ++c, q.next(RC)) {
                 const int nblk = a.nsub;
-                for (int j = 0; j < nblk; ++j, ++gb, qa.next(SA)) {
+                for (int j = 0; j < nblk; ++j) {
                     const bool mine = g4 == grp;
                     if (++g4 == kDequantGroups) g4 = 0;
                     if (!mine) continue;
+                    const int sa = grp * SAg + qa.s;
                     bool landed = wait_fast(smem_u32(&tail->code_full[q.s]), q.ph, abort, a.status);
-                    // the weight-tile slot is free once the block SA back finished
-                    if (landed && gb >= SA)
-                        landed = wait_fast(smem_u32(&tail->a_free[qa.s]), qa.ph ^ 1u, abort,
+                    // the tile slot is free once this group's block SA/4 back finished
+                    if (landed && own >= SAg)
+                        landed = wait_fast(smem_u32(&tail->a_free[sa]), qa.ph ^ 1u, abort,
                                            a.status);
                     if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
                         ok = false;
@@ -645,7 +622,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                         z2 = zero_pair((zw >> (4 * (rr & 7))) & 0xFu);
                     }
                     // chunk h (rows 32h .. 32h+31 of the block) -> TMEM columns 16h .. 16h+15
-                    const uint32_t col = lane_addr + (uint32_t)(qa.s * kACols);
+                    const uint32_t col = lane_addr + (uint32_t)(sa * kACols);
                     {
                         const uint32_t words[4] = {q0.x, q0.y, q0.z, q0.w};
                         uint32_t v[16];
@@ -670,9 +647,11 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(smem_u32(&tail->a_full[qa.s]));
+                        mbar_arrive(smem_u32(&tail->a_full[sa]));
                         mbar_arrive(smem_u32(&tail->code_free[q.s]));  // codes read
                     }
+                    qa.next(SAg);
+                    ++own;
                 }
             }
         }
@@ -681,7 +660,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
         const int quad = warp & 3;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
         int j = 0;
-        int g0 = 0;  // first copy stage of the item (counted over the CTA's items) modulo I
+        int g0 = 0;  // first block of the item (counted over the CTA's items) modulo I
         for (int it = blockIdx.x; it < a.items; it += gridDim.x, ++j) {
             const Item t = decode_item(a, it);
             const int buf = a.bufs == 2 ? (j & 1) : 0;
@@ -692,8 +671,8 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
             const bool live = __all_sync(0xffffffffu, done && !*abort);
             if (live) {  // tcgen05.ld is warp-collective
                 const int nn = t.n0 + quad * 32 + lane;
-                // issuer i received stages of this item iff (i - g0) mod I < ncs;
-                // the item's first stage went to issuer g0
+                // issuer i received blocks of this item iff (i - g0) mod I < nkb;
+                // the item's first block went to issuer g0
                 const uint32_t acc0 = lane_base + (uint32_t)(buf * I * a.bn);
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
@@ -702,7 +681,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                     tmem_ld_wait();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(r[jj]);
-                    for (int k = 1; k < min(I, t.ncs); ++k) {
+                    for (int k = 1; k < min(I, t.nkb); ++k) {
                         const int i = g0 + k < I ? g0 + k : g0 + k - I;
                         tmem_ld_16(acc0 + (uint32_t)(i * a.bn) + c0, r);
                         tmem_ld_wait();
@@ -729,7 +708,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tail->tmem_empty[buf]));
             if (!live) break;
-            g0 = (g0 + t.ncs) % I;
+            g0 = (g0 + t.nkb) % I;
             if (a.split > 1) {
                 // the last CTA of this tile to arrive converts the fp32 sum to
                 // bf16 and clears the accumulator for the next call
