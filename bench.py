@@ -93,7 +93,7 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"skinny": ["skinny.cu", "dequant.cuh"], "tcgen05": ["tc_gemm.cu", "dequant.cuh"]}
+KERNEL_FILES = {"skinny": ["skinny.cu", "dequant.cuh"], "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "dequant.cuh"]}
 
 
 def traffic_from_profiles(kernel: str, workload_name: str):
