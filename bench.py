@@ -280,7 +280,7 @@ def run_gpu(args, gemms, rank, world, device):
     if args.per_gemm:
         per_gemm_table(gemms, layers, ws, stream, device, load_peaks()[0], path=FORCE)
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, gemms, layers, device, ws, pick)
+    e2e = run_e2e(args, gemms, layers, device, ws, pick, n_copies)
     return ms, clk.summary(), paths, n_copies, e2e
 
 
@@ -327,42 +327,75 @@ def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200, path=-1
               f"{fl / us / 1e6:8.1f} TFLOP/s", file=sys.stderr, flush=True)
 
 
-def run_e2e(args, gemms, layers, device, ws, pick):
+def run_e2e(args, gemms, layers, device, ws, pick, n_copies):
+    """End to end through the public API with host buffers: every step copies
+    all of its inputs from one pinned host buffer to the device, runs the step's
+    GEMMs through ``w4a16_gemm`` and copies all outputs back to one pinned host
+    buffer.  Timed twice: replaying CUDA graphs of that sequence (one per weight
+    rotation, as a serving loop would; the copies happen on every replay), and
+    eagerly (one Python call per GEMM).  Returns both."""
     import torch
 
     import weight_only_int4_gemm_gb300 as w
     from weight_only_int4_gemm_gb300 import inputs
 
-    host_x, host_y, dev_x, dev_y = [], [], [], []
+    x_sizes = [B * K for _, B, K, _, _, _ in gemms]
+    y_sizes = [B * N for _, B, _, N, _, _ in gemms]
+    host_x = torch.empty(sum(x_sizes), dtype=torch.bfloat16).pin_memory()
+    host_y = torch.empty(sum(y_sizes), dtype=torch.bfloat16).pin_memory()
+    off = 0
     for i, (label, B, K, N, zp, outl) in enumerate(gemms):
-        host_x.append(inputs.make_activations(B, K, seed=20_000 + i, outlier_frac=outl).pin_memory())
-        host_y.append(torch.empty((B, N), dtype=torch.bfloat16).pin_memory())
-        dev_x.append(torch.empty((B, K), dtype=torch.bfloat16, device=device))
-        dev_y.append(torch.empty((B, N), dtype=torch.bfloat16, device=device))
-    h2d = sum(t.numel() * 2 for t in host_x)
-    d2h = sum(t.numel() * 2 for t in host_y)
+        host_x[off:off + x_sizes[i]] = inputs.make_activations(
+            B, K, seed=20_000 + i, outlier_frac=outl).reshape(-1)
+        off += x_sizes[i]
+    dev_x = torch.empty_like(host_x, device=device)
+    dev_y = torch.empty_like(host_y, device=device)
+    xs, ys, ox, oy = [], [], 0, 0
+    for i, (label, B, K, N, zp, _) in enumerate(gemms):
+        xs.append(dev_x[ox:ox + x_sizes[i]].view(B, K))
+        ys.append(dev_y[oy:oy + y_sizes[i]].view(B, N))
+        ox += x_sizes[i]
+        oy += y_sizes[i]
+    h2d, d2h = host_x.numel() * 2, host_y.numel() * 2
     steps = max(3, min(args.steps, args.e2e_steps))
     stream = torch.cuda.Stream(device)
 
     def step(k):
+        dev_x.copy_(host_x, non_blocking=True)
         for i, (label, B, K, N, zp, _) in enumerate(gemms):
             packed, sc = layers[(K, N, zp)][pick(k, i, (K, N, zp))]
-            dev_x[i].copy_(host_x[i], non_blocking=True)
-            w.w4a16_gemm(dev_x[i], packed, sc, zp, N, out=dev_y[i], workspace=ws, stream=stream)
-            host_y[i].copy_(dev_y[i], non_blocking=True)
+            w.w4a16_gemm(xs[i], packed, sc, zp, N, out=ys[i], workspace=ws, stream=stream,
+                         path=FORCE)
+        host_y.copy_(dev_y, non_blocking=True)
+
+    def timed(run):
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for k in range(steps):
+                run(k)
+            stop.record(stream)
+        stop.synchronize()
+        return start.elapsed_time(stop)
 
     with torch.cuda.stream(stream):
         for k in range(3):
             step(k)
     stream.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eager_ms = timed(step)
+    graphs = []
+    for g in range(n_copies):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step(g)
+        graphs.append(graph)
+    stream.synchronize()
     with torch.cuda.stream(stream):
-        start.record(stream)
-        for k in range(steps):
-            step(k)
-        stop.record(stream)
-    stop.synchronize()
-    return start.elapsed_time(stop), steps, h2d, d2h
+        for k in range(3):
+            graphs[k % n_copies].replay()
+    stream.synchronize()
+    graph_ms = timed(lambda k: graphs[k % n_copies].replay())
+    return graph_ms, eager_ms, steps, h2d, d2h
 
 
 # --------------------------------------------------------------- oracle arm
@@ -516,8 +549,10 @@ def main():
         build()
 
     import weight_only_int4_gemm_gb300 as w
-    ms, clocks, paths, n_copies, (e2e_ms, e2e_steps, h2d, d2h) = run_gpu(args, gemms, rank, world, device)
+    ms, clocks, paths, n_copies, (e2e_ms, eager_ms, e2e_steps, h2d, d2h) = \
+        run_gpu(args, gemms, rank, world, device)
     ms, e2e_step_ms = reduce_times_over_ranks(ms, e2e_ms / e2e_steps, world, device)
+    _, eager_step_ms = reduce_times_over_ranks(ms, eager_ms / e2e_steps, world, device)
 
     t_step = ms / 1e3 / args.steps
     value = aggregate_value(sbytes, world, t_step)
@@ -563,7 +598,12 @@ def main():
             "roofline": roof, "clocks": clocks, "gpu_launches": args.steps * len(gemms),
             "e2e": {"value": sbytes * world / (e2e_step_ms / 1e3) / 1e12, "unit": "TB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps, "ms_per_step": e2e_step_ms}}
+                    "steps": e2e_steps, "ms_per_step": e2e_step_ms,
+                    "launch": "CUDA graph per weight rotation of: one H2D copy of the step's "
+                              "inputs, the step's w4a16_gemm calls, one D2H copy of its outputs",
+                    "eager": {"value": sbytes * world / (eager_step_ms / 1e3) / 1e12,
+                              "ms_per_step": eager_step_ms,
+                              "launch": "one Python w4a16_gemm call per GEMM, same copies"}}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
