@@ -148,12 +148,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// 16-byte asynchronous copy that reads src_bytes (0 or 16) and zero-fills the rest.
-__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -305,20 +299,19 @@ skinny_kernel(const Args a) {
                     }
                     w_issued = step + 1;
                 }
-                // activations (valid rows only), scales, zero-points
+                // activations (valid rows only: the padding rows of an mma tile
+                // keep whatever the slot held -- each batch row's outputs depend
+                // only on its own row of x, and padding rows are never written),
+                // scales, zero-points
                 const int g0 = w.g_begin + st * kSlotGroups;
                 const int ngs = min(kSlotGroups, w.g_begin + w.ng - g0);
                 const uint32_t xbase = smem_u32(slot_x(s));
                 const int p = lane & 15;
-                const int rows8 = (w.rows + 7) & ~7;  // rows read by the mma tiles in use
                 for (int gl = 0; gl < ngs; ++gl)
-                    for (int r = lane >> 4; r < rows8; r += 2) {
-                        const bool valid = r < w.rows;  // padding rows are zero-filled
-                        cp_async_16z(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
-                                     a.x + (size_t)(w.b0 + (valid ? r : 0)) * a.K +
-                                         (size_t)kGroup * (g0 + gl) + 8 * p,
-                                     valid ? 16u : 0u);
-                    }
+                    for (int r = lane >> 4; r < w.rows; r += 2)
+                        cp_async_16(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
+                                    a.x + (size_t)(w.b0 + r) * a.K + (size_t)kGroup * (g0 + gl) +
+                                        8 * p);
                 const int gl = lane >> 4;
                 if (gl < ngs && p < w.width / 8) {
                     cp_async_16(smem_u32(slot_scales(s)) + 2u * (gl * kTileCols + 8 * p),
