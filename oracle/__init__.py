@@ -72,6 +72,8 @@ def _load():
         lib.oracle_gemm_cols.argtypes = [u16p, u32p, u16p, u32p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
         lib.oracle_gemm_cols.restype = None
+        lib.oracle_quantize_rtn_mse.argtypes = [u16p, ctypes.c_int, ctypes.c_int, u32p, u16p]
+        lib.oracle_quantize_rtn_mse.restype = None
         lib.oracle_format_bits_per_weight.argtypes = [ctypes.c_longlong, ctypes.c_longlong,
                                                       ctypes.c_int]
         lib.oracle_format_bits_per_weight.restype = ctypes.c_double
@@ -163,6 +165,18 @@ def gemm(x, qweight, scales, qzeros=None, cols=None):
                              _ptr(y, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
                              _ptr(bound, ctypes.c_double))
     return y, acc, bound
+
+
+def quantize_rtn_mse(w) -> tuple[np.ndarray, np.ndarray]:
+    """MSE-optimal clipping quantizer (round to nearest): bf16 bits w [K][N] ->
+    (canonical qweight uint32 [K/8][N], scales bf16 bits uint16 [K/128][N])."""
+    w = _as_u16(w)
+    K, N = w.shape
+    qw = np.zeros((K // 8, N), dtype=np.uint32)
+    sc = np.zeros((K // 128, N), dtype=np.uint16)
+    _load().oracle_quantize_rtn_mse(_ptr(w, ctypes.c_uint16), K, N, _ptr(qw, ctypes.c_uint32),
+                                    _ptr(sc, ctypes.c_uint16))
+    return qw, sc
 
 
 def format_bits_per_weight(K: int, N: int, has_zeros: bool) -> float:

@@ -197,3 +197,95 @@ double oracle_format_bits_per_weight(long long K, long long N, int has_zeros)
     double zero_bytes = has_zeros ? (double)(groups * N) / 2.0 : 0.0;
     return (code_bytes + scale_bytes + zero_bytes) * 8.0 / (double)(K * N);
 }
+
+/* ------------------------------------------------------------------------
+ * Offline quantizer: round to nearest with MSE-optimal clipping.
+ *
+ * "Give Me BF16 or Give Me Death" (summary page), section "W4A16-INT
+ * Quantization", paragraph "Weight quantization algorithm: GPTQ with
+ * MSE-optimal clipping": for each group of 128 consecutive weights (along K,
+ * per output column), search a clipping ratio alpha on a grid; the scale is
+ * alpha * max|x| / 7, a weight is rounded to the nearest multiple of the scale
+ * and saturated to [-7, 7] (symmetric signed INT4, -8 unused), and the alpha
+ * with the smallest sum of squared errors sum (x - Q_alpha(x))^2 is kept.  The
+ * GPTQ Hessian update needs calibration data and is not part of this path.
+ *
+ * Readings (the pages leave these open; listed in the design notes):
+ *  - grid alpha_i = 1 - i/32, i = 0 .. 23 (1 down to 0.28125), every
+ *    alpha * max exact in binary32;
+ *  - the scale is stored as bf16, so it is rounded (RNE) before the codes are
+ *    chosen, and the error is measured on the weights the GEMM will see,
+ *    RNE_bf16(code * scale);
+ *  - code = clamp(round_half_even(x / s), -7, 7), stored with bias 8;
+ *  - the divisions and the rounding to an integer are binary32 operations, as
+ *    in the kernel (a quantised code is a decision both sides must take in the
+ *    same precision); x - Q(x) is exact in binary32 (both are bf16 values at
+ *    most a few binades apart, or Q(x) = 0) and its square exact in binary64;
+ *    the error is summed in binary64 in k order;
+ *  - ties between grid points keep the earlier (larger) alpha; a group of
+ *    zeros gets scale 0 and codes 8.
+ * Inputs: w bf16 [K][N] (row k, column n).  Outputs: canonical qweight uint32
+ * [K/8][N] and scales bf16 [K/128][N].
+ */
+#define ORACLE_QGRID 24
+
+static float oracle_bf16_to_float(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+void oracle_quantize_rtn_mse(const uint16_t *w, int K, int N, uint32_t *qweight,
+                             uint16_t *scales)
+{
+    memset(qweight, 0, (size_t)(K / 8) * (size_t)N * sizeof(uint32_t));
+    for (int g = 0; g < K / ORACLE_GROUP; ++g) {
+        for (int n = 0; n < N; ++n) {
+            float m = 0.0f;
+            for (int r = 0; r < ORACLE_GROUP; ++r) {
+                float v = fabsf(oracle_bf16_to_float(w[(size_t)(g * ORACLE_GROUP + r) * N + n]));
+                if (v > m) m = v;
+            }
+            int best = -1;
+            double best_err = 0.0;
+            uint16_t best_s = 0;
+            for (int i = 0; i < ORACLE_QGRID; ++i) {
+                float alpha = 1.0f - (float)i / 32.0f;
+                float sf = (alpha * m) / 7.0f;
+                uint16_t sb = oracle_bf16_from_double((double)sf);
+                float s = oracle_bf16_to_float(sb);
+                if (!(s > 0.0f)) continue;
+                double err = 0.0;
+                for (int r = 0; r < ORACLE_GROUP; ++r) {
+                    float x = oracle_bf16_to_float(w[(size_t)(g * ORACLE_GROUP + r) * N + n]);
+                    float q = rintf(x / s);
+                    if (q > 7.0f) q = 7.0f;
+                    if (q < -7.0f) q = -7.0f;
+                    float xq = oracle_bf16_to_float(oracle_dequant_one((int)q + 8, 8, sb));
+                    float e = x - xq;
+                    err += (double)e * (double)e;
+                }
+                if (best < 0 || err < best_err) {
+                    best = i;
+                    best_err = err;
+                    best_s = sb;
+                }
+            }
+            scales[(size_t)g * N + n] = best < 0 ? 0 : best_s;
+            for (int r = 0; r < ORACLE_GROUP; ++r) {
+                int code = 8;
+                if (best >= 0) {
+                    float x = oracle_bf16_to_float(w[(size_t)(g * ORACLE_GROUP + r) * N + n]);
+                    float q = rintf(x / oracle_bf16_to_float(best_s));
+                    if (q > 7.0f) q = 7.0f;
+                    if (q < -7.0f) q = -7.0f;
+                    code = (int)q + 8;
+                }
+                int k = g * ORACLE_GROUP + r;
+                qweight[(size_t)(k / 8) * N + n] |= (uint32_t)code << (4 * (k % 8));
+            }
+        }
+    }
+}
