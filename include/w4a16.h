@@ -135,6 +135,26 @@ w4a16_status w4a16_gemm_path(const void *x, const void *packed, const void *scal
 w4a16_status w4a16_dequant_ref(const void *packed, const void *scales, int has_zeros, void *w,
                                int K, int N, int group_size, void *stream);
 
+/* Offline quantizer for the symmetric format: bf16 weights -> canonical
+ * codes and bf16 group scales, ready for w4a16_pack.  "Give Me BF16 or Give
+ * Me Death", section "W4A16-INT Quantization", paragraph "Weight quantization
+ * algorithm: GPTQ with MSE-optimal clipping", without the GPTQ update (which
+ * needs calibration data): for each group of 128 consecutive weights along K
+ * of each column, the clipping ratio alpha on the grid 1 - i/32 (i = 0..23)
+ * whose round-to-nearest quantisation has the smallest sum of squared errors;
+ * scale = RNE_bf16(alpha * max|x| / 7), code = clamp(rint(x / scale), -7, 7)
+ * + 8 (codes 1..15; 8 with scale 0 for an all-zero group).  The error is
+ * measured on RNE_bf16((code - 8) * scale), the weights the GEMM uses.  The
+ * result is deterministic (binary32 division and rounding, binary64 error
+ * sums in k order; ties keep the larger alpha).
+ *   w        device bf16 [K][N], row-major (read)
+ *   qweight  device uint32 [K/8][N], canonical layout (written)
+ *   scales   device bf16 [K/128][N] (written)
+ * Errors: UNSUPPORTED (group_size != 128), SHAPE (K % 128, N % 8), NULL,
+ * ALIGN (16 bytes), CUDA (launch).  Asynchronous on stream. */
+w4a16_status w4a16_quantize_rtn(const void *w, int K, int N, int group_size, uint32_t *qweight,
+                                void *scales, void *stream);
+
 /* Path w4a16_gemm would take for this shape on the current device
  * (W4A16_PATH_*), or -1 for invalid shapes. */
 int w4a16_select_path(int B, int K, int N);

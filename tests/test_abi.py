@@ -97,6 +97,14 @@ def test_pack_and_dequant_validation(lib):
     assert lib.w4a16_dequant_ref(FAKE + 1, FAKE, 0, FAKE, 128, 8, 128, None) == ERR_ALIGN
 
 
+def test_quantize_validation(lib):
+    assert lib.w4a16_quantize_rtn(FAKE, 128, 8, 64, FAKE, FAKE, None) == ERR_UNSUP
+    assert lib.w4a16_quantize_rtn(FAKE, 100, 8, 128, FAKE, FAKE, None) == ERR_SHAPE
+    assert lib.w4a16_quantize_rtn(FAKE, 128, 12, 128, FAKE, FAKE, None) == ERR_SHAPE
+    assert lib.w4a16_quantize_rtn(None, 128, 8, 128, FAKE, FAKE, None) == ERR_NULL
+    assert lib.w4a16_quantize_rtn(FAKE, 128, 8, 128, FAKE + 4, FAKE, None) == ERR_ALIGN
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert lib.w4a16_status_string(s)

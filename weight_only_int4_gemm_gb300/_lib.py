@@ -38,6 +38,7 @@ SIGNATURES = {
     "w4a16_select_path": (_I, [_I, _I, _I]),
     "w4a16_debug_forced_timeout": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_device_status": (_I, [_I]),
+    "w4a16_quantize_rtn": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -188,6 +189,18 @@ def w4a16_dequant_ref(packed: torch.Tensor, scales: torch.Tensor, has_zeros: boo
         packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0, out.data_ptr(), K, N,
         GROUP, _stream(stream)))
     return out
+
+
+def w4a16_quantize_rtn(w: torch.Tensor, *, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Offline quantizer (round to nearest, MSE-optimal clipping): bf16 W [K][N]
+    -> (canonical qweight int32 [K/8][N], scales bf16 [K/128][N])."""
+    K, N = w.shape
+    _need(w, torch.bfloat16, (K, N), "w")
+    qweight = torch.empty((K // 8, N), dtype=torch.int32, device=w.device)
+    scales = torch.empty((K // GROUP, N), dtype=torch.bfloat16, device=w.device)
+    _check("w4a16_quantize_rtn", load().w4a16_quantize_rtn(
+        w.data_ptr(), K, N, GROUP, qweight.data_ptr(), scales.data_ptr(), _stream(stream)))
+    return qweight, scales
 
 
 def w4a16_debug_forced_timeout(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,

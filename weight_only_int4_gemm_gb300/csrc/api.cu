@@ -204,6 +204,15 @@ w4a16_status w4a16_dequant_ref(const void* packed, const void* scales, int has_z
                                         static_cast<cudaStream_t>(stream)));
 }
 
+w4a16_status w4a16_quantize_rtn(const void* w, int K, int N, int group_size, uint32_t* qweight,
+                                void* scales, void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (!w || !qweight || !scales) return W4A16_ERR_NULL;
+    if (!aligned16(w) || !aligned16(qweight) || !aligned16(scales)) return W4A16_ERR_ALIGN;
+    return from_cuda(launch_quantize(w, K, N, qweight, scales, static_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status w4a16_debug_forced_timeout(const void* x, const void* packed, const void* scales,
                                         int has_zeros, void* y, int B, int K, int N,
                                         int group_size, void* workspace, size_t ws_bytes,

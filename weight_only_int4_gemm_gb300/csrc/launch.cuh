@@ -40,6 +40,8 @@ cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K
                           void* packed, cudaStream_t stream);
 cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,
                                int K, int N, cudaStream_t stream);
+cudaError_t launch_quantize(const void* w, int K, int N, uint32_t* qweight, void* scales,
+                            cudaStream_t stream);
 
 // ---- small-batch streaming kernel (skinny.cu) ----
 struct SkinnyPlan {
