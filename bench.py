@@ -276,12 +276,25 @@ def run_gpu(args, gemms, rank, world, device):
         dist.barrier()
     ms = start.elapsed_time(stop)
     assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
+    # per-step distribution: events around each of up to 200 further replays
+    n_dist = min(args.steps, 200)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_dist + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for k in range(n_dist):
+            replay(k)
+            evs[k + 1].record(stream)
+    evs[-1].synchronize()
+    per_step = sorted(evs[k].elapsed_time(evs[k + 1]) for k in range(n_dist))
+    step_pct = {"p10_ms": per_step[int(0.1 * (n_dist - 1))],
+                "p50_ms": per_step[int(0.5 * (n_dist - 1))],
+                "p90_ms": per_step[int(0.9 * (n_dist - 1))], "replays": n_dist}
 
     if args.per_gemm:
         per_gemm_table(gemms, layers, ws, stream, device, load_peaks()[0], path=FORCE)
     # end to end through the public API with host buffers
     e2e = run_e2e(args, gemms, layers, device, ws, pick, n_copies)
-    return ms, clk.summary(), paths, n_copies, e2e
+    return ms, clk.summary(), paths, n_copies, e2e, step_pct
 
 
 def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200, path=-1):
@@ -467,6 +480,69 @@ def aggregate_value(bytes_per_step: int, world: int, step_s: float) -> float:
     return bytes_per_step * world / step_s / 1e12
 
 
+# --------------------------------------------------------------- offline quantizer
+
+FP64_NOMINAL_TFLOPS = 1.25  # GB300 dense FP64 (CUDA cores), nominal
+
+
+def run_quantize(args):
+    """Times the offline quantizer (round to nearest, MSE-optimal clipping) on
+    one bf16 weight matrix, and the oracle on a column sample of it.  Its
+    arithmetic is binary64 squared-error sums: 24 grid points x 128 weights x
+    (multiply + add) per group of a column."""
+    import numpy as np
+    import torch
+
+    import weight_only_int4_gemm_gb300 as w
+    K, N = (int(v) for v in (args.shape or "4096x28672").split("x"))
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from __graft_entry__ import build
+    build()
+    g = torch.Generator().manual_seed(0)
+    wt = (torch.randn((K, N), generator=g) * 0.02).to(torch.bfloat16)
+    wd = wt.to(device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            w.w4a16_quantize_rtn(wd, stream=stream)
+    stream.synchronize()
+    steps = max(1, min(args.steps, 50))
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps):
+                w.w4a16_quantize_rtn(wd, stream=stream)
+            stop.record(stream)
+        stop.synchronize()
+    t = start.elapsed_time(stop) / 1e3 / steps
+    in_bytes = K * N * 2
+    flops64 = (K // 128) * N * 24 * 128 * 2
+    line = {"metric": "W4A16 offline quantizer (RTN, MSE-optimal clipping), GB/s of bf16 weights",
+            "value": in_bytes / t / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "dtype": "bf16 in, f32 decisions, f64 error sums", "data": "synthetic N(0, 0.02)",
+            "config": {"workload": "quantize", "shape_KxN": f"{K}x{N}", "group": 128, "grid": 24},
+            "roofline": {"bound": "alu", "achieved": flops64 / t / 1e12,
+                         "peak": FP64_NOMINAL_TFLOPS, "unit": "TFLOP/s (fp64)",
+                         "frac": flops64 / t / 1e12 / FP64_NOMINAL_TFLOPS,
+                         "peak_source": "nominal GB300 FP64"},
+            "clocks": clk.summary(), "gpu_launches": steps}
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cols = min(N, 512)
+        sub = np.ascontiguousarray(wt[:, :cols].view(torch.int16).numpy().view(np.uint16))
+        t0 = time.perf_counter()
+        oracle.quantize_rtn_mse(sub)
+        t_cpu = (time.perf_counter() - t0) * N / cols
+        line["cpu_baseline"] = {"value": in_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{cols} of {N} columns, scaled by N/columns"}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------- main
 
 def main():
@@ -476,7 +552,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_layer",
-                    choices=["decode_layer", "single", "decode_step", "prefill", "zp70b"])
+                    choices=["decode_layer", "single", "decode_step", "prefill", "zp70b",
+                             "quantize"])
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--shape", default=None, help="KxN for --workload single (default 4096x4096)")
     ap.add_argument("--e2e-steps", type=int, default=300)
@@ -495,6 +572,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload == "quantize":
+        run_quantize(args)
+        return
     gemms = workload(args.workload, args.batch, args.shape)
     sbytes, sflops = step_bytes_flops(gemms)
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
@@ -549,7 +629,7 @@ def main():
         build()
 
     import weight_only_int4_gemm_gb300 as w
-    ms, clocks, paths, n_copies, (e2e_ms, eager_ms, e2e_steps, h2d, d2h) = \
+    ms, clocks, paths, n_copies, (e2e_ms, eager_ms, e2e_steps, h2d, d2h), step_pct = \
         run_gpu(args, gemms, rank, world, device)
     ms, e2e_step_ms = reduce_times_over_ranks(ms, e2e_ms / e2e_steps, world, device)
     _, eager_step_ms = reduce_times_over_ranks(ms, eager_ms / e2e_steps, world, device)
@@ -587,7 +667,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
-            "us_per_step": t_step * 1e6, "tflops": sflops * world / t_step / 1e12,
+            "us_per_step": t_step * 1e6, "step_distribution": step_pct,
+            "tflops": sflops * world / t_step / 1e12,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; Llama-3-8B shapes, no trained weights)",
             "config": dict(config, parallelism=f"replicas{world}",
@@ -621,6 +702,15 @@ def main():
         line["cpu_baseline"] = {"value": sbytes / t_cpu / 1e12, "unit": "TB/s",
                                 "cores": oracle.omp_threads(), "kind": "oracle", "sample": sample,
                                 "us_per_step": t_cpu * 1e6}
+        # the same oracle on one core, on a smaller column sample
+        oracle.set_threads(1)
+        sampler.cols = max(1, sampler.cols // 16)
+        t1 = time.perf_counter()
+        t_one = sampler.step()
+        line["cpu_baseline"]["single_core"] = {
+            "value": sbytes / t_one / 1e12, "unit": "TB/s", "us_per_step": t_one * 1e6,
+            "sample": sampler.describe(1, time.perf_counter() - t1)}
+        oracle.set_threads(oracle.omp_threads())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -72,6 +72,8 @@ def _load():
         lib.oracle_gemm_cols.argtypes = [u16p, u32p, u16p, u32p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
         lib.oracle_gemm_cols.restype = None
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = None
         lib.oracle_quantize_rtn_mse.argtypes = [u16p, ctypes.c_int, ctypes.c_int, u32p, u16p]
         lib.oracle_quantize_rtn_mse.restype = None
         lib.oracle_format_bits_per_weight.argtypes = [ctypes.c_longlong, ctypes.c_longlong,
@@ -181,6 +183,11 @@ def quantize_rtn_mse(w) -> tuple[np.ndarray, np.ndarray]:
 
 def format_bits_per_weight(K: int, N: int, has_zeros: bool) -> float:
     return float(_load().oracle_format_bits_per_weight(K, N, 1 if has_zeros else 0))
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's OpenMP loops from now on."""
+    _load().oracle_set_threads(int(n))
 
 
 def omp_threads() -> int:

@@ -47,6 +47,21 @@
 
 #define ORACLE_GROUP 128
 
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads for the OpenMP loops below (the CPU-baseline timing runs the oracle
+ * on all host cores and on one). */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
+
 /* bf16 -> double: the 16 bits are the top half of a binary32, which a double
  * holds exactly. */
 double oracle_bf16_to_double(uint16_t h)
