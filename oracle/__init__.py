@@ -12,10 +12,17 @@ Sources, by page title and section:
   * "When quantization pays -- and when it does not", "Counting c from the
     kernel, not from intuition": uint4 codes with bias 8, exact (q - 8) first,
     then one bf16 multiply by the group scale.
+  * "When quantization pays -- and when it does not", "The three regimes"
+    (mixture-of-experts paragraphs): each routed expert's GEMM sees only
+    its own rows (``gemm_grouped``).
+  * "Give Me BF16 or Give Me Death", "W4A16-INT Quantization": round to
+    nearest with MSE-optimal clipping (``quantize_rtn_mse``).
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+Parity status: every function here is pinned -- ``tests/test_oracle_pins.py``
 (exhaustive nearest-bf16 check, integer special cases, exact-rational brute
-force, invariants, hand-built unpack cases, the 4.125-bit accounting).
+force, invariants, hand-built unpack cases, the 4.125-bit accounting),
+``tests/test_quantizer_pins.py`` (quantizer) and ``tests/test_grouped_pins.py``
+(closed-form expert routing).
 """
 from __future__ import annotations
 
@@ -166,6 +173,35 @@ def gemm(x, qweight, scales, qzeros=None, cols=None):
                              B, K, N, _ptr(c, ctypes.c_int), nc,
                              _ptr(y, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
                              _ptr(bound, ctypes.c_double))
+    return y, acc, bound
+
+
+def gemm_grouped(x, offsets, qweights, scales, qzeros=None, cols=None):
+    """Mixture-of-experts GEMM ("When quantization pays -- and when it does
+    not", section "The three regimes", the mixture-of-experts paragraphs: a
+    routed expert's weights multiply only the rows sent to it).
+
+    Rows offsets[e] .. offsets[e+1]-1 of x [T][K] use expert e's weights
+    (qweights[e], scales[e], qzeros[e]); each expert is one ``gemm`` on its
+    rows.  Returns ``(y, acc, bound)`` over all T rows, like ``gemm``.
+    """
+    xb = _as_u16(x)
+    T = xb.shape[0]
+    off = np.asarray(offsets, dtype=np.int64)
+    E = off.shape[0] - 1
+    assert off[0] == 0 and off[E] == T and np.all(np.diff(off) >= 0)
+    N = _as_u32(qweights[0]).shape[1]
+    nc = N if cols is None else len(cols)
+    y = np.zeros((T, nc), dtype=np.uint16)
+    acc = np.zeros((T, nc), dtype=np.float64)
+    bound = np.zeros((T, nc), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        ye, ae, be = gemm(xb[r0:r1], qweights[e], scales[e],
+                          None if qzeros is None else qzeros[e], cols=cols)
+        y[r0:r1], acc[r0:r1], bound[r0:r1] = ye, ae, be
     return y, acc, bound
 
 

@@ -12,7 +12,12 @@ Recipe (shapes and value distributions of the workloads):
                 words, i.e. uniform zero-points 0..15 (asymmetric variant);
   * x        -- bf16 [B][K]: N(0, 1) rounded to bf16; with ``outlier_frac``,
                 round(outlier_frac * K) input channels picked without
-                replacement are multiplied by 20 before the rounding.
+                replacement are multiplied by 20 before the rounding;
+  * routing  -- mixture-of-experts layers: every token picks k distinct
+                experts of E uniformly at random (the uniform-routing
+                assumption of the pages' effective-M estimate); the routed
+                rows are grouped by expert, giving per-expert row offsets;
+                expert e's weights are drawn like one layer's, seed + e.
 
 Draws use ``torch.Generator(device).manual_seed(seed)``; CPU and CUDA
 generators give different streams, so each comparison uses one generated copy
@@ -77,3 +82,50 @@ def make_problem(B: int, K: int, N: int, seed: int, *, zero_points: bool = False
     qweight, scales, qzeros = make_weights(K, N, seed, zero_points=zero_points, device=device)
     x = make_activations(B, K, seed + 1_000_003, outlier_frac=outlier_frac, device=device)
     return LinearProblem(x, qweight, scales, qzeros)
+
+
+def make_routing(tokens: int, E: int, k: int, seed: int) -> torch.Tensor:
+    """Row offsets int32 [E+1] of ``tokens * k`` routed rows grouped by expert:
+    each token picks k distinct experts uniformly at random."""
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    picks = torch.rand((tokens, E), generator=gen).argsort(dim=1)[:, :k]
+    counts = torch.bincount(picks.reshape(-1), minlength=E)
+    offsets = torch.zeros(E + 1, dtype=torch.int64)
+    offsets[1:] = torch.cumsum(counts, 0)
+    return offsets.to(torch.int32)
+
+
+def offsets_from_counts(counts) -> torch.Tensor:
+    """Row offsets int32 [E+1] for explicit per-expert row counts."""
+    c = torch.as_tensor(counts, dtype=torch.int64)
+    offsets = torch.zeros(c.numel() + 1, dtype=torch.int64)
+    offsets[1:] = torch.cumsum(c, 0)
+    return offsets.to(torch.int32)
+
+
+@dataclass
+class GroupedProblem:
+    x: torch.Tensor          # bf16 [T][K], rows grouped by expert
+    offsets: torch.Tensor    # int32 [E+1]
+    qweight: torch.Tensor    # int32 [E][K/8][N]
+    scales: torch.Tensor     # bf16 [E][K/128][N]
+    qzeros: torch.Tensor | None  # int32 [E][K/128][N/8] or None
+
+    def to(self, device) -> "GroupedProblem":
+        return GroupedProblem(
+            self.x.to(device), self.offsets.to(device), self.qweight.to(device),
+            self.scales.to(device), None if self.qzeros is None else self.qzeros.to(device))
+
+
+def make_grouped_problem(offsets: torch.Tensor, K: int, N: int, seed: int, *,
+                         zero_points: bool = False, device="cpu") -> GroupedProblem:
+    """E experts' weights (expert e from seed + e) and T = offsets[-1] rows of x."""
+    E = offsets.numel() - 1
+    T = int(offsets[-1])
+    ws = [make_weights(K, N, seed + e, zero_points=zero_points, device=device) for e in range(E)]
+    qweight = torch.stack([w[0] for w in ws])
+    scales = torch.stack([w[1] for w in ws])
+    qzeros = torch.stack([w[2] for w in ws]) if zero_points else None
+    x = make_activations(T, K, seed + 1_000_003, device=device)
+    return GroupedProblem(x, offsets.to(device), qweight, scales, qzeros)
