@@ -543,6 +543,168 @@ def run_quantize(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------- mixture of experts
+
+MOE_EXPERTS, MOE_TOPK, MOE_HIDDEN, MOE_WIDTH = 128, 8, 2048, 768
+
+
+def run_moe(args):
+    """One mixture-of-experts layer's routed-expert GEMMs at decode: 128
+    experts, top-8 routing, hidden 2048, expert width 768 -- the gate+up
+    grouped GEMM (K=2048, N=2x768) and the down grouped GEMM (K=768, N=2048)
+    over B tokens x 8 routed rows.  Uniform random routing (seeded); both
+    GEMMs get seeded activations (the activation function between them is not
+    part of this path).  Bytes: codes + scales of every expert that receives
+    rows, plus x and y."""
+    import numpy as np
+    import torch
+
+    import weight_only_int4_gemm_gb300 as w
+    from weight_only_int4_gemm_gb300 import inputs
+    tokens = args.batch or 64
+    E, topk = MOE_EXPERTS, MOE_TOPK
+    T = tokens * topk
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from __graft_entry__ import build
+    build()
+    shapes = [("gate_up", MOE_HIDDEN, 2 * MOE_WIDTH), ("down", MOE_WIDTH, MOE_HIDDEN)]
+    offs = [inputs.make_routing(tokens, E, topk, seed=101 + i) for i in range(len(shapes))]
+    n_copies = 2  # 2 x 311 MB of expert weights: every step streams from HBM
+    weights, xs, ys, bytes_step, max_rows = [], [], [], 0, []
+    for i, (lbl, K, N) in enumerate(shapes):
+        reps = []
+        for c in range(n_copies):
+            packed, scales = [], []
+            for e in range(E):
+                qw, sc, _ = inputs.make_weights(K, N, seed=5000 * i + 97 * c + e, device=device)
+                packed.append(w.w4a16_pack(qw))
+                scales.append(sc)
+            reps.append((torch.stack(packed), torch.stack(scales)))
+        weights.append(reps)
+        xs.append(inputs.make_activations(T, K, seed=40_000 + i, device=device))
+        ys.append(torch.empty((T, N), dtype=torch.bfloat16, device=device))
+        counts = offs[i][1:] - offs[i][:-1]
+        active = int((counts > 0).sum())
+        bytes_step += active * (K * N // 2 + (K // 128) * N * 2) + T * K * 2 + T * N * 2
+        max_rows.append(int(counts.max()))
+    dev_offs = [o.to(device) for o in offs]
+    ws = torch.zeros(max(w.w4a16_grouped_workspace_bytes(T, E, m, K, N)
+                         for m, (_, K, N) in zip(max_rows, shapes)) + 256,
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step(c, x_list=xs, y_list=ys):
+        for i, (lbl, K, N) in enumerate(shapes):
+            packed, scales = weights[i][c]
+            w.w4a16_gemm_grouped(x_list[i], dev_offs[i], packed, scales, False, max_rows[i],
+                                 out=y_list[i], workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for k in range(max(3, args.warmup)):
+            step(k % n_copies)
+    stream.synchronize()
+    graphs = []
+    for c in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            graphs[k % n_copies].replay()
+    stream.synchronize()
+    steps = max(1, min(args.steps, 5000))
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for k in range(steps):
+                graphs[k % n_copies].replay()
+            stop.record(stream)
+        stop.synchronize()
+    assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
+    t = start.elapsed_time(stop) / 1e3 / steps
+    hbm, _, _, peak_src = load_peaks()
+    achieved = bytes_step / t / 1e9
+
+    # end to end: host x and routing tables in, host y out, every step
+    host_in = [x.cpu().pin_memory() for x in xs] + [o.pin_memory() for o in offs]
+    host_out = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
+    dev_in = list(xs) + dev_offs
+
+    def e2e_step(c):
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step(c)
+        for h, d in zip(host_out, ys):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            e2e_step(k % n_copies)
+    stream.synchronize()
+    e2e_graphs = []
+    for c in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_step(c)
+        e2e_graphs.append(g)
+    e_steps = max(3, min(steps, args.e2e_steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for k in range(e_steps):
+            e2e_graphs[k % n_copies].replay()
+        e1.record(stream)
+    e1.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3 / e_steps
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+
+    line = {"metric": "W4A16 mixture-of-experts layer (routed experts) µs/step & TB/s",
+            "value": bytes_step / t / 1e12, "unit": "TB/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3, "us_per_step": t * 1e6,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded weights, uniform random top-8 routing)",
+            "config": {"workload": "moe", "experts": E, "top_k": topk, "tokens": tokens,
+                       "routed_rows": T, "hidden": MOE_HIDDEN, "expert_width": MOE_WIDTH,
+                       "gemms": [f"{lbl} {K}x{N}" for lbl, K, N in shapes],
+                       "max_rows": max_rows, "algorithmic_bytes_per_step": bytes_step,
+                       "l2": f"expert weights rotated over {n_copies} copies (2 x 311 MB)",
+                       "cuda_graph": True},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
+                         "kernel": "skinny (grouped)", "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_step / len(shapes)},
+            "clocks": clk.summary(), "gpu_launches": steps * len(shapes),
+            "e2e": {"value": bytes_step / t_e2e / 1e12, "unit": "TB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": t_e2e * 1e3, "steps": e_steps}}
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        t_cpu = 0.0
+        cols_used = []
+        for i, (lbl, K, N) in enumerate(shapes):
+            cols = 16
+            qws = [inputs.make_weights(K, cols, seed=e)[0].numpy().view(np.uint32)
+                   for e in range(E)]
+            scs = [inputs.make_weights(K, cols, seed=e)[1].view(torch.int16).numpy()
+                   .view(np.uint16) for e in range(E)]
+            xb = xs[i].cpu().view(torch.int16).numpy().view(np.uint16)
+            t0 = time.perf_counter()
+            oracle.gemm_grouped(xb, offs[i].numpy(), qws, scs)
+            t_cpu += (time.perf_counter() - t0) * N / cols
+            cols_used.append(cols)
+        line["cpu_baseline"] = {"value": bytes_step / t_cpu / 1e12, "unit": "TB/s",
+                                "cores": oracle.omp_threads(), "kind": "oracle",
+                                "us_per_step": t_cpu * 1e6,
+                                "sample": f"{cols_used} columns of each expert of the two "
+                                          "grouped GEMMs (all rows, all K), scaled by N/columns"}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------- main
 
 def main():
@@ -553,7 +715,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_layer",
                     choices=["decode_layer", "single", "decode_step", "prefill", "zp70b",
-                             "quantize"])
+                             "quantize", "moe"])
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--shape", default=None, help="KxN for --workload single (default 4096x4096)")
     ap.add_argument("--e2e-steps", type=int, default=300)
@@ -574,6 +736,11 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.workload == "quantize":
         run_quantize(args)
+        return
+    if args.workload == "moe":
+        if args.impl == "reference" or rank != 0:
+            raise SystemExit("--workload moe runs our arm on one GPU only")
+        run_moe(args)
         return
     gemms = workload(args.workload, args.batch, args.shape)
     sbytes, sflops = step_bytes_flops(gemms)

@@ -135,6 +135,35 @@ w4a16_status w4a16_gemm_path(const void *x, const void *packed, const void *scal
 w4a16_status w4a16_dequant_ref(const void *packed, const void *scales, int has_zeros, void *w,
                                int K, int N, int group_size, void *stream);
 
+/* Grouped GEMM for mixture-of-experts layers: one launch computes, for every
+ * expert e, y[r] = x[r] . dequant(W_e) for the rows r of x that belong to e.
+ * Rows are grouped by expert: offsets (device int32 [E+1], non-decreasing,
+ * offsets[0] = 0, offsets[E] = T) gives expert e the rows offsets[e] ..
+ * offsets[e+1]-1 of x [T][K] and y [T][N]; an expert may have no rows.  The
+ * offsets are read on the device, after the previous kernel on the stream has
+ * finished, so the routing may come from that kernel.  A malformed table
+ * cannot reach outside x and y: entries are clamped to [0, T] and a
+ * decreasing entry is raised to the largest one before it (the experts' row
+ * ranges stay disjoint); rows not covered by any expert are left unwritten.
+ * "When quantization pays -- and when it does not", section "The three
+ * regimes", mixture-of-experts paragraphs: a routed expert's GEMM sees only
+ * the rows sent to it, B*k/E of them on average.
+ *   packed     E packed blobs back to back, each w4a16_packed_bytes(K, N,
+ *              128, has_zeros) bytes (from w4a16_pack)
+ *   scales     bf16 [E][K/128][N]
+ *   max_rows   an upper bound on one expert's rows (picks the batch tile:
+ *              <= 8, <= 16, else 32 rows); an expert with more rows is still
+ *              computed correctly, in more tiles
+ *   workspace  w4a16_grouped_workspace_bytes(T, E, max_rows, K, N, 128) bytes,
+ *              same contract as w4a16_gemm's (zero-filled once, left zero)
+ * Errors: UNSUPPORTED (group_size), SHAPE (K, N, T < 1, E outside 1..256,
+ * max_rows < 1), NULL, ALIGN (16 bytes; offsets 4), WORKSPACE, CUDA. */
+size_t w4a16_grouped_workspace_bytes(int T, int E, int max_rows, int K, int N, int group_size);
+w4a16_status w4a16_gemm_grouped(const void *x, const int *offsets, int E, int T,
+                                const void *packed, const void *scales, int has_zeros, void *y,
+                                int max_rows, int K, int N, int group_size, void *workspace,
+                                size_t ws_bytes, void *stream);
+
 /* Offline quantizer for the symmetric format: bf16 weights -> canonical
  * codes and bf16 group scales, ready for w4a16_pack.  "Give Me BF16 or Give
  * Me Death", section "W4A16-INT Quantization", paragraph "Weight quantization

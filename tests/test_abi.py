@@ -105,6 +105,39 @@ def test_quantize_validation(lib):
     assert lib.w4a16_quantize_rtn(FAKE, 128, 8, 128, FAKE + 4, FAKE, None) == ERR_ALIGN
 
 
+def _grouped(lib, x=FAKE, offsets=FAKE, E=8, T=64, y=FAKE, max_rows=16, K=2048, N=1536,
+             group=128, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.w4a16_grouped_workspace_bytes(T, E, max_rows, K, N, 128)
+    return lib.w4a16_gemm_grouped(x, offsets, E, T, FAKE, FAKE, 0, y, max_rows, K, N, group,
+                                  ws, ws_bytes, None)
+
+
+def test_grouped_validation(lib):
+    bad = ctypes.c_size_t(-1).value
+    need = lib.w4a16_grouped_workspace_bytes(64, 8, 16, 2048, 1536, 128)
+    assert 0 < need < bad
+    assert lib.w4a16_grouped_workspace_bytes(64, 0, 16, 2048, 1536, 128) == bad
+    assert lib.w4a16_grouped_workspace_bytes(64, 257, 16, 2048, 1536, 128) == bad
+    assert lib.w4a16_grouped_workspace_bytes(0, 8, 16, 2048, 1536, 128) == bad
+    assert lib.w4a16_grouped_workspace_bytes(64, 8, 16, 2048, 1536, 64) == bad
+    assert _grouped(lib, group=64) == ERR_UNSUP
+    assert _grouped(lib, K=100) == ERR_SHAPE
+    assert _grouped(lib, N=12) == ERR_SHAPE
+    assert _grouped(lib, T=0, ws_bytes=need) == ERR_SHAPE
+    assert _grouped(lib, E=0, ws_bytes=need) == ERR_SHAPE
+    assert _grouped(lib, E=257, ws_bytes=need) == ERR_SHAPE
+    assert _grouped(lib, max_rows=0, ws_bytes=need) == ERR_SHAPE
+    assert _grouped(lib, x=None) == ERR_NULL
+    assert _grouped(lib, offsets=None) == ERR_NULL
+    assert _grouped(lib, y=None) == ERR_NULL
+    assert _grouped(lib, ws=None) == ERR_NULL
+    assert _grouped(lib, x=FAKE + 8) == ERR_ALIGN
+    assert _grouped(lib, offsets=FAKE + 2) == ERR_ALIGN
+    assert _grouped(lib, ws=FAKE + 4) == ERR_ALIGN
+    assert _grouped(lib, ws_bytes=need - 1) == ERR_WS
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert lib.w4a16_status_string(s)

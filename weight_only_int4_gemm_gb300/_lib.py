@@ -39,6 +39,8 @@ SIGNATURES = {
     "w4a16_debug_forced_timeout": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_device_status": (_I, [_I]),
     "w4a16_quantize_rtn": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "w4a16_grouped_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
+    "w4a16_gemm_grouped": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -188,6 +190,39 @@ def w4a16_dequant_ref(packed: torch.Tensor, scales: torch.Tensor, has_zeros: boo
     _check("w4a16_dequant_ref", load().w4a16_dequant_ref(
         packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0, out.data_ptr(), K, N,
         GROUP, _stream(stream)))
+    return out
+
+
+def w4a16_grouped_workspace_bytes(T: int, E: int, max_rows: int, K: int, N: int) -> int:
+    v = int(load().w4a16_grouped_workspace_bytes(T, E, max_rows, K, N, GROUP))
+    if v == ctypes.c_size_t(-1).value:
+        raise ValueError(f"invalid grouped shape T={T} E={E} max_rows={max_rows} K={K} N={N}")
+    return v
+
+
+def w4a16_gemm_grouped(x: torch.Tensor, offsets: torch.Tensor, packed: torch.Tensor,
+                       scales: torch.Tensor, has_zeros: bool, max_rows: int, *,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Mixture-of-experts GEMM: rows offsets[e] .. offsets[e+1]-1 of x use expert
+    e's weights.  packed: uint8 [E][packed_bytes]; scales: bf16 [E][K/128][N];
+    offsets: int32 [E+1] on the device."""
+    T, K = x.shape
+    E, G, N = scales.shape
+    _need(x, torch.bfloat16, (T, K), "x")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(scales, torch.bfloat16, (E, K // GROUP, N), "scales")
+    _need(packed, torch.uint8, (E, w4a16_packed_bytes(K, N, has_zeros)), "packed")
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (T, N), "out")
+    need = w4a16_grouped_workspace_bytes(T, E, max_rows, K, N)
+    if workspace is None:
+        workspace = _default_ws.get(need, x.device)
+    _check("w4a16_gemm_grouped", load().w4a16_gemm_grouped(
+        x.data_ptr(), offsets.data_ptr(), E, T, packed.data_ptr(), scales.data_ptr(),
+        1 if has_zeros else 0, out.data_ptr(), max_rows, K, N, GROUP, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

@@ -72,6 +72,7 @@ int num_sms() {
 // mma.sync kernel needs 32-row batch tiles) the tensor-core kernel is 1.7x
 // faster.
 constexpr int kSkinnyMaxB = 16;
+constexpr int kMaxGroupedExperts = 256;
 
 int choose_path(int B, int K, int N) {
     (void)K;
@@ -202,6 +203,34 @@ w4a16_status w4a16_dequant_ref(const void* packed, const void* scales, int has_z
     if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return W4A16_ERR_ALIGN;
     return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_grouped_workspace_bytes(int T, int E, int max_rows, int K, int N, int group_size) {
+    if (group_size != kGroup || !shape_ok(K, N) || T < 1 || T > kMaxB || E < 1 ||
+        E > kMaxGroupedExperts || max_rows < 1)
+        return (size_t)-1;
+    return skinny_workspace_bytes(plan_skinny_grouped(T, E, max_rows, K, N, num_sms()), T, N);
+}
+
+w4a16_status w4a16_gemm_grouped(const void* x, const int* offsets, int E, int T,
+                                const void* packed, const void* scales, int has_zeros, void* y,
+                                int max_rows, int K, int N, int group_size, void* workspace,
+                                size_t ws_bytes, void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N) || T < 1 || T > kMaxB || E < 1 || E > kMaxGroupedExperts ||
+        max_rows < 1)
+        return W4A16_ERR_SHAPE;
+    if (!x || !offsets || !packed || !scales || !y || !workspace) return W4A16_ERR_NULL;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales) || !aligned16(y) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0)
+        return W4A16_ERR_ALIGN;
+    const SkinnyPlan p = plan_skinny_grouped(T, E, max_rows, K, N, num_sms());
+    if (ws_bytes < skinny_workspace_bytes(p, T, N)) return W4A16_ERR_WORKSPACE;
+    unsigned int* status = device_status_word();
+    if (status == nullptr) return W4A16_ERR_CUDA;
+    return from_cuda(launch_skinny_grouped(p, x, offsets, E, packed, scales, has_zeros != 0, y, T,
+                                           K, N, workspace, status,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_quantize_rtn(const void* w, int K, int N, int group_size, uint32_t* qweight,

@@ -55,6 +55,13 @@ struct SkinnyPlan {
 };
 SkinnyPlan plan_skinny(int B, int K, int N, int num_sms);
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N);
+// grouped (mixture-of-experts) variant: T rows of x sorted by expert, device
+// offsets[E+1]; max_rows bounds one expert's rows (picks the batch tile)
+SkinnyPlan plan_skinny_grouped(int T, int E, int max_rows, int K, int N, int num_sms);
+cudaError_t launch_skinny_grouped(const SkinnyPlan& p, const void* x, const int* offsets, int E,
+                                  const void* packed, const void* scales, bool has_zeros,
+                                  void* y, int T, int K, int N, void* workspace,
+                                  unsigned int* status, cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
                           const void* scales, bool has_zeros, void* y, int B, int K, int N,
                           void* workspace, unsigned int* status, cudaStream_t stream);

@@ -82,7 +82,16 @@ struct Args {
     unsigned int* status;
     int B, K, N;
     int tiles, split, gps, units;
+    // grouped (mixture-of-experts) GEMM: offsets != nullptr.  Rows
+    // offsets[e] .. offsets[e+1]-1 of x and y belong to expert e, whose packed
+    // blob and scales sit w_stride bytes / s_stride scales after expert e-1's;
+    // B is the total row count, units is then counted on the device.
+    const int* offsets;
+    int E;
+    size_t w_stride, s_stride;
 };
+
+constexpr int kMaxExperts = 256;
 
 struct Tail {
     uint64_t full[8];
@@ -93,6 +102,11 @@ struct Tail {
     int slot_step[8];    // step of the unit held by the slot
     int res_unit[2];
     int abort;
+    int total_units;                     // units of this call
+    // grouped: expert e owns rows row_start[e] .. row_start[e+1]-1 and the
+    // batch chunks chunk_prefix[e] .. chunk_prefix[e+1]-1
+    int row_start[kMaxExperts + 1];
+    int chunk_prefix[kMaxExperts + 1];
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -169,13 +183,19 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// Work unit u -> (batch chunk, tile, split index) and its extents.
+// Work unit u -> (batch chunk, tile, split index) and its extents.  bc counts
+// batch chunks over all experts (it indexes the split-K arrival counters);
+// b0 is the unit's first row of x and y; packed / scales / zeros point at the
+// unit's expert.
 struct Unit {
     int bc, tile, sk, g_begin, ng, n0, width, b0, rows, nsteps;
+    const uint8_t* packed;
+    const uint16_t* scales;
+    const uint32_t* zeros;
 };
 
 template <int NT>
-__device__ __forceinline__ Unit decode_unit(const Args& a, int u) {
+__device__ __forceinline__ Unit decode_unit(const Args& a, const Tail* t, int u) {
     constexpr int kRows = 8 * NT;
     Unit w;
     w.sk = u % a.split;
@@ -186,9 +206,28 @@ __device__ __forceinline__ Unit decode_unit(const Args& a, int u) {
     w.ng = min(a.gps, a.K / kGroup - w.g_begin);
     w.n0 = w.tile * kTileCols;
     w.width = packed_tile_width(a.N, w.tile);
-    w.b0 = w.bc * kRows;
-    w.rows = min(kRows, a.B - w.b0);
     w.nsteps = (w.ng + kSlotGroups - 1) / kSlotGroups;
+    if (a.offsets == nullptr) {
+        w.b0 = w.bc * kRows;
+        w.rows = min(kRows, a.B - w.b0);
+        w.packed = a.packed;
+        w.scales = a.scales;
+        w.zeros = a.zeros;
+    } else {
+        // the expert whose chunks hold bc (chunk_prefix is non-decreasing)
+        int lo = 0, hi = a.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (t->chunk_prefix[mid] <= w.bc) lo = mid;
+            else hi = mid - 1;
+        }
+        const int e = lo;
+        w.b0 = t->row_start[e] + (w.bc - t->chunk_prefix[e]) * kRows;
+        w.rows = min(kRows, t->row_start[e + 1] - w.b0);
+        w.packed = a.packed + (size_t)e * a.w_stride;
+        w.scales = a.scales + (size_t)e * a.s_stride;
+        w.zeros = reinterpret_cast<const uint32_t*>(w.packed + ((const uint8_t*)a.zeros - a.packed));
+    }
     return w;
 }
 
@@ -236,7 +275,72 @@ skinny_kernel(const Args a) {
         tail->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (a.offsets != nullptr) {
+        // grouped: the routing table may be written by the previous kernel on
+        // the stream, so wait for it before the first read
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (warp == 0) {
+            // Row boundaries m_i = max(clamp(offsets[j], 0, B), j <= i): the
+            // experts' row ranges are then disjoint and inside x and y whatever
+            // the table holds, and there are at most min(B, B/kRows + E) batch
+            // chunks (the counter prefix is sized for that).  Lane l owns
+            // boundaries 8l+1 .. 8l+8; two warp scans (max, then sum).
+            constexpr int kPer = kMaxExperts / 32;
+            const int b_first = min(max(__ldg(a.offsets), 0), a.B);
+            int m[kPer];
+            int run = 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int i = kPer * lane + j + 1;
+                const int v = i <= a.E ? min(max(__ldg(a.offsets + i), 0), a.B) : 0;
+                run = max(run, v);
+                m[j] = run;
+            }
+            int incl = run;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl = max(incl, o);
+            }
+            int before = __shfl_up_sync(0xffffffffu, incl, 1);
+            before = lane == 0 ? b_first : max(before, b_first);
+            int chunks[kPer];
+            int csum = 0;
+            int prev = before;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                m[j] = max(m[j], before);
+                chunks[j] = (kPer * lane + j < a.E) ? (m[j] - prev + kRows - 1) / kRows : 0;
+                csum += chunks[j];
+                prev = m[j];
+            }
+            int cincl = csum;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, cincl, d);
+                if (lane >= d) cincl += o;
+            }
+            int c = cincl - csum;
+            if (lane == 0) {
+                tail->row_start[0] = b_first;
+                tail->chunk_prefix[0] = 0;
+            }
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int i = kPer * lane + j + 1;
+                c += chunks[j];
+                if (i <= a.E) {
+                    tail->row_start[i] = m[j];
+                    tail->chunk_prefix[i] = c;
+                }
+            }
+            if (lane == 31) tail->total_units = cincl * a.tiles * a.split;
+        }
+    } else if (threadIdx.x == 0) {
+        tail->total_units = a.units;
+    }
     __syncthreads();
+    const int total_units = tail->total_units;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
@@ -249,8 +353,9 @@ skinny_kernel(const Args a) {
         bool ok = true;
         // The first unit is fixed (blockIdx.x): its first slots' code copies go
         // out before waiting for the previous kernel on the stream.
-        const Unit first = decode_unit<NT>(a, blockIdx.x);
-        const uint8_t* first_codes = a.packed + packed_tile_base(a.K, first.tile);
+        const bool has_first = (int)blockIdx.x < total_units;
+        const Unit first = decode_unit<NT>(a, tail, has_first ? (int)blockIdx.x : 0);
+        const uint8_t* first_codes = first.packed + packed_tile_base(a.K, first.tile);
         auto issue_codes = [&](const Unit& w, const uint8_t* tile_codes, int st, int pos) {
             const int s = pos % S;
             const int g0 = w.g_begin + st * kSlotGroups;
@@ -267,7 +372,7 @@ skinny_kernel(const Args a) {
                 "r"(bytes), "r"(full), "l"(evict_first)
                 : "memory");
         };
-        const int pre = min(S, first.nsteps);
+        const int pre = has_first ? min(S, first.nsteps) : 0;
         if (lane == 0) {
             for (int st = 0; st < pre; ++st) {
                 tail->slot_unit[st] = blockIdx.x;
@@ -281,8 +386,19 @@ skinny_kernel(const Args a) {
         int u = blockIdx.x;
         uint32_t* work = a.counters + kWorkCounter;
         while (ok) {
-            const Unit w = decode_unit<NT>(a, u);
-            const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, w.tile);
+            if (u >= total_units) {
+                if (lane == 0) {
+                    // the last CTA to run out of work resets the scheduler words
+                    const uint32_t done = atomicAdd(a.counters + kDoneCounter, 1u);
+                    if (done == gridDim.x - 1) {
+                        a.counters[kWorkCounter] = 0u;
+                        a.counters[kDoneCounter] = 0u;
+                    }
+                }
+                break;
+            }
+            const Unit w = decode_unit<NT>(a, tail, u);
+            const uint8_t* tile_codes = w.packed + packed_tile_base(a.K, w.tile);
             for (int st = 0; st < w.nsteps; ++st, ++step) {
                 const int s = step % S;
                 const uint32_t full = smem_u32(&tail->full[s]);
@@ -315,10 +431,10 @@ skinny_kernel(const Args a) {
                 const int gl = lane >> 4;
                 if (gl < ngs && p < w.width / 8) {
                     cp_async_16(smem_u32(slot_scales(s)) + 2u * (gl * kTileCols + 8 * p),
-                                a.scales + (size_t)(g0 + gl) * a.N + w.n0 + 8 * p);
+                                w.scales + (size_t)(g0 + gl) * a.N + w.n0 + 8 * p);
                     if (kHasZeros)
                         cp_async_4(smem_u32(slot_zeros(s)) + 4u * (gl * (kTileCols / 8) + p),
-                                   a.zeros + (size_t)(g0 + gl) * packed_zero_row_words(a.N) + w.n0 / 8 + p);
+                                   w.zeros + (size_t)(g0 + gl) * packed_zero_row_words(a.N) + w.n0 / 8 + p);
                 }
                 cp_async_arrive_noinc(full);
                 issued = step + 1;
@@ -327,19 +443,7 @@ skinny_kernel(const Args a) {
             // next unit from the work counter (units [0, grid) are the fixed first ones)
             int next = 0;
             if (lane == 0) next = (int)gridDim.x + (int)atomicAdd(work, 1u);
-            next = __shfl_sync(0xffffffffu, next, 0);
-            if (next >= a.units) {
-                if (lane == 0) {
-                    // the last CTA to run out of work resets the scheduler words
-                    const uint32_t done = atomicAdd(a.counters + kDoneCounter, 1u);
-                    if (done == gridDim.x - 1) {
-                        a.counters[kWorkCounter] = 0u;
-                        a.counters[kDoneCounter] = 0u;
-                    }
-                }
-                break;
-            }
-            u = next;
+            u = __shfl_sync(0xffffffffu, next, 0);  // the loop top checks it
         }
         // end marker for the consumers
         if (ok) {
@@ -387,7 +491,7 @@ skinny_kernel(const Args a) {
                 }
                 break;
             }
-            const Unit w = decode_unit<NT>(a, u);
+            const Unit w = decode_unit<NT>(a, tail, u);
             if (st == 0) {
 #pragma unroll
                 for (int bt = 0; bt < NT; ++bt)
@@ -479,7 +583,7 @@ skinny_kernel(const Args a) {
             if (!warp_wait(smem_u32(&tail->res_full[buf]), (k >> 1) & 1, abort, a.status)) break;
             const int u = tail->res_unit[buf];
             if (u < 0) break;
-            const Unit w = decode_unit<NT>(a, u);
+            const Unit w = decode_unit<NT>(a, tail, u);
             const float* r = res + buf * (result_bytes<NT>() / 4);
             const bool mine = c4 < w.width;
             // element (column c, row b) of the unit lives at
@@ -567,32 +671,68 @@ int ctas_per_sm(int nt) { return nt >= 4 ? 1 : 2; }
 
 }  // namespace
 
-SkinnyPlan plan_skinny(int B, int K, int N, int num_sms) {
-    SkinnyPlan p;
-    p.nt = B <= 8 ? 1 : (B <= 16 ? 2 : 4);
-    p.batch_chunks = (B + 8 * p.nt - 1) / (8 * p.nt);
-    p.col_blocks = (N + kTileCols - 1) / kTileCols;
+namespace {
+
+// The K split for `chunks` batch chunks of a K x N layer (see plan_skinny).
+void choose_split(SkinnyPlan& p, long long chunks, int K, int num_sms) {
     const int G = K / kGroup;
-    const long long base = (long long)p.col_blocks * p.batch_chunks;
+    const long long base = (long long)p.col_blocks * chunks;
     const long long slots = (long long)num_sms * ctas_per_sm(p.nt);
-    // Units are handed out dynamically, so only their size matters: the K
-    // split is the smallest that gives every CTA at least one unit (small
-    // layers), and otherwise keeps units of a few ring slots so the tail
-    // (the last units finishing) stays short, without multiplying the
-    // split-K partial traffic.
     int split = 1;
     while (split < G && split < 32 && base * split < slots) ++split;
     while (split < G && split < 32 && base * split < 3 * slots &&
            (G + split - 1) / split > 8)
         ++split;
-    if (base > kMaxCounters - 2) split = 1;
     int gps = (G + split - 1) / split;
     split = (G + gps - 1) / gps;  // no empty units
     p.split = split;
     p.gps = gps;
-    const long long units = base * split;
+}
+
+}  // namespace
+
+SkinnyPlan plan_skinny(int B, int K, int N, int num_sms) {
+    SkinnyPlan p;
+    p.nt = B <= 8 ? 1 : (B <= 16 ? 2 : 4);
+    p.batch_chunks = (B + 8 * p.nt - 1) / (8 * p.nt);
+    p.col_blocks = (N + kTileCols - 1) / kTileCols;
+    // Units are handed out dynamically, so only their size matters: the K
+    // split is the smallest that gives every CTA at least one unit (small
+    // layers), and otherwise keeps units of a few ring slots so the tail
+    // (the last units finishing) stays short, without multiplying the
+    // split-K partial traffic.
+    choose_split(p, p.batch_chunks, K, num_sms);
+    const long long base = (long long)p.col_blocks * p.batch_chunks;
+    if (base > kMaxCounters - 2) {
+        p.split = 1;
+        p.gps = K / kGroup;
+    }
+    const long long slots = (long long)num_sms * ctas_per_sm(p.nt);
+    const long long units = base * p.split;
     p.units = (int)units;
     p.grid = (int)std::min<long long>(units, slots);
+    return p;
+}
+
+SkinnyPlan plan_skinny_grouped(int T, int E, int max_rows, int K, int N, int num_sms) {
+    SkinnyPlan p;
+    p.nt = max_rows <= 8 ? 1 : (max_rows <= 16 ? 2 : 4);
+    const int rows = 8 * p.nt;
+    p.col_blocks = (N + kTileCols - 1) / kTileCols;
+    // the chunks each expert's rows fill are only known on the device: size
+    // the split for the typical count (every expert with rows, or the rows in
+    // full chunks, whichever is more), and keep every possible chunk's
+    // split-K counter inside the counter prefix
+    const long long worst_chunks = std::min<long long>((long long)T, (long long)(T + rows - 1) / rows + E);
+    const long long est_chunks = std::max<long long>((T + rows - 1) / rows, std::min(T, E));
+    choose_split(p, est_chunks, K, num_sms);
+    if (worst_chunks * p.col_blocks > kMaxCounters - 2) {
+        p.split = 1;
+        p.gps = K / kGroup;
+    }
+    p.batch_chunks = (int)worst_chunks;
+    p.units = 0;  // counted on the device
+    p.grid = num_sms * ctas_per_sm(p.nt);
     return p;
 }
 
@@ -601,9 +741,10 @@ size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N) {
     return p.split > 1 ? kCounterBytes + (size_t)B * N * sizeof(float) : kCounterBytes;
 }
 
-cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
-                          const void* scales, bool has_zeros, void* y, int B, int K, int N,
-                          void* workspace, unsigned int* status, cudaStream_t stream) {
+static cudaError_t launch_skinny_impl(const SkinnyPlan& p, const void* x, const void* packed,
+                                      const void* scales, bool has_zeros, void* y, int B, int K,
+                                      int N, void* workspace, unsigned int* status,
+                                      const int* offsets, int E, cudaStream_t stream) {
     Args a;
     a.x = static_cast<const uint16_t*>(x);
     a.packed = static_cast<const uint8_t*>(packed);
@@ -621,6 +762,10 @@ cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed
     a.split = p.split;
     a.gps = p.gps;
     a.units = p.units;
+    a.offsets = offsets;
+    a.E = E;
+    a.w_stride = packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);
+    a.s_stride = (size_t)(K / kGroup) * N;
     switch (p.nt * 2 + (has_zeros ? 1 : 0)) {
         case 2: return launch_t<1, false>(p, a, stream);
         case 3: return launch_t<1, true>(p, a, stream);
@@ -630,6 +775,21 @@ cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed
         case 9: return launch_t<4, true>(p, a, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
+                          const void* scales, bool has_zeros, void* y, int B, int K, int N,
+                          void* workspace, unsigned int* status, cudaStream_t stream) {
+    return launch_skinny_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
+                              nullptr, 0, stream);
+}
+
+cudaError_t launch_skinny_grouped(const SkinnyPlan& p, const void* x, const int* offsets, int E,
+                                  const void* packed, const void* scales, bool has_zeros,
+                                  void* y, int T, int K, int N, void* workspace,
+                                  unsigned int* status, cudaStream_t stream) {
+    return launch_skinny_impl(p, x, packed, scales, has_zeros, y, T, K, N, workspace, status,
+                              offsets, E, stream);
 }
 
 }  // namespace w4a16
