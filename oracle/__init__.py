@@ -17,12 +17,18 @@ Sources, by page title and section:
     its own rows (``gemm_grouped``).
   * "Give Me BF16 or Give Me Death", "W4A16-INT Quantization": round to
     nearest with MSE-optimal clipping (``quantize_rtn_mse``).
+  * "Give Me BF16 or Give Me Death", "W8A8-FP Quantization": per-channel FP8
+    weights, dynamic per-token FP8 activations, their product
+    (``fp8_quantize_rows``, ``fp8_quantize_cols``, ``fp8_gemm``; C source
+    ``w8a8_fp8_oracle.c``).
 
 Parity status: every function here is pinned -- ``tests/test_oracle_pins.py``
 (exhaustive nearest-bf16 check, integer special cases, exact-rational brute
 force, invariants, hand-built unpack cases, the 4.125-bit accounting),
-``tests/test_quantizer_pins.py`` (quantizer) and ``tests/test_grouped_pins.py``
-(closed-form expert routing).
+``tests/test_quantizer_pins.py`` (quantizer), ``tests/test_grouped_pins.py``
+(closed-form expert routing) and ``tests/test_fp8_pins.py`` (E4M3 codec
+against the format's published constants and brute-force nearest search,
+scale invariants, exact integer GEMM).
 """
 from __future__ import annotations
 
@@ -35,6 +41,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "w8a8_fp8_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -44,11 +51,12 @@ GROUP = 128
 
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/liboracle.so`` (gcc, -O2, OpenMP)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    if not force and os.path.exists(_LIB) and \
+            os.path.getmtime(_LIB) >= max(os.path.getmtime(p) for p in _SRCS):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+           "-fno-fast-math", "-ffp-contract=off", *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -83,6 +91,19 @@ def _load():
         lib.oracle_set_threads.restype = None
         lib.oracle_quantize_rtn_mse.argtypes = [u16p, ctypes.c_int, ctypes.c_int, u32p, u16p]
         lib.oracle_quantize_rtn_mse.restype = None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_e4m3_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+        lib.oracle_fp8_quantize_rows.argtypes = [u16p, ctypes.c_int, ctypes.c_int, u8p, f32p]
+        lib.oracle_fp8_quantize_rows.restype = None
+        lib.oracle_fp8_quantize_cols.argtypes = [u16p, ctypes.c_int, ctypes.c_int, u8p, f32p]
+        lib.oracle_fp8_quantize_cols.restype = None
+        lib.oracle_fp8_gemm_cols.argtypes = [u8p, f32p, u8p, f32p, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
+        lib.oracle_fp8_gemm_cols.restype = None
         lib.oracle_format_bits_per_weight.argtypes = [ctypes.c_longlong, ctypes.c_longlong,
                                                       ctypes.c_int]
         lib.oracle_format_bits_per_weight.restype = ctypes.c_double
@@ -215,6 +236,64 @@ def quantize_rtn_mse(w) -> tuple[np.ndarray, np.ndarray]:
     _load().oracle_quantize_rtn_mse(_ptr(w, ctypes.c_uint16), K, N, _ptr(qw, ctypes.c_uint32),
                                     _ptr(sc, ctypes.c_uint16))
     return qw, sc
+
+
+# ---- W8A8-FP8 comparison path ("Give Me BF16 or Give Me Death", section
+# "W8A8-FP Quantization: 8-Bit Floating-Point Weights and Activations")
+
+def e4m3_to_double(code: int) -> float:
+    return float(_load().oracle_e4m3_to_double(int(code)))
+
+
+def e4m3_from_double(v: float) -> int:
+    return int(_load().oracle_e4m3_from_double(float(v)))
+
+
+def fp8_quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
+    """Dynamic per-token quantisation: bf16 bits x [B][K] -> (E4M3 codes uint8
+    [B][K], binary32 scales [B])."""
+    x = _as_u16(x)
+    B, K = x.shape
+    codes = np.zeros((B, K), dtype=np.uint8)
+    sc = np.zeros(B, dtype=np.float32)
+    _load().oracle_fp8_quantize_rows(_ptr(x, ctypes.c_uint16), B, K,
+                                     _ptr(codes, ctypes.c_uint8), _ptr(sc, ctypes.c_float))
+    return codes, sc
+
+
+def fp8_quantize_cols(w) -> tuple[np.ndarray, np.ndarray]:
+    """Per-output-channel weight quantisation: bf16 bits W [K][N] -> (E4M3
+    codes uint8 [N][K], binary32 scales [N])."""
+    w = _as_u16(w)
+    K, N = w.shape
+    codes = np.zeros((N, K), dtype=np.uint8)
+    sc = np.zeros(N, dtype=np.float32)
+    _load().oracle_fp8_quantize_cols(_ptr(w, ctypes.c_uint16), K, N,
+                                     _ptr(codes, ctypes.c_uint8), _ptr(sc, ctypes.c_float))
+    return codes, sc
+
+
+def fp8_gemm(xq, sx, wq, sw, cols=None):
+    """y = (s_x q_x) . (s_w q_w) on the listed columns: returns (y bf16 bits
+    [B][ncols], acc = exact code sum float64, bound float64)."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    B, K = xq.shape
+    N = wq.shape[0]
+    assert wq.shape == (N, K) and sx.shape == (B,) and sw.shape == (N,)
+    assert K <= 1 << 15, "the exact-sum argument holds for K <= 2^15"
+    c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, dtype=np.int32)
+    nc = int(c.shape[0])
+    y = np.empty((B, nc), dtype=np.uint16)
+    acc = np.empty((B, nc), dtype=np.float64)
+    bound = np.empty((B, nc), dtype=np.float64)
+    _load().oracle_fp8_gemm_cols(_ptr(xq, ctypes.c_uint8), _ptr(sx, ctypes.c_float),
+                                 _ptr(wq, ctypes.c_uint8), _ptr(sw, ctypes.c_float), B, K, N,
+                                 _ptr(c, ctypes.c_int), nc, _ptr(y, ctypes.c_uint16),
+                                 _ptr(acc, ctypes.c_double), _ptr(bound, ctypes.c_double))
+    return y, acc, bound
 
 
 def format_bits_per_weight(K: int, N: int, has_zeros: bool) -> float:
