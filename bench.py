@@ -705,6 +705,126 @@ def run_moe(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------- FP8 comparison
+
+def run_fp8(args):
+    """The three regimes on one GPU: one Llama-3-8B decoder layer's linear set
+    at batch B as W8A8-FP8 (dynamic per-token activation quantisation + FP8
+    tensor-core GEMM, per-channel weight scales), beside the same set as
+    W4A16 and as plain bf16 (torch.matmul, i.e. cuBLAS).  One line per B; the
+    line's value is the FP8 step time."""
+    import torch
+
+    import weight_only_int4_gemm_gb300 as w
+    from weight_only_int4_gemm_gb300 import inputs
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from __graft_entry__ import build
+    build()
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    batches = [args.batch] if args.batch else [1, 16, 64, 128, 256, 512, 1024]
+    n_copies = 2
+    fp8_w, w4_w, bf_w = {}, {}, {}
+    for lbl, K, N in LAYER:
+        fp8_w[lbl], w4_w[lbl], bf_w[lbl] = [], [], []
+        for c in range(n_copies):
+            wt = inputs.make_dense_weight(K, N, seed=K + N + 7919 * c, device=device)
+            fp8_w[lbl].append(w.w8a8_fp8_quantize_weight(wt))
+            qw, sc, _ = inputs.make_weights(K, N, seed=K * 3 + N + 7919 * c, device=device)
+            w4_w[lbl].append((w.w4a16_pack(qw), sc))
+            bf_w[lbl].append(wt)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device)
+
+    def time_graphs(step_fn, steps):
+        graphs = []
+        with torch.cuda.stream(stream):
+            for c in range(n_copies):
+                step_fn(c)
+        stream.synchronize()
+        for c in range(n_copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step_fn(c)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for k in range(max(3, args.warmup)):
+                graphs[k % n_copies].replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in range(steps):
+                graphs[k % n_copies].replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / steps * 1e3  # µs per step
+
+    for B in batches:
+        xs = {lbl: inputs.make_activations(B, K, seed=50 + K + N, device=device)
+              for lbl, K, N in LAYER}
+        xq = {lbl: (torch.empty((B, K), dtype=torch.uint8, device=device),
+                    torch.empty(B, dtype=torch.float32, device=device)) for lbl, K, N in LAYER}
+        ys = {lbl: torch.empty((B, N), dtype=torch.bfloat16, device=device) for lbl, K, N in LAYER}
+        ws = torch.zeros(max(max(w.w8a8_fp8_workspace_bytes(B, K, N),
+                                 w.w4a16_workspace_bytes(B, K, N)) for _, K, N in LAYER) + 256,
+                         dtype=torch.uint8, device=device)
+
+        def fp8_step(c):
+            for lbl, K, N in LAYER:
+                q, sxb = w.w8a8_fp8_quantize_act(xs[lbl], out=xq[lbl], stream=stream)
+                wq, sw = fp8_w[lbl][c]
+                w.w8a8_fp8_gemm(q, sxb, wq, sw, out=ys[lbl], workspace=ws, stream=stream)
+
+        def w4_step(c):
+            for lbl, K, N in LAYER:
+                packed, sc = w4_w[lbl][c]
+                w.w4a16_gemm(xs[lbl], packed, sc, False, N, out=ys[lbl], workspace=ws,
+                             stream=stream)
+
+        def bf16_step(c):
+            for lbl, K, N in LAYER:
+                torch.matmul(xs[lbl], bf_w[lbl][c], out=ys[lbl])
+
+        steps = max(20, min(args.steps, 2000 if B <= 128 else 300))
+        with ClockSampler(0) as clk:
+            t_fp8 = time_graphs(fp8_step, steps)
+        assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
+        t_w4 = time_graphs(w4_step, steps)
+        t_bf = time_graphs(bf16_step, steps)
+        wbytes = sum(K * N + 4 * N for _, K, N in LAYER)
+        abytes = sum(B * K * 2 + B * K * 2 + 4 * B + B * N * 2 for _, K, N in LAYER)
+        flops = sum(2 * B * K * N for _, K, N in LAYER)
+        fp8_peak = 2.0 * tf_sust
+        memory_bound = (wbytes + abytes) / (hbm * 1e9) >= flops / (fp8_peak * 1e12)
+        t = t_fp8 * 1e-6
+        if memory_bound:
+            ach = (wbytes + abytes) / t / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "peak_source": f"{peak_src} hbm_gbs"}
+        else:
+            ach = flops / t / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": ach / fp8_peak,
+                    "peak_source": f"{peak_src} bf16 sustained x 2 (nominal fp8/bf16 ratio)"}
+        roof.update({"kernel": "fp8_gemm_kernel + fp8_quant_rows_kernel (whole step)",
+                     "traffic": None, "algorithmic_bytes_per_step": wbytes + abytes})
+        line = {"metric": "W8A8-FP8 linear set µs/step (comparison path), beside W4A16 and "
+                          "bf16 cuBLAS", "value": t_fp8, "unit": "µs/step", "n_gpus": 1,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": t_fp8 / 1e3,
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic (seeded; Llama-3-8B shapes)",
+                "config": {"workload": "fp8", "batch": B,
+                           "gemms": [f"{lbl} {K}x{N}" for lbl, K, N in LAYER],
+                           "l2": f"weights rotated over {n_copies} copies", "cuda_graph": True},
+                "compare": {"w4a16_us": t_w4, "bf16_cublas_us": t_bf,
+                            "fp8_over_w4a16": t_fp8 / t_w4, "fp8_over_bf16": t_fp8 / t_bf},
+                "tflops": flops / t / 1e12, "roofline": roof, "clocks": clk.summary(),
+                "gpu_launches": steps * 2 * len(LAYER)}
+        print(json.dumps(line), flush=True)
+        del xs, xq, ys, ws
+
+
 # --------------------------------------------------------------- main
 
 def main():
@@ -715,7 +835,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_layer",
                     choices=["decode_layer", "single", "decode_step", "prefill", "zp70b",
-                             "quantize", "moe"])
+                             "quantize", "moe", "fp8"])
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--shape", default=None, help="KxN for --workload single (default 4096x4096)")
     ap.add_argument("--e2e-steps", type=int, default=300)
@@ -736,6 +856,11 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.workload == "quantize":
         run_quantize(args)
+        return
+    if args.workload == "fp8":
+        if args.impl == "reference" or rank != 0:
+            raise SystemExit("--workload fp8 runs our arm on one GPU only")
+        run_fp8(args)
         return
     if args.workload == "moe":
         if args.impl == "reference" or rank != 0:

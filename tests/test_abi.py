@@ -11,16 +11,18 @@ import weight_only_int4_gemm_gb300 as w
 from weight_only_int4_gemm_gb300 import _lib
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "w4a16.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("w4a16.h", "w8a8_fp8.h")]
 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_UNSUP, ERR_WS = 0, 1, 2, 3, 4, 5
 FAKE = 0x10000  # an aligned, never-dereferenced address
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4a16_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:w4a16|w8a8_fp8)_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -32,6 +34,7 @@ def lib():
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert "w4a16_gemm" in names and "w4a16_pack" in names and "w4a16_dequant_ref" in names
+    assert "w8a8_fp8_gemm" in names and "w8a8_fp8_quantize_act" in names
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with header"
@@ -136,6 +139,41 @@ def test_grouped_validation(lib):
     assert _grouped(lib, offsets=FAKE + 2) == ERR_ALIGN
     assert _grouped(lib, ws=FAKE + 4) == ERR_ALIGN
     assert _grouped(lib, ws_bytes=need - 1) == ERR_WS
+
+
+def test_fp8_validation(lib):
+    bad = ctypes.c_size_t(-1).value
+    assert lib.w8a8_fp8_workspace_bytes(1, 4096, 4096) > 0  # small batch splits K
+    assert lib.w8a8_fp8_workspace_bytes(0, 4096, 4096) == bad
+    assert lib.w8a8_fp8_workspace_bytes(1, 100, 4096) == bad
+    assert lib.w8a8_fp8_quantize_act(FAKE, 4, 100, FAKE, FAKE, None) == ERR_SHAPE
+    assert lib.w8a8_fp8_quantize_act(FAKE, 0, 128, FAKE, FAKE, None) == ERR_SHAPE
+    assert lib.w8a8_fp8_quantize_act(None, 4, 128, FAKE, FAKE, None) == ERR_NULL
+    assert lib.w8a8_fp8_quantize_act(FAKE, 4, 128, FAKE + 8, FAKE, None) == ERR_ALIGN
+    assert lib.w8a8_fp8_quantize_act(FAKE, 4, 128, FAKE, FAKE + 2, None) == ERR_ALIGN
+    assert lib.w8a8_fp8_quantize_weight(FAKE, 128, 12, FAKE, FAKE, None) == ERR_SHAPE
+    assert lib.w8a8_fp8_quantize_weight(FAKE, 128, 8, None, FAKE, None) == ERR_NULL
+    assert lib.w8a8_fp8_quantize_weight(FAKE + 4, 128, 8, FAKE, FAKE, None) == ERR_ALIGN
+
+    def gemm(xq=FAKE, sx=FAKE, wq=FAKE, sw=FAKE, y=FAKE, B=1, K=4096, N=4096, ws=FAKE,
+             ws_bytes=None):
+        if ws_bytes is None:
+            ws_bytes = lib.w8a8_fp8_workspace_bytes(B, K, N)
+        return lib.w8a8_fp8_gemm(xq, sx, wq, sw, y, B, K, N, ws, ws_bytes, None)
+
+    assert gemm(K=96, ws_bytes=0) == ERR_SHAPE
+    assert gemm(N=4, ws_bytes=0) == ERR_SHAPE
+    assert gemm(B=0, ws_bytes=0) == ERR_SHAPE
+    assert gemm(sw=None) == ERR_NULL
+    assert gemm(y=None) == ERR_NULL
+    assert gemm(xq=FAKE + 8) == ERR_ALIGN
+    assert gemm(sx=FAKE + 1) == ERR_ALIGN
+    assert gemm(ws=None) == ERR_NULL
+    assert gemm(ws=FAKE + 4) == ERR_ALIGN
+    need = lib.w8a8_fp8_workspace_bytes(1, 4096, 4096)
+    assert gemm(ws_bytes=need - 1) == ERR_WS
+    # valid arguments without tcgen05 tensor cores: refused, nothing launched
+    assert gemm() == ERR_UNSUP
 
 
 def test_status_strings(lib):

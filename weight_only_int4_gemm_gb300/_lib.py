@@ -42,6 +42,11 @@ SIGNATURES = {
     "w4a16_grouped_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "w4a16_gemm_grouped": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
+    # include/w8a8_fp8.h
+    "w8a8_fp8_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
+    "w8a8_fp8_quantize_weight": (_I, [_P, _I, _I, _P, _P, _P]),
+    "w8a8_fp8_workspace_bytes": (_S, [_I, _I, _I]),
+    "w8a8_fp8_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _S, _P]),
 }
 
 
@@ -257,3 +262,65 @@ def w4a16_debug_forced_timeout(x: torch.Tensor, packed: torch.Tensor, scales: to
 
 def w4a16_device_status(clear: bool = True) -> int:
     return int(load().w4a16_device_status(1 if clear else 0))
+
+
+# ---- W8A8-FP8 comparison path (include/w8a8_fp8.h)
+
+def w8a8_fp8_quantize_act(x: torch.Tensor, *, out: tuple | None = None,
+                          stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Dynamic per-token quantisation: bf16 x [B][K] -> (E4M3 codes uint8 [B][K],
+    fp32 scales [B])."""
+    B, K = x.shape
+    _need(x, torch.bfloat16, (B, K), "x")
+    if out is None:
+        out = (torch.empty((B, K), dtype=torch.uint8, device=x.device),
+               torch.empty(B, dtype=torch.float32, device=x.device))
+    xq, sx = out
+    _need(xq, torch.uint8, (B, K), "xq")
+    _need(sx, torch.float32, (B,), "sx")
+    _check("w8a8_fp8_quantize_act", load().w8a8_fp8_quantize_act(
+        x.data_ptr(), B, K, xq.data_ptr(), sx.data_ptr(), _stream(stream)))
+    return xq, sx
+
+
+def w8a8_fp8_quantize_weight(w: torch.Tensor, *, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Per-output-channel quantisation: bf16 W [K][N] -> (E4M3 codes uint8 [N][K],
+    fp32 scales [N])."""
+    K, N = w.shape
+    _need(w, torch.bfloat16, (K, N), "w")
+    wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    sw = torch.empty(N, dtype=torch.float32, device=w.device)
+    _check("w8a8_fp8_quantize_weight", load().w8a8_fp8_quantize_weight(
+        w.data_ptr(), K, N, wq.data_ptr(), sw.data_ptr(), _stream(stream)))
+    return wq, sw
+
+
+def w8a8_fp8_workspace_bytes(B: int, K: int, N: int) -> int:
+    v = int(load().w8a8_fp8_workspace_bytes(B, K, N))
+    if v == ctypes.c_size_t(-1).value:
+        raise ValueError(f"invalid shape B={B} K={K} N={N}")
+    return v
+
+
+def w8a8_fp8_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor, *,
+                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """y[B][N] = (sx * dec(xq)) . (sw * dec(wq))^T, bf16."""
+    B, K = xq.shape
+    N = wq.shape[0]
+    _need(xq, torch.uint8, (B, K), "xq")
+    _need(wq, torch.uint8, (N, K), "wq")
+    _need(sx, torch.float32, (B,), "sx")
+    _need(sw, torch.float32, (N,), "sw")
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.bfloat16, device=xq.device)
+    _need(out, torch.bfloat16, (B, N), "out")
+    need = w8a8_fp8_workspace_bytes(B, K, N)
+    if workspace is None:
+        workspace = _default_ws.get(need, xq.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w8a8_fp8_gemm", load().w8a8_fp8_gemm(
+        xq.data_ptr(), sx.data_ptr(), wq.data_ptr(), sw.data_ptr(), out.data_ptr(), B, K, N,
+        ws_ptr, ws_bytes, _stream(stream)))
+    return out

@@ -7,6 +7,7 @@
 #include <unordered_map>
 
 #include "w4a16.h"
+#include "w8a8_fp8.h"
 #include "launch.cuh"
 
 namespace w4a16 {
@@ -231,6 +232,51 @@ w4a16_status w4a16_gemm_grouped(const void* x, const int* offsets, int E, int T,
     return from_cuda(launch_skinny_grouped(p, x, offsets, E, packed, scales, has_zeros != 0, y, T,
                                            K, N, workspace, status,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w8a8_fp8_quantize_act(const void* x, int B, int K, void* xq, float* sx,
+                                   void* stream) {
+    if (!shape_ok(K, 8) || B < 1 || B > kMaxB) return W4A16_ERR_SHAPE;
+    if (!x || !xq || !sx) return W4A16_ERR_NULL;
+    if (!aligned16(x) || !aligned16(xq) || (reinterpret_cast<uintptr_t>(sx) & 3u) != 0)
+        return W4A16_ERR_ALIGN;
+    return from_cuda(launch_fp8_quantize_rows(x, B, K, xq, sx, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w8a8_fp8_quantize_weight(const void* w, int K, int N, void* wq, float* sw,
+                                      void* stream) {
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (!w || !wq || !sw) return W4A16_ERR_NULL;
+    if (!aligned16(w) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u) != 0)
+        return W4A16_ERR_ALIGN;
+    return from_cuda(launch_fp8_quantize_cols(w, K, N, wq, sw, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w8a8_fp8_workspace_bytes(int B, int K, int N) {
+    if (!shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
+    return fp8_workspace_bytes(plan_fp8(B, K, N, num_sms()), B, N);
+}
+
+w4a16_status w8a8_fp8_gemm(const void* xq, const float* sx, const void* wq, const float* sw,
+                           void* y, int B, int K, int N, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    if (!shape_ok(K, N) || B < 1 || B > kMaxB) return W4A16_ERR_SHAPE;
+    if (!xq || !sx || !wq || !sw || !y) return W4A16_ERR_NULL;
+    if (!aligned16(xq) || !aligned16(wq) || !aligned16(y) ||
+        ((reinterpret_cast<uintptr_t>(sx) | reinterpret_cast<uintptr_t>(sw)) & 3u) != 0)
+        return W4A16_ERR_ALIGN;
+    const Fp8Plan p = plan_fp8(B, K, N, num_sms());
+    const size_t need = fp8_workspace_bytes(p, B, N);
+    if (need > 0) {
+        if (workspace == nullptr) return W4A16_ERR_NULL;
+        if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
+        if (ws_bytes < need) return W4A16_ERR_WORKSPACE;
+    }
+    if (!tc_available()) return W4A16_ERR_UNSUPPORTED;
+    unsigned int* status = device_status_word();
+    if (status == nullptr) return W4A16_ERR_CUDA;
+    return from_cuda(launch_fp8_gemm(p, xq, sx, wq, sw, y, B, K, N, workspace, status,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_quantize_rtn(const void* w, int K, int N, int group_size, uint32_t* qweight,

@@ -97,6 +97,25 @@ cudaError_t launch_tc_wide(const TcPlan& p, const void* x, const void* packed,
                            void* workspace, unsigned int* status, int force_timeout_ms,
                            cudaStream_t stream);
 
+// ---- W8A8-FP8 comparison path (fp8.cu) ----
+struct Fp8Plan {
+    int bn;           // batch rows per tile (MMA N): 16 .. 256, multiple of 16
+    int batch_tiles;  // ceil(B / bn)
+    int col_tiles;    // ceil(N / 128)
+    int kb_per_split; // 128-row K blocks per split
+    int split;        // K splits (1 = no workspace)
+    int grid;         // persistent CTAs
+};
+Fp8Plan plan_fp8(int B, int K, int N, int num_sms);
+size_t fp8_workspace_bytes(const Fp8Plan& p, int B, int N);
+cudaError_t launch_fp8_quantize_rows(const void* x, int B, int K, void* xq, float* sx,
+                                     cudaStream_t stream);
+cudaError_t launch_fp8_quantize_cols(const void* w, int K, int N, void* wq, float* sw,
+                                     cudaStream_t stream);
+cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx, const void* wq,
+                            const float* sw, void* y, int B, int K, int N, void* workspace,
+                            unsigned int* status, cudaStream_t stream);
+
 // Validation + dispatch + launch shared by the C entry points (api.cu).
 // Returns a w4a16_status value.
 int gemm_entry(const void* x, const void* packed, const void* scales, int has_zeros, void* y,

@@ -17,7 +17,9 @@ Recipe (shapes and value distributions of the workloads):
                 experts of E uniformly at random (the uniform-routing
                 assumption of the pages' effective-M estimate); the routed
                 rows are grouped by expert, giving per-expert row offsets;
-                expert e's weights are drawn like one layer's, seed + e.
+                expert e's weights are drawn like one layer's, seed + e;
+  * dense    -- bf16 weights W [K][N] for the quantisers and the FP8
+                comparison path: N(0, 1) * 0.02 rounded to bf16.
 
 Draws use ``torch.Generator(device).manual_seed(seed)``; CPU and CUDA
 generators give different streams, so each comparison uses one generated copy
@@ -129,3 +131,10 @@ def make_grouped_problem(offsets: torch.Tensor, K: int, N: int, seed: int, *,
     qzeros = torch.stack([w[2] for w in ws]) if zero_points else None
     x = make_activations(T, K, seed + 1_000_003, device=device)
     return GroupedProblem(x, offsets.to(device), qweight, scales, qzeros)
+
+
+def make_dense_weight(K: int, N: int, seed: int, *, device="cpu") -> torch.Tensor:
+    """bf16 W [K][N], N(0, 1) * 0.02."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return (torch.randn((K, N), generator=gen, device=device) * 0.02).to(torch.bfloat16)
