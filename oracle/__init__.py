@@ -26,7 +26,9 @@ Parity status: every function here is pinned -- ``tests/test_oracle_pins.py``
 (exhaustive nearest-bf16 check, integer special cases, exact-rational brute
 force, invariants, hand-built unpack cases, the 4.125-bit accounting),
 ``tests/test_quantizer_pins.py`` (quantizer), ``tests/test_grouped_pins.py``
-(closed-form expert routing) and ``tests/test_fp8_pins.py`` (E4M3 codec
+(closed-form expert routing), ``tests/test_epilogue_pins.py`` (closed-form
+bias and SiLU-gate cases, an independent tanh route to silu) and
+``tests/test_fp8_pins.py`` (E4M3 codec
 against the format's published constants and brute-force nearest search,
 scale invariants, exact integer GEMM).
 """
@@ -87,6 +89,8 @@ def _load():
         lib.oracle_gemm_cols.argtypes = [u16p, u32p, u16p, u32p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
         lib.oracle_gemm_cols.restype = None
+        lib.oracle_bf16_from_double_array.argtypes = [f64p, ctypes.c_longlong, u16p]
+        lib.oracle_bf16_from_double_array.restype = None
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_set_threads.restype = None
         lib.oracle_quantize_rtn_mse.argtypes = [u16p, ctypes.c_int, ctypes.c_int, u32p, u16p]
@@ -195,6 +199,59 @@ def gemm(x, qweight, scales, qzeros=None, cols=None):
                              _ptr(y, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
                              _ptr(bound, ctypes.c_double))
     return y, acc, bound
+
+
+def bf16_round(v) -> np.ndarray:
+    """RNE_bf16 of every element of a float64 array (bit patterns)."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().oracle_bf16_from_double_array(_ptr(a, ctypes.c_double), a.size,
+                                          _ptr(out, ctypes.c_uint16))
+    return out
+
+
+EPI_BIAS, EPI_SILU_MUL = 1, 2
+SILU_SLOPE_MAX = 1.1  # sup |d/dg silu(g)| = 1.0998...
+
+
+def silu(g):
+    """silu(g) = g / (1 + e^-g), float64."""
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def gemm_epilogue(x, qweight, scales, qzeros=None, bias=None, mode=0, cols=None):
+    """GEMM with a fused output epilogue, on the exact sums of ``gemm``.
+
+    mode: EPI_BIAS adds bias[n] (bf16 bits [N]); EPI_SILU_MUL treats columns
+    (2j, 2j+1) as (gate, up) and returns h[b][j] = RNE_bf16(silu(g) * u).
+    With EPI_SILU_MUL, ``cols`` (if given) lists gate columns 2j; their up
+    partners are added.  Returns (y bits, value before rounding, bound): the
+    bound is the GEMM bound carried through the epilogue -- for the SiLU form
+    1.1 * b_g * (|u| + b_u) + |silu(g)| * b_u (slope of silu at most 1.1) plus
+    one bf16 step of the result, 2^-7 |h|.
+    """
+    silu_mode = bool(mode & EPI_SILU_MUL)
+    if silu_mode and cols is not None:
+        gates = np.asarray(cols, dtype=np.int64)
+        assert np.all(gates % 2 == 0)
+        cols = np.stack([gates, gates + 1], axis=1).reshape(-1)
+    _, acc, bound = gemm(x, qweight, scales, qzeros, cols=cols)
+    N = _as_u32(qweight).shape[1]
+    c = np.arange(N) if cols is None else np.asarray(cols)
+    v = acc.copy()
+    if mode & EPI_BIAS:
+        bb = _as_u16(bias).astype(np.uint32)
+        bvals = (bb << 16).view(np.float32).astype(np.float64)[c]
+        v = v + bvals[None, :]
+        bound = bound + 2.0 ** -7 * np.abs(bvals)[None, :]
+    if not silu_mode:
+        return bf16_round(v), v, bound
+    g, u = v[:, 0::2], v[:, 1::2]
+    bg, bu = bound[:, 0::2], bound[:, 1::2]
+    h = silu(g) * u
+    hb = SILU_SLOPE_MAX * bg * (np.abs(u) + bu) + np.abs(silu(g)) * bu + 2.0 ** -7 * np.abs(h) + 1e-6
+    return bf16_round(h), h, hb
 
 
 def gemm_grouped(x, offsets, qweights, scales, qzeros=None, cols=None):

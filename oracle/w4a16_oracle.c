@@ -112,6 +112,13 @@ uint16_t oracle_bf16_from_double(double v)
     return (uint16_t)(sign | (uint16_t)(field << 7) | frac);
 }
 
+/* Element-wise oracle_bf16_from_double over an array. */
+void oracle_bf16_from_double_array(const double *v, long long n, uint16_t *out)
+{
+    for (long long i = 0; i < n; ++i)
+        out[i] = oracle_bf16_from_double(v[i]);
+}
+
 /* Code of weight (k, n) from the canonical uint32 [K/8][N] array. */
 int oracle_code(const uint32_t *qweight, int N, int k, int n)
 {
