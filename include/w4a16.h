@@ -121,6 +121,32 @@ w4a16_status w4a16_gemm(const void *x, const void *packed, const void *scales, i
                         void *y, int B, int K, int N, int group_size,
                         void *workspace, size_t ws_bytes, void *stream);
 
+/* Fused output epilogues (flags, may be combined): the sums are converted
+ * once, after the K reduction, so nothing extra goes through HBM.
+ *   W4A16_EPI_BIAS      y[b][n] = bf16(acc[b][n] + bias[n])
+ *   W4A16_EPI_SILU_MUL  gated MLP: the N columns are interleaved gate / up
+ *                       (column 2j = gate j, column 2j + 1 = up j) and
+ *                       y[b][j] = bf16(silu(g) * u), silu(g) = g / (1 + e^-g),
+ *                       with g and u the (biased) fp32 sums; y is [B][N/2]. */
+enum {
+    W4A16_EPI_NONE = 0,
+    W4A16_EPI_BIAS = 1,
+    W4A16_EPI_SILU_MUL = 2
+};
+
+/* w4a16_gemm with a fused epilogue (W4A16_EPI_* flags).
+ *   bias   device bf16 [N], 16-byte aligned; required with W4A16_EPI_BIAS,
+ *          ignored otherwise
+ *   y      device bf16 [B][N], or [B][N/2] with W4A16_EPI_SILU_MUL
+ * Other arguments, the path choice and the workspace as for w4a16_gemm.
+ * Errors: UNSUPPORTED for unknown flags, NULL / ALIGN for the bias, then as
+ * w4a16_gemm.  The gated form needs a weight whose gate and up columns were
+ * interleaved before quantisation (a column permutation of [W_gate | W_up]). */
+w4a16_status w4a16_gemm_fused(const void *x, const void *packed, const void *scales,
+                              int has_zeros, const void *bias, int epilogue, void *y, int B,
+                              int K, int N, int group_size, void *workspace, size_t ws_bytes,
+                              void *stream);
+
 /* As w4a16_gemm, but with the kernel path forced (W4A16_PATH_*; AUTO = same
  * as w4a16_gemm).  For tests and ablations; the result must agree with
  * every other path within the GEMM error bound. */

@@ -141,6 +141,19 @@ def test_grouped_validation(lib):
     assert _grouped(lib, ws_bytes=need - 1) == ERR_WS
 
 
+def test_fused_validation(lib):
+    def fused(bias=FAKE, epi=1, y=FAKE, B=1, K=128, N=8, group=128):
+        return lib.w4a16_gemm_fused(FAKE, FAKE, FAKE, 0, bias, epi, y, B, K, N, group, None, 0,
+                                    None)
+    assert fused(epi=4) == ERR_UNSUP
+    assert fused(epi=-1) == ERR_UNSUP
+    assert fused(bias=None) == ERR_NULL
+    assert fused(bias=FAKE + 2) == ERR_ALIGN
+    assert fused(epi=2, bias=None, K=100) == ERR_SHAPE   # bias not needed without the flag
+    assert fused(group=64) == ERR_UNSUP
+    assert fused(y=None) == ERR_NULL
+
+
 def test_fp8_validation(lib):
     bad = ctypes.c_size_t(-1).value
     assert lib.w8a8_fp8_workspace_bytes(1, 4096, 4096) > 0  # small batch splits K

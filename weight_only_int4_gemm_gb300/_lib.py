@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libw4a16.so")
 GROUP = 128
 
 PATH_AUTO, PATH_SKINNY, PATH_TCGEN05 = -1, 0, 1
+EPI_NONE, EPI_BIAS, EPI_SILU_MUL = 0, 1, 2
 PATH_NAMES = {PATH_SKINNY: "skinny", PATH_TCGEN05: "tcgen05"}
 
 _STATUS = {0: "W4A16_OK", 1: "W4A16_ERR_NULL", 2: "W4A16_ERR_SHAPE", 3: "W4A16_ERR_ALIGN",
@@ -32,6 +33,7 @@ SIGNATURES = {
     "w4a16_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "w4a16_pack": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "w4a16_gemm": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "w4a16_gemm_fused": (_I, [_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
     "w4a16_gemm_path": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_dequant_ref": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
     "w4a16_gemm_static_scratch": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),
@@ -181,6 +183,37 @@ def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, has_
                                  1 if has_zeros else 0, out.data_ptr(), B, K, N, GROUP,
                                  ws_ptr, ws_bytes, int(path), _stream(stream))
         _check("w4a16_gemm_path", st)
+    return out
+
+
+def w4a16_gemm_fused(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                     has_zeros: bool, epilogue: int, bias: torch.Tensor | None = None, *,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """w4a16_gemm with a fused epilogue (EPI_BIAS and/or EPI_SILU_MUL): bias
+    bf16 [N]; with EPI_SILU_MUL the N columns are interleaved gate/up pairs and
+    the output is [B][N/2]."""
+    B, K = x.shape
+    N = scales.shape[1]
+    _need(x, torch.bfloat16, (B, K), "x")
+    _need(scales, torch.bfloat16, (K // GROUP, N), "scales")
+    if packed.numel() * packed.element_size() < w4a16_packed_bytes(K, N, has_zeros):
+        raise ValueError("packed: too small for this shape")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (N,), "bias")
+    n_out = N // 2 if epilogue & EPI_SILU_MUL else N
+    if out is None:
+        out = torch.empty((B, n_out), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (B, n_out), "out")
+    need = w4a16_workspace_bytes(B, K, N)
+    if workspace is None:
+        workspace = _default_ws.get(need, x.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w4a16_gemm_fused", load().w4a16_gemm_fused(
+        x.data_ptr(), packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0,
+        None if bias is None else bias.data_ptr(), int(epilogue), out.data_ptr(), B, K, N, GROUP,
+        ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

@@ -92,7 +92,8 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 
 w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, int has_zeros,
                        void* y, int B, int K, int N, int group_size, void* workspace,
-                       size_t ws_bytes, int path, void* stream, int forced_timeout_ms = 0) {
+                       size_t ws_bytes, int path, void* stream, int forced_timeout_ms = 0,
+                       const Epilogue& epi = Epilogue{}) {
     if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
     if (!shape_ok(K, N) || B < 1 || B > kMaxB) return W4A16_ERR_SHAPE;
     if (!x || !packed || !scales || !y) return W4A16_ERR_NULL;
@@ -112,13 +113,13 @@ w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, in
     if (status == nullptr) return W4A16_ERR_CUDA;
     if (path == W4A16_PATH_SKINNY)
         return from_cuda(launch_skinny(plan_skinny(B, K, N, num_sms()), x, packed, scales,
-                                       has_zeros != 0, y, B, K, N, workspace, status, s));
+                                       has_zeros != 0, y, B, K, N, workspace, status, epi, s));
     if (forced_timeout_ms > 0)
         return from_cuda(launch_tc_forced_timeout(plan_tc(B, K, N, num_sms()), x, packed, scales,
                                                   has_zeros != 0, y, B, K, N, workspace, status,
                                                   forced_timeout_ms, s));
     return from_cuda(launch_tc(plan_tc(B, K, N, num_sms()), x, packed, scales, has_zeros != 0,
-                               y, B, K, N, workspace, status, s));
+                               y, B, K, N, workspace, status, epi, s));
 }
 
 }  // namespace
@@ -204,6 +205,21 @@ w4a16_status w4a16_dequant_ref(const void* packed, const void* scales, int has_z
     if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return W4A16_ERR_ALIGN;
     return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_gemm_fused(const void* x, const void* packed, const void* scales,
+                              int has_zeros, const void* bias, int epilogue, void* y, int B, int K,
+                              int N, int group_size, void* workspace, size_t ws_bytes,
+                              void* stream) {
+    if ((epilogue & ~(W4A16_EPI_BIAS | W4A16_EPI_SILU_MUL)) != 0) return W4A16_ERR_UNSUPPORTED;
+    const bool want_bias = (epilogue & W4A16_EPI_BIAS) != 0;
+    if (want_bias && bias == nullptr) return W4A16_ERR_NULL;
+    if (want_bias && !aligned16(bias)) return W4A16_ERR_ALIGN;
+    Epilogue epi;
+    epi.bias = want_bias ? static_cast<const uint16_t*>(bias) : nullptr;
+    epi.mode = epilogue;
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     W4A16_PATH_AUTO, stream, 0, epi);
 }
 
 size_t w4a16_grouped_workspace_bytes(int T, int E, int max_rows, int K, int N, int group_size) {

@@ -30,6 +30,15 @@ inline float* ws_partials(void* ws) {
                          : reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
 }
 
+// Fused output epilogue (applied where the fp32 sums become bf16; see
+// epilogue.cuh): flags of W4A16_EPI_* in w4a16.h.
+constexpr int kEpiBias = 1;     // y = acc + bias[n]
+constexpr int kEpiSiluMul = 2;  // y[b][j] = silu(acc[b][2j]) * acc[b][2j+1], y is [B][N/2]
+struct Epilogue {
+    const uint16_t* bias = nullptr;  // bf16 [N] with kEpiBias
+    int mode = 0;
+};
+
 // Programmatic dependent launch: kernels may start (and prefetch weights)
 // while the previous kernel on the stream finishes; they wait before reading
 // activations or touching outputs and workspace.
@@ -64,7 +73,8 @@ cudaError_t launch_skinny_grouped(const SkinnyPlan& p, const void* x, const int*
                                   unsigned int* status, cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
                           const void* scales, bool has_zeros, void* y, int B, int K, int N,
-                          void* workspace, unsigned int* status, cudaStream_t stream);
+                          void* workspace, unsigned int* status, const Epilogue& epi,
+                          cudaStream_t stream);
 
 // ---- tcgen05 tensor-core kernel (tc_gemm.cu) ----
 struct TcPlan {
@@ -84,7 +94,7 @@ TcPlan plan_tc(int B, int K, int N, int num_sms);
 size_t tc_workspace_bytes(const TcPlan& p, int B, int N);
 cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
                       bool has_zeros, void* y, int B, int K, int N, void* workspace,
-                      unsigned int* status, cudaStream_t stream);
+                      unsigned int* status, const Epilogue& epi, cudaStream_t stream);
 cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void* packed,
                                      const void* scales, bool has_zeros, void* y, int B, int K,
                                      int N, void* workspace, unsigned int* status, int wait_ms,
@@ -95,7 +105,7 @@ TcPlan plan_tc_wide(int B, int K, int N, int num_sms);
 cudaError_t launch_tc_wide(const TcPlan& p, const void* x, const void* packed,
                            const void* scales, bool has_zeros, void* y, int B, int K, int N,
                            void* workspace, unsigned int* status, int force_timeout_ms,
-                           cudaStream_t stream);
+                           const Epilogue& epi, cudaStream_t stream);
 
 // ---- W8A8-FP8 comparison path (fp8.cu) ----
 struct Fp8Plan {

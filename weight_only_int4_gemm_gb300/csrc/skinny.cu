@@ -45,6 +45,7 @@
 #include <algorithm>
 
 #include "dequant.cuh"
+#include "epilogue.cuh"
 #include "launch.cuh"
 
 namespace w4a16 {
@@ -89,6 +90,7 @@ struct Args {
     const int* offsets;
     int E;
     size_t w_stride, s_stride;
+    Epilogue epi;        // fused output epilogue (plain bf16 when mode == 0)
 };
 
 constexpr int kMaxExperts = 256;
@@ -178,11 +180,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
-    __nv_bfloat16 h = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t*>(&h);
-}
-
 // Work unit u -> (batch chunk, tile, split index) and its extents.  bc counts
 // batch chunks over all experts (it indexes the split-K arrival counters);
 // b0 is the unit's first row of x and y; packed / scales / zeros point at the
@@ -194,7 +191,17 @@ struct Unit {
     const uint32_t* zeros;
 };
 
-template <int NT>
+// Four fp32 values -> four bf16 (RNE) at a 8-byte aligned address.
+__device__ __forceinline__ void store4_bf16(uint16_t* dst, float v0, float v1, float v2, float v3) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(epi_f32_to_bf16(v0) | (epi_f32_to_bf16(v1) << 16),
+                                                epi_f32_to_bf16(v2) | (epi_f32_to_bf16(v3) << 16));
+}
+
+// Kernel variants (compiled separately so the plain kernel carries no code
+// of the others): plain, grouped (mixture of experts), fused epilogue.
+constexpr int kPlain = 0, kGrouped = 1, kFusedEpi = 2;
+
+template <int NT, int kMode>
 __device__ __forceinline__ Unit decode_unit(const Args& a, const Tail* t, int u) {
     constexpr int kRows = 8 * NT;
     Unit w;
@@ -207,7 +214,7 @@ __device__ __forceinline__ Unit decode_unit(const Args& a, const Tail* t, int u)
     w.n0 = w.tile * kTileCols;
     w.width = packed_tile_width(a.N, w.tile);
     w.nsteps = (w.ng + kSlotGroups - 1) / kSlotGroups;
-    if (a.offsets == nullptr) {
+    if constexpr (kMode != kGrouped) {
         w.b0 = w.bc * kRows;
         w.rows = min(kRows, a.B - w.b0);
         w.packed = a.packed;
@@ -233,7 +240,7 @@ __device__ __forceinline__ Unit decode_unit(const Args& a, const Tail* t, int u)
 
 // ------------------------------------------------------------ kernel
 
-template <int NT, bool kHasZeros>
+template <int NT, bool kHasZeros, int kMode>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_t<NT>())
 skinny_kernel(const Args a) {
     constexpr int kRows = 8 * NT;
@@ -275,7 +282,7 @@ skinny_kernel(const Args a) {
         tail->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (a.offsets != nullptr) {
+    if constexpr (kMode == kGrouped) {
         // grouped: the routing table may be written by the previous kernel on
         // the stream, so wait for it before the first read
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -354,7 +361,7 @@ skinny_kernel(const Args a) {
         // The first unit is fixed (blockIdx.x): its first slots' code copies go
         // out before waiting for the previous kernel on the stream.
         const bool has_first = (int)blockIdx.x < total_units;
-        const Unit first = decode_unit<NT>(a, tail, has_first ? (int)blockIdx.x : 0);
+        const Unit first = decode_unit<NT, kMode>(a, tail, has_first ? (int)blockIdx.x : 0);
         const uint8_t* first_codes = first.packed + packed_tile_base(a.K, first.tile);
         auto issue_codes = [&](const Unit& w, const uint8_t* tile_codes, int st, int pos) {
             const int s = pos % S;
@@ -397,7 +404,7 @@ skinny_kernel(const Args a) {
                 }
                 break;
             }
-            const Unit w = decode_unit<NT>(a, tail, u);
+            const Unit w = decode_unit<NT, kMode>(a, tail, u);
             const uint8_t* tile_codes = w.packed + packed_tile_base(a.K, w.tile);
             for (int st = 0; st < w.nsteps; ++st, ++step) {
                 const int s = step % S;
@@ -491,7 +498,7 @@ skinny_kernel(const Args a) {
                 }
                 break;
             }
-            const Unit w = decode_unit<NT>(a, tail, u);
+            const Unit w = decode_unit<NT, kMode>(a, tail, u);
             if (st == 0) {
 #pragma unroll
                 for (int bt = 0; bt < NT; ++bt)
@@ -583,7 +590,7 @@ skinny_kernel(const Args a) {
             if (!warp_wait(smem_u32(&tail->res_full[buf]), (k >> 1) & 1, abort, a.status)) break;
             const int u = tail->res_unit[buf];
             if (u < 0) break;
-            const Unit w = decode_unit<NT>(a, tail, u);
+            const Unit w = decode_unit<NT, kMode>(a, tail, u);
             const float* r = res + buf * (result_bytes<NT>() / 4);
             const bool mine = c4 < w.width;
             // element (column c, row b) of the unit lives at
@@ -600,9 +607,10 @@ skinny_kernel(const Args a) {
                             v3 = elem(c4 + 3, b);
                 const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c4;
                 if (a.split == 1) {
-                    const uint32_t lo = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
-                    const uint32_t hi = (uint32_t)f32_to_bf16_rn(v2) | ((uint32_t)f32_to_bf16_rn(v3) << 16);
-                    *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                    if constexpr (kMode == kFusedEpi)
+                        epi_store4_fused(a.y, a.N, w.b0 + b, w.n0 + c4, v0, v1, v2, v3, a.epi);
+                    else
+                        store4_bf16(a.y + off, v0, v1, v2, v3);
                 } else {
                     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                                  ::"l"(a.partial + off), "f"(v0), "f"(v1), "f"(v2), "f"(v3)
@@ -637,11 +645,11 @@ skinny_kernel(const Args a) {
                         for (int j = 0; j < 8; ++j) {
                             if (b0 + j < w.rows) {
                                 const size_t off = (size_t)(w.b0 + b0 + j) * a.N + w.n0 + c4;
-                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[j].x) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[j].y) << 16);
-                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[j].z) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[j].w) << 16);
-                                *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                                if constexpr (kMode == kFusedEpi)
+                                    epi_store4_fused(a.y, a.N, w.b0 + b0 + j, w.n0 + c4, v[j].x,
+                                                     v[j].y, v[j].z, v[j].w, a.epi);
+                                else
+                                    store4_bf16(a.y + off, v[j].x, v[j].y, v[j].z, v[j].w);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
                             }
@@ -659,7 +667,10 @@ template <int NT, bool Z>
 cudaError_t launch_t(const SkinnyPlan& p, Args a, cudaStream_t stream) {
     const size_t smem = (size_t)ring_slots<NT>() * slot_bytes<NT>() + 2 * result_bytes<NT>() +
                         sizeof(Tail);
-    const void* kern = reinterpret_cast<const void*>(skinny_kernel<NT, Z>);
+    const void* kern =
+        a.offsets != nullptr ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kGrouped>)
+        : a.epi.mode != 0    ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kFusedEpi>)
+                             : reinterpret_cast<const void*>(skinny_kernel<NT, Z, kPlain>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
@@ -744,7 +755,8 @@ size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N) {
 static cudaError_t launch_skinny_impl(const SkinnyPlan& p, const void* x, const void* packed,
                                       const void* scales, bool has_zeros, void* y, int B, int K,
                                       int N, void* workspace, unsigned int* status,
-                                      const int* offsets, int E, cudaStream_t stream) {
+                                      const int* offsets, int E, const Epilogue& epi,
+                                      cudaStream_t stream) {
     Args a;
     a.x = static_cast<const uint16_t*>(x);
     a.packed = static_cast<const uint8_t*>(packed);
@@ -766,6 +778,7 @@ static cudaError_t launch_skinny_impl(const SkinnyPlan& p, const void* x, const 
     a.E = E;
     a.w_stride = packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);
     a.s_stride = (size_t)(K / kGroup) * N;
+    a.epi = epi;
     switch (p.nt * 2 + (has_zeros ? 1 : 0)) {
         case 2: return launch_t<1, false>(p, a, stream);
         case 3: return launch_t<1, true>(p, a, stream);
@@ -779,9 +792,10 @@ static cudaError_t launch_skinny_impl(const SkinnyPlan& p, const void* x, const 
 
 cudaError_t launch_skinny(const SkinnyPlan& p, const void* x, const void* packed,
                           const void* scales, bool has_zeros, void* y, int B, int K, int N,
-                          void* workspace, unsigned int* status, cudaStream_t stream) {
+                          void* workspace, unsigned int* status, const Epilogue& epi,
+                          cudaStream_t stream) {
     return launch_skinny_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
-                              nullptr, 0, stream);
+                              nullptr, 0, epi, stream);
 }
 
 cudaError_t launch_skinny_grouped(const SkinnyPlan& p, const void* x, const int* offsets, int E,
@@ -789,7 +803,7 @@ cudaError_t launch_skinny_grouped(const SkinnyPlan& p, const void* x, const int*
                                   void* y, int T, int K, int N, void* workspace,
                                   unsigned int* status, cudaStream_t stream) {
     return launch_skinny_impl(p, x, packed, scales, has_zeros, y, T, K, N, workspace, status,
-                              offsets, E, stream);
+                              offsets, E, Epilogue{}, stream);
 }
 
 }  // namespace w4a16

@@ -52,6 +52,7 @@
 #include <mutex>
 
 #include "dequant.cuh"
+#include "epilogue.cuh"
 #include "launch.cuh"
 
 namespace w4a16 {
@@ -106,6 +107,7 @@ struct Args {
     uint32_t scale_off, zero_off;  // offsets inside a code slot (codes at 0)
     int x3d;               // x of a stage is one 3-D box (else one 2-D box per block)
     int force_timeout;     // test hook: wait on a barrier nobody arrives at
+    Epilogue epi;          // fused output epilogue (plain bf16 when mode == 0)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -269,11 +271,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
-    __nv_bfloat16 h = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t*>(&h);
-}
-
 // ------------------------------------------------------------ kernel
 
 struct SharedTail {
@@ -367,7 +364,7 @@ __device__ __forceinline__ void issue_x_copies(const Args& a, const CUtensorMap*
     }
 }
 
-template <bool kHasZeros>
+template <bool kHasZeros, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
           const __grid_constant__ CUtensorMap zmap, const Args a) {
@@ -688,13 +685,21 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) v[jj] += __uint_as_float(r[jj]);
                     }
-                    if (nn < a.N) {
+                    if (kFused && a.split == 1) {
+                        // fused epilogue; b is the same in every lane (the
+                        // SiLU form pairs lanes)
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int b = t.b0 + c0 + jj;
+                            if (b < a.B) epi_store_lane_fused(a.y, a.N, b, nn, v[jj], nn < a.N, a.epi);
+                        }
+                    } else if (nn < a.N) {
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
                             const int b = t.b0 + c0 + jj;
                             if (b < a.B) {
                                 if (a.split == 1)
-                                    a.y[(size_t)b * a.N + nn] = f32_to_bf16_rn(v[jj]);
+                                    a.y[(size_t)b * a.N + nn] = (uint16_t)epi_f32_to_bf16(v[jj]);
                                 else
                                     asm volatile("red.global.add.f32 [%0], %1;"
                                                  ::"l"(a.partial + (size_t)b * a.N + nn), "f"(v[jj])
@@ -749,11 +754,12 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
                                 const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
-                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[jj].x) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[jj].y) << 16);
-                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[jj].z) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[jj].w) << 16);
-                                *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                                if constexpr (kFused)
+                                    epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x, v[jj].y,
+                                           v[jj].z, v[jj].w, a.epi);
+                                else
+                                    epi_store4_plain(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x, v[jj].y,
+                                           v[jj].z, v[jj].w, a.epi);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
                             }
@@ -921,10 +927,11 @@ size_t tc_workspace_bytes(const TcPlan& p, int B, int N) {
 static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* packed,
                                   const void* scales, bool has_zeros, void* y, int B, int K,
                                   int N, void* workspace, unsigned int* status,
-                                  int force_timeout_ms, cudaStream_t stream) {
+                                  int force_timeout_ms, const Epilogue& epi,
+                                  cudaStream_t stream) {
     if (p.wide)
         return launch_tc_wide(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
-                              force_timeout_ms, stream);
+                              force_timeout_ms, epi, stream);
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     const int ng = p.nsub > 1 ? p.nsub / 2 : 1;
@@ -1008,11 +1015,16 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     a.zero_off = lay.zero_off;
     a.x3d = x3d;
     a.force_timeout = force_timeout_ms;
+    a.epi = epi;
     if (a.a_slots < 4 || a.code_slots < 2 || a.x_slots < 2) return cudaErrorInvalidConfiguration;
 
     const size_t smem = lay.smem;
-    const void* kern = has_zeros ? reinterpret_cast<const void*>(tc_kernel<true>)
-                                 : reinterpret_cast<const void*>(tc_kernel<false>);
+    const bool fused = epi.mode != 0;
+    const void* kern =
+        has_zeros ? (fused ? reinterpret_cast<const void*>(tc_kernel<true, true>)
+                           : reinterpret_cast<const void*>(tc_kernel<true, false>))
+                  : (fused ? reinterpret_cast<const void*>(tc_kernel<false, true>)
+                           : reinterpret_cast<const void*>(tc_kernel<false, false>));
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -1023,9 +1035,9 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
 
 cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
                       bool has_zeros, void* y, int B, int K, int N, void* workspace,
-                      unsigned int* status, cudaStream_t stream) {
+                      unsigned int* status, const Epilogue& epi, cudaStream_t stream) {
     return launch_tc_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status, 0,
-                          stream);
+                          epi, stream);
 }
 
 cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void* packed,
@@ -1033,7 +1045,7 @@ cudaError_t launch_tc_forced_timeout(const TcPlan& p, const void* x, const void*
                                      int N, void* workspace, unsigned int* status, int wait_ms,
                                      cudaStream_t stream) {
     return launch_tc_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
-                          wait_ms, stream);
+                          wait_ms, Epilogue{}, stream);
 }
 
 }  // namespace w4a16

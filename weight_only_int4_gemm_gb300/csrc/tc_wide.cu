@@ -49,6 +49,7 @@
 #include <mutex>
 
 #include "dequant.cuh"
+#include "epilogue.cuh"
 #include "launch.cuh"
 
 namespace w4a16 {
@@ -87,6 +88,7 @@ struct Args {
     uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= max(32, bn))
     int raw_slots;      // depth of the codes + x ring
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
+    Epilogue epi;          // fused output epilogue (plain bf16 when mode == 0)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -228,11 +230,6 @@ __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
-    __nv_bfloat16 h = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t*>(&h);
-}
-
 // ------------------------------------------------------------ kernel
 
 struct SharedTail {
@@ -275,7 +272,7 @@ __device__ __forceinline__ void epilogue_bar() {  // the 4 epilogue warps only
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-template <bool kHasZeros>
+template <bool kHasZeros, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     extern __shared__ uint8_t smem_raw[];
@@ -493,13 +490,21 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
                     tmem_ld_16(taddr + c0, v);
-                    if (nn < a.N) {
+                    if (kFused && a.split == 1) {
+                        // fused epilogue; b is the same in every lane (the
+                        // SiLU form pairs lanes)
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int b = t.b0 + c0 + jj;
+                            if (b < a.B) epi_store_lane_fused(a.y, a.N, b, nn, v[jj], nn < a.N, a.epi);
+                        }
+                    } else if (nn < a.N) {
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
                             const int b = t.b0 + c0 + jj;
                             if (b < a.B) {
                                 if (a.split == 1)
-                                    a.y[(size_t)b * a.N + nn] = f32_to_bf16_rn(v[jj]);
+                                    a.y[(size_t)b * a.N + nn] = (uint16_t)epi_f32_to_bf16(v[jj]);
                                 else
                                     asm volatile("red.global.add.f32 [%0], %1;"
                                                  ::"l"(a.partial + (size_t)b * a.N + nn), "f"(v[jj])
@@ -554,11 +559,12 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
                                 const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
-                                const uint32_t lo = (uint32_t)f32_to_bf16_rn(v[j].x) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[j].y) << 16);
-                                const uint32_t hi = (uint32_t)f32_to_bf16_rn(v[j].z) |
-                                                    ((uint32_t)f32_to_bf16_rn(v[j].w) << 16);
-                                *reinterpret_cast<uint2*>(a.y + off) = make_uint2(lo, hi);
+                                if constexpr (kFused)
+                                    epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[j].x, v[j].y,
+                                           v[j].z, v[j].w, a.epi);
+                                else
+                                    epi_store4_plain(a.y, a.N, t.b0 + rr, t.n0 + cc, v[j].x, v[j].y,
+                                           v[j].z, v[j].w, a.epi);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
                             }
@@ -655,7 +661,8 @@ TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
 
 static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
                            bool has_zeros, void* y, int B, int K, int N, void* workspace,
-                           unsigned int* status, int force_timeout_ms, cudaStream_t stream) {
+                           unsigned int* status, int force_timeout_ms, const Epilogue& epi,
+                           cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     CUtensorMap xmap;
@@ -690,10 +697,15 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.acc_cols = acc_cols_for(p.bn);
     a.raw_slots = raw_slots_for(p.bn);
     a.force_timeout = force_timeout_ms;
+    a.epi = epi;
 
     const size_t smem = smem_bytes(p.bn);
-    const void* kern = has_zeros ? reinterpret_cast<const void*>(wide_kernel<true>)
-                                 : reinterpret_cast<const void*>(wide_kernel<false>);
+    const bool fused = epi.mode != 0;
+    const void* kern =
+        has_zeros ? (fused ? reinterpret_cast<const void*>(wide_kernel<true, true>)
+                           : reinterpret_cast<const void*>(wide_kernel<true, false>))
+                  : (fused ? reinterpret_cast<const void*>(wide_kernel<false, true>)
+                           : reinterpret_cast<const void*>(wide_kernel<false, false>));
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -705,9 +717,9 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
 cudaError_t launch_tc_wide(const TcPlan& p, const void* x, const void* packed,
                            const void* scales, bool has_zeros, void* y, int B, int K, int N,
                            void* workspace, unsigned int* status, int force_timeout_ms,
-                           cudaStream_t stream) {
+                           const Epilogue& epi, cudaStream_t stream) {
     return launch_wide_impl(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
-                            force_timeout_ms, stream);
+                            force_timeout_ms, epi, stream);
 }
 
 }  // namespace w4a16

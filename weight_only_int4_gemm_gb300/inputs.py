@@ -19,7 +19,8 @@ Recipe (shapes and value distributions of the workloads):
                 rows are grouped by expert, giving per-expert row offsets;
                 expert e's weights are drawn like one layer's, seed + e;
   * dense    -- bf16 weights W [K][N] for the quantisers and the FP8
-                comparison path: N(0, 1) * 0.02 rounded to bf16.
+                comparison path: N(0, 1) * 0.02 rounded to bf16;
+  * bias     -- bf16 [N]: N(0, 1) * 0.5 rounded to bf16.
 
 Draws use ``torch.Generator(device).manual_seed(seed)``; CPU and CUDA
 generators give different streams, so each comparison uses one generated copy
@@ -138,3 +139,10 @@ def make_dense_weight(K: int, N: int, seed: int, *, device="cpu") -> torch.Tenso
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     return (torch.randn((K, N), generator=gen, device=device) * 0.02).to(torch.bfloat16)
+
+
+def make_bias(N: int, seed: int, *, device="cpu") -> torch.Tensor:
+    """bf16 bias [N], N(0, 1) * 0.5."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return (torch.randn(N, generator=gen, device=device) * 0.5).to(torch.bfloat16)
