@@ -93,7 +93,8 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"skinny": ["skinny.cu", "dequant.cuh"], "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "dequant.cuh"]}
+KERNEL_FILES = {"skinny": ["skinny.cu", "dequant.cuh", "epilogue.cuh"],
+                "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "dequant.cuh", "epilogue.cuh"]}
 
 
 def traffic_from_profiles(kernel: str, workload_name: str):
@@ -729,7 +730,9 @@ def run_fp8(args):
         fp8_w[lbl], w4_w[lbl], bf_w[lbl] = [], [], []
         for c in range(n_copies):
             wt = inputs.make_dense_weight(K, N, seed=K + N + 7919 * c, device=device)
-            fp8_w[lbl].append(w.w8a8_fp8_quantize_weight(wt))
+            wq, sw = w.w8a8_fp8_quantize_weight(wt)
+            fp8_w[lbl].append((w.w8a8_fp8_pack_weight(wq), sw))
+            del wq
             qw, sc, _ = inputs.make_weights(K, N, seed=K * 3 + N + 7919 * c, device=device)
             w4_w[lbl].append((w.w4a16_pack(qw), sc))
             bf_w[lbl].append(wt)

@@ -44,14 +44,26 @@ w4a16_status w8a8_fp8_quantize_act(const void *x, int B, int K, void *xq, float 
 w4a16_status w8a8_fp8_quantize_weight(const void *w, int K, int N, void *wq, float *sw,
                                       void *stream);
 
+/* Bytes of the GEMM's weight layout: ceil(N/128) * 128 * K. */
+size_t w8a8_fp8_packed_bytes(int K, int N);
+
+/* Reorder the [N][K] codes into the GEMM's layout: tiles of 128 channels x
+ * 128 k, each one contiguous 16 KB block holding the shared-memory image the
+ * MMA reads (128-byte rows, 128-byte swizzle), tile t / k block kb at block
+ * t * (K/128) + kb, channels past N zero.  A pure byte permutation.
+ *   wq      device uint8 [N][K] (from w8a8_fp8_quantize_weight)   (read)
+ *   packed  device, w8a8_fp8_packed_bytes(K, N) bytes             (written) */
+w4a16_status w8a8_fp8_pack_weight(const void *wq, int K, int N, void *packed, void *stream);
+
 /* Workspace bytes w8a8_fp8_gemm needs for this shape (0: none; SIZE_MAX for an
  * invalid shape).  Same contract as w4a16_gemm's: zero-filled once by the
  * caller, left zero by every call, shareable with the W4A16 calls. */
 size_t w8a8_fp8_workspace_bytes(int B, int K, int N);
 
 /* y[b][n] = bf16( sum_k dec(xq[b][k]) * dec(wq[n][k]) * sx[b] * sw[n] ), fp32
- * accumulation on the tensor cores (tcgen05.mma kind::f8f6f4), bf16 y [B][N]. */
-w4a16_status w8a8_fp8_gemm(const void *xq, const float *sx, const void *wq, const float *sw,
+ * accumulation on the tensor cores (tcgen05.mma kind::f8f6f4), bf16 y [B][N];
+ * the weight codes are read from `packed` (w8a8_fp8_pack_weight). */
+w4a16_status w8a8_fp8_gemm(const void *xq, const float *sx, const void *packed, const float *sw,
                            void *y, int B, int K, int N, void *workspace, size_t ws_bytes,
                            void *stream);
 

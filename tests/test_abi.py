@@ -168,6 +168,12 @@ def test_fp8_validation(lib):
     assert lib.w8a8_fp8_quantize_weight(FAKE, 128, 8, None, FAKE, None) == ERR_NULL
     assert lib.w8a8_fp8_quantize_weight(FAKE + 4, 128, 8, FAKE, FAKE, None) == ERR_ALIGN
 
+    assert lib.w8a8_fp8_packed_bytes(256, 264) == 3 * 128 * 256
+    assert lib.w8a8_fp8_packed_bytes(100, 8) == 0
+    assert lib.w8a8_fp8_pack_weight(FAKE, 128, 12, FAKE, None) == ERR_SHAPE
+    assert lib.w8a8_fp8_pack_weight(None, 128, 8, FAKE, None) == ERR_NULL
+    assert lib.w8a8_fp8_pack_weight(FAKE, 128, 8, FAKE + 8, None) == ERR_ALIGN
+
     def gemm(xq=FAKE, sx=FAKE, wq=FAKE, sw=FAKE, y=FAKE, B=1, K=4096, N=4096, ws=FAKE,
              ws_bytes=None):
         if ws_bytes is None:

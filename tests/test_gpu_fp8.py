@@ -51,8 +51,9 @@ def test_weight_quantizer_bit_exact(K, N):
 
 
 def check_gemm(xq, sx, wq, sw, cols=None, exact=False):
+    packed = w.w8a8_fp8_pack_weight(torch.from_numpy(np.ascontiguousarray(wq)).cuda())
     y = w.w8a8_fp8_gemm(torch.from_numpy(xq).cuda(), torch.from_numpy(sx).cuda(),
-                        torch.from_numpy(wq).cuda(), torch.from_numpy(sw).cuda())
+                        packed, torch.from_numpy(sw).cuda())
     torch.cuda.synchronize()
     assert w.w4a16_device_status() == 0
     yo, _, bound = oracle.fp8_gemm(xq, sx, wq, sw, cols=cols)
@@ -94,6 +95,24 @@ def test_gemm_bit_exact_on_integer_codes(B, K, N):
     check_gemm(xq, sx, wq, sw, exact=True)  # the split-K workspace is clean again
 
 
+@pytest.mark.parametrize("K,N", [(128, 8), (1024, 264), (256, 1000)])
+def test_pack_layout(K, N):
+    """The packed weight blocks hold exactly the codes, tiled and swizzled:
+    checked by rebuilding the blocks on the host from the layout's definition."""
+    rng = np.random.default_rng(K + N)
+    wq = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    got = w.w8a8_fp8_pack_weight(torch.from_numpy(wq).cuda()).cpu().numpy()
+    tiles, nkb = -(-N // 128), K // 128
+    want = np.zeros((tiles, nkb, 128, 8, 16), dtype=np.uint8)
+    pad = np.zeros((tiles * 128, K), dtype=np.uint8)
+    pad[:N] = wq
+    src = pad.reshape(tiles, 128, nkb, 8, 16).transpose(0, 2, 1, 3, 4)  # [t][kb][r][c][16]
+    for c in range(8):
+        for r in range(128):
+            want[:, :, r, c ^ (r & 7)] = src[:, :, r, c]
+    assert np.array_equal(got, want.reshape(-1))
+
+
 def test_pipeline_on_the_gpu():
     """Both quantisers and the GEMM on the device, the oracle's chain beside it."""
     B, K, N = 24, 4096, 4096
@@ -101,7 +120,7 @@ def test_pipeline_on_the_gpu():
     wt = inputs.make_dense_weight(K, N, 22)
     xq, sx = w.w8a8_fp8_quantize_act(x.cuda())
     wq, sw = w.w8a8_fp8_quantize_weight(wt.cuda())
-    y = w.w8a8_fp8_gemm(xq, sx, wq, sw)
+    y = w.w8a8_fp8_gemm(xq, sx, w.w8a8_fp8_pack_weight(wq), sw)
     torch.cuda.synchronize()
     assert w.w4a16_device_status() == 0
     oxq, osx = oracle.fp8_quantize_rows(bits(x))

@@ -47,6 +47,8 @@ SIGNATURES = {
     # include/w8a8_fp8.h
     "w8a8_fp8_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
     "w8a8_fp8_quantize_weight": (_I, [_P, _I, _I, _P, _P, _P]),
+    "w8a8_fp8_packed_bytes": (_S, [_I, _I]),
+    "w8a8_fp8_pack_weight": (_I, [_P, _I, _I, _P, _P]),
     "w8a8_fp8_workspace_bytes": (_S, [_I, _I, _I]),
     "w8a8_fp8_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _S, _P]),
 }
@@ -328,6 +330,20 @@ def w8a8_fp8_quantize_weight(w: torch.Tensor, *, stream=None) -> tuple[torch.Ten
     return wq, sw
 
 
+def w8a8_fp8_packed_bytes(K: int, N: int) -> int:
+    return int(load().w8a8_fp8_packed_bytes(K, N))
+
+
+def w8a8_fp8_pack_weight(wq: torch.Tensor, *, stream=None) -> torch.Tensor:
+    """[N][K] E4M3 codes -> the GEMM's tiled, pre-swizzled weight layout (uint8)."""
+    N, K = wq.shape
+    _need(wq, torch.uint8, (N, K), "wq")
+    packed = torch.empty(w8a8_fp8_packed_bytes(K, N), dtype=torch.uint8, device=wq.device)
+    _check("w8a8_fp8_pack_weight", load().w8a8_fp8_pack_weight(
+        wq.data_ptr(), K, N, packed.data_ptr(), _stream(stream)))
+    return packed
+
+
 def w8a8_fp8_workspace_bytes(B: int, K: int, N: int) -> int:
     v = int(load().w8a8_fp8_workspace_bytes(B, K, N))
     if v == ctypes.c_size_t(-1).value:
@@ -335,14 +351,15 @@ def w8a8_fp8_workspace_bytes(B: int, K: int, N: int) -> int:
     return v
 
 
-def w8a8_fp8_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor, *,
+def w8a8_fp8_gemm(xq: torch.Tensor, sx: torch.Tensor, packed: torch.Tensor, sw: torch.Tensor, *,
                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                   stream=None) -> torch.Tensor:
-    """y[B][N] = (sx * dec(xq)) . (sw * dec(wq))^T, bf16."""
+    """y[B][N] = (sx * dec(xq)) . (sw * dec(wq))^T, bf16; `packed` from
+    w8a8_fp8_pack_weight(wq)."""
     B, K = xq.shape
-    N = wq.shape[0]
+    N = sw.shape[0]
     _need(xq, torch.uint8, (B, K), "xq")
-    _need(wq, torch.uint8, (N, K), "wq")
+    _need(packed, torch.uint8, (w8a8_fp8_packed_bytes(K, N),), "packed")
     _need(sx, torch.float32, (B,), "sx")
     _need(sw, torch.float32, (N,), "sw")
     if out is None:
@@ -354,6 +371,6 @@ def w8a8_fp8_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torc
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("w8a8_fp8_gemm", load().w8a8_fp8_gemm(
-        xq.data_ptr(), sx.data_ptr(), wq.data_ptr(), sw.data_ptr(), out.data_ptr(), B, K, N,
+        xq.data_ptr(), sx.data_ptr(), packed.data_ptr(), sw.data_ptr(), out.data_ptr(), B, K, N,
         ws_ptr, ws_bytes, _stream(stream)))
     return out

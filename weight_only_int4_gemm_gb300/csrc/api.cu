@@ -268,17 +268,28 @@ w4a16_status w8a8_fp8_quantize_weight(const void* w, int K, int N, void* wq, flo
     return from_cuda(launch_fp8_quantize_cols(w, K, N, wq, sw, static_cast<cudaStream_t>(stream)));
 }
 
+size_t w8a8_fp8_packed_bytes(int K, int N) {
+    return shape_ok(K, N) ? fp8_packed_bytes(K, N) : 0;
+}
+
+w4a16_status w8a8_fp8_pack_weight(const void* wq, int K, int N, void* packed, void* stream) {
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (!wq || !packed) return W4A16_ERR_NULL;
+    if (!aligned16(wq) || !aligned16(packed)) return W4A16_ERR_ALIGN;
+    return from_cuda(launch_fp8_pack(wq, K, N, packed, static_cast<cudaStream_t>(stream)));
+}
+
 size_t w8a8_fp8_workspace_bytes(int B, int K, int N) {
     if (!shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
     return fp8_workspace_bytes(plan_fp8(B, K, N, num_sms()), B, N);
 }
 
-w4a16_status w8a8_fp8_gemm(const void* xq, const float* sx, const void* wq, const float* sw,
+w4a16_status w8a8_fp8_gemm(const void* xq, const float* sx, const void* packed, const float* sw,
                            void* y, int B, int K, int N, void* workspace, size_t ws_bytes,
                            void* stream) {
     if (!shape_ok(K, N) || B < 1 || B > kMaxB) return W4A16_ERR_SHAPE;
-    if (!xq || !sx || !wq || !sw || !y) return W4A16_ERR_NULL;
-    if (!aligned16(xq) || !aligned16(wq) || !aligned16(y) ||
+    if (!xq || !sx || !packed || !sw || !y) return W4A16_ERR_NULL;
+    if (!aligned16(xq) || !aligned16(packed) || !aligned16(y) ||
         ((reinterpret_cast<uintptr_t>(sx) | reinterpret_cast<uintptr_t>(sw)) & 3u) != 0)
         return W4A16_ERR_ALIGN;
     const Fp8Plan p = plan_fp8(B, K, N, num_sms());
@@ -291,7 +302,7 @@ w4a16_status w8a8_fp8_gemm(const void* xq, const float* sx, const void* wq, cons
     if (!tc_available()) return W4A16_ERR_UNSUPPORTED;
     unsigned int* status = device_status_word();
     if (status == nullptr) return W4A16_ERR_CUDA;
-    return from_cuda(launch_fp8_gemm(p, xq, sx, wq, sw, y, B, K, N, workspace, status,
+    return from_cuda(launch_fp8_gemm(p, xq, sx, packed, sw, y, B, K, N, workspace, status,
                                      static_cast<cudaStream_t>(stream)));
 }
 

@@ -15,14 +15,23 @@
 // divisions, rounded once to E4M3 by the hardware conversion (nearest, ties
 // to even, saturating); an all-zero row has scale 0 and codes 0.
 //
+// Weight layout for the GEMM (w8a8_fp8_pack_weight): the [N][K] codes are cut
+// into tiles of 128 output channels x 128 k, each stored as one contiguous
+// 16 KB block that is already the shared-memory image the MMA reads (rows of
+// 128 bytes, 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7));
+// tile t, k block kb sits at block t * (K / 128) + kb; channels past N are
+// zero.  One bulk copy per stage then streams the weights: reading the [N][K]
+// matrix as 2-D boxes of 128 rows x 128 bytes, K bytes apart, reached only
+// about half the HBM bandwidth.
+//
 // GEMM tile (operands swapped so the weight tile is the 128-row MMA operand):
 //   D[128 weight columns][bn batch rows] (fp32, TMEM)
-//     += Wq[128 columns][128 k] (E4M3, smem, TMA)  .  Xq[bn rows][128 k]^T
+//     += Wq[128 columns][128 k] (E4M3, smem, bulk copy) . Xq[bn rows][128 k]^T (TMA)
 // Both operand tiles are 128 bytes per row, so they use the same K-major
 // 128-byte-swizzled layout as the bf16 kernels' 64-element blocks; one stage
 // is four tcgen05.mma kind::f8f6f4 (K = 32 each).  Persistent CTAs take work
 // items (column tile, batch tile, K split) round robin.  Warp roles:
-//   warp 0     : TMA thread (weight tile + activation tile per stage, one
+//   warp 0     : copy thread (weight block + activation tile per stage, one
 //                mbarrier with the expected byte count);
 //   warp 1     : TMEM allocator + the MMA-issuing thread (commit per stage to
 //                "empty", per item to the accumulator's "full");
@@ -136,6 +145,25 @@ fp8_quant_cols_kernel(const uint16_t* __restrict__ w, int K, int N, const float*
                    p[6] | (p[7] << 16));
 }
 
+constexpr int kPackThreads = 256;
+
+// [N][K] codes -> tiled, pre-swizzled blocks (one thread per 16-byte chunk).
+__global__ void __launch_bounds__(kPackThreads)
+fp8_pack_kernel(const uint8_t* __restrict__ wq, int K, int N, uint8_t* __restrict__ packed,
+                long long chunks) {
+    const long long i = (long long)blockIdx.x * kPackThreads + threadIdx.x;
+    if (i >= chunks) return;
+    const int c = (int)(i & 7);               // 16-byte chunk of the 128-byte row
+    const int r = (int)((i >> 3) & 127);      // channel inside the tile
+    const long long blk = i >> 10;            // (tile, k block)
+    const int nkb = K / 128;
+    const int t = (int)(blk / nkb), kb = (int)(blk % nkb);
+    const int n = t * 128 + r;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) v = *reinterpret_cast<const uint4*>(wq + (size_t)n * K + (size_t)kb * 128 + 16 * c);
+    *reinterpret_cast<uint4*>(packed + (size_t)blk * 16384 + r * 128 + ((c ^ (r & 7)) * 16)) = v;
+}
+
 // ------------------------------------------------------------ GEMM
 
 constexpr int kBlockK = 128;                          // k per stage (bytes per operand row)
@@ -148,6 +176,7 @@ constexpr size_t kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 struct Args {
+    const uint8_t* wpacked;  // tiled weight blocks (fp8_pack_kernel)
     const float* sx;
     const float* sw;
     uint16_t* y;
@@ -198,8 +227,7 @@ __device__ __forceinline__ void epilogue_bar() {  // the 4 epilogue warps only
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-fp8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                const Args a) {
+fp8_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const int S = a.stages;
@@ -209,6 +237,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant_
     const int lane = threadIdx.x & 31;
     volatile int* abort = &tail->abort;
     auto w_tile = [&](int s) { return smem + s * sbytes; };
+    auto w_block = [&](const Item& t, int kb) {
+        return a.wpacked + ((size_t)t.col_tile * a.nkb + kb) * kWTileBytes;
+    };
     auto x_tile = [&](int s) { return smem + s * sbytes + kWTileBytes; };
 
     if (threadIdx.x == 0) {
@@ -222,7 +253,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant_
         }
         tail->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
     }
     if (warp == 1) {
@@ -251,7 +281,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant_
             for (int i = 0; i < pre; ++i) {
                 const uint32_t bar = smem_u32(&tail->full[i]);
                 mbar_arrive_expect_tx(bar, kWTileBytes + xbytes);
-                tma_load_2d(smem_u32(w_tile(i)), &wmap, (first.kb_begin + i) * kBlockK, first.n0, bar);
+                bulk_g2s(smem_u32(w_tile(i)), w_block(first, first.kb_begin + i), kWTileBytes, bar);
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             int stage = 0, issued = 0;
@@ -270,7 +300,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant_
                             break;
                         }
                         mbar_arrive_expect_tx(bar, kWTileBytes + xbytes);
-                        tma_load_2d(smem_u32(w_tile(s)), &wmap, kb * kBlockK, t.n0, bar);
+                        bulk_g2s(smem_u32(w_tile(s)), w_block(t, kb), kWTileBytes, bar);
                     }
                     tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, t.b0, bar);
                     issued = stage + 1;
@@ -477,9 +507,11 @@ Fp8Plan plan_fp8(int B, int K, int N, int num_sms) {
     p.col_tiles = (N + kTileN - 1) / kTileN;
     const int nkb = K / kBlockK;
     const long long tiles = (long long)p.col_tiles * p.batch_tiles;
-    // persistent CTAs (one per SM) take items round robin: choose the K split
-    // minimising the busiest CTA's stages plus a fixed cost per item and a
-    // small cost per split (accumulator traffic)
+    // persistent CTAs (one per SM) take items round robin.  One SM streams
+    // only a share of the HBM bandwidth, so the step time follows the busiest
+    // CTA's stages (plus a fixed cost per item and, with a K split, the fp32
+    // reduction of a bn x 128 tile: bn / 32 stage-equivalents), scaled up
+    // when fewer items than SMs leave SMs idle
     double best = 1e300;
     int best_split = 1, best_kbps = nkb;
     for (int split = 1; split <= std::min(32, nkb); ++split) {
@@ -488,7 +520,9 @@ Fp8Plan plan_fp8(int B, int K, int N, int num_sms) {
         const int s = (nkb + kbps - 1) / kbps;
         const long long items = tiles * s;
         const long long per_cta = (items + num_sms - 1) / num_sms;
-        const double cost = (double)per_cta * (kbps + 2) * (1.0 + 0.02 * (s - 1));
+        const double idle = items < num_sms ? (double)num_sms / (double)items : 1.0;
+        const double cost =
+            (double)per_cta * (kbps + 2 + (s > 1 ? p.bn / 32.0 : 0.0)) * idle;
         if (cost < best - 1e-9) {
             best = cost;
             best_split = s;
@@ -521,16 +555,27 @@ cudaError_t launch_fp8_quantize_cols(const void* w, int K, int N, void* wq, floa
     return cudaGetLastError();
 }
 
-cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx, const void* wq,
-                            const float* sw, void* y, int B, int K, int N, void* workspace,
-                            unsigned int* status, cudaStream_t stream) {
+size_t fp8_packed_bytes(int K, int N) {
+    return (size_t)((N + kTileN - 1) / kTileN) * kTileN * (size_t)K;
+}
+
+cudaError_t launch_fp8_pack(const void* wq, int K, int N, void* packed, cudaStream_t stream) {
+    const long long chunks = (long long)fp8_packed_bytes(K, N) / 16;
+    const long long blocks = (chunks + kPackThreads - 1) / kPackThreads;
+    fp8_pack_kernel<<<(unsigned)blocks, kPackThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(wq), K, N, static_cast<uint8_t*>(packed), chunks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx,
+                            const void* wpacked, const float* sw, void* y, int B, int K, int N,
+                            void* workspace, unsigned int* status, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    CUtensorMap wmap, xmap;
-    if (!encode_operand(enc, &wmap, wq, K, N, kTileN) ||
-        !encode_operand(enc, &xmap, xq, K, B, p.bn))
-        return cudaErrorInvalidValue;
+    CUtensorMap xmap;
+    if (!encode_operand(enc, &xmap, xq, K, B, p.bn)) return cudaErrorInvalidValue;
     Args a;
+    a.wpacked = static_cast<const uint8_t*>(wpacked);
     a.sx = sx;
     a.sw = sw;
     a.y = static_cast<uint16_t*>(y);
@@ -554,7 +599,7 @@ cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx, c
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    void* args[] = {&wmap, &xmap, &a};
+    void* args[] = {&xmap, &a};
     return launch_with_pdl(kern, dim3(std::min(a.items, p.grid)), dim3(kThreads), smem, stream,
                            args);
 }

@@ -122,9 +122,11 @@ cudaError_t launch_fp8_quantize_rows(const void* x, int B, int K, void* xq, floa
                                      cudaStream_t stream);
 cudaError_t launch_fp8_quantize_cols(const void* w, int K, int N, void* wq, float* sw,
                                      cudaStream_t stream);
-cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx, const void* wq,
-                            const float* sw, void* y, int B, int K, int N, void* workspace,
-                            unsigned int* status, cudaStream_t stream);
+size_t fp8_packed_bytes(int K, int N);
+cudaError_t launch_fp8_pack(const void* wq, int K, int N, void* packed, cudaStream_t stream);
+cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx,
+                            const void* wpacked, const float* sw, void* y, int B, int K, int N,
+                            void* workspace, unsigned int* status, cudaStream_t stream);
 
 // Validation + dispatch + launch shared by the C entry points (api.cu).
 // Returns a w4a16_status value.
