@@ -779,6 +779,12 @@ def run_fp8(args):
                 wq, sw = fp8_w[lbl][c]
                 w.w8a8_fp8_gemm(q, sxb, wq, sw, out=ys[lbl], workspace=ws, stream=stream)
 
+        def fp8_gemm_step(c):  # activations already quantised: the GEMMs alone
+            for lbl, K, N in LAYER:
+                wq, sw = fp8_w[lbl][c]
+                w.w8a8_fp8_gemm(xq[lbl][0], xq[lbl][1], wq, sw, out=ys[lbl], workspace=ws,
+                                stream=stream)
+
         def w4_step(c):
             for lbl, K, N in LAYER:
                 packed, sc = w4_w[lbl][c]
@@ -793,6 +799,7 @@ def run_fp8(args):
         with ClockSampler(0) as clk:
             t_fp8 = time_graphs(fp8_step, steps)
         assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
+        t_fp8_gemm = time_graphs(fp8_gemm_step, steps)
         t_w4 = time_graphs(w4_step, steps)
         t_bf = time_graphs(bf16_step, steps)
         wbytes = sum(K * N + 4 * N for _, K, N in LAYER)
@@ -821,6 +828,7 @@ def run_fp8(args):
                            "gemms": [f"{lbl} {K}x{N}" for lbl, K, N in LAYER],
                            "l2": f"weights rotated over {n_copies} copies", "cuda_graph": True},
                 "compare": {"w4a16_us": t_w4, "bf16_cublas_us": t_bf,
+                            "fp8_gemms_only_us": t_fp8_gemm,
                             "fp8_over_w4a16": t_fp8 / t_w4, "fp8_over_bf16": t_fp8 / t_bf},
                 "tflops": flops / t / 1e12, "roofline": roof, "clocks": clk.summary(),
                 "gpu_launches": steps * 2 * len(LAYER)}
