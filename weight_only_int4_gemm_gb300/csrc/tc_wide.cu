@@ -51,9 +51,12 @@
 #include "dequant.cuh"
 #include "epilogue.cuh"
 #include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace w4a16 {
 namespace {
+
+using namespace ptx;
 
 constexpr int kBlockK = 64;                  // K rows per pipeline stage
 constexpr int kTileN = 128;                  // weight columns per tile (MMA M)
@@ -69,7 +72,6 @@ constexpr int kThreads = 32 * kNumWarps;     // 704
 constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
 constexpr uint32_t kRawBytes = kTileN * kBlockK / 2;     // 4 KB of packed codes
 constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
-constexpr unsigned int kStatusTimeout = 7;               // W4A16_ERR_TIMEOUT
 
 struct Args {
     const uint8_t* packed;
@@ -90,145 +92,6 @@ struct Args {
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
     Epilogue epi;          // fused output epilogue (plain bf16 when mode == 0)
 };
-
-// ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: true when the phase with this parity completed; false when the
-// CTA is aborting (another wait expired) or this wait expired (then it sets
-// the abort flag and the device status word).
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status, unsigned long long limit_ns) {
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer() - t0 > limit_ns) {
-            *abort = 1;
-            atomicExch(status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-// Inline fast path: one try_wait, the bounded loop only if the phase is not
-// complete yet.
-__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_bounded(bar, parity, abort, status, limit_ns);
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart; start address in 16-byte units.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3FFFu);       // start address
-    d |= (uint64_t)1 << 16;                        // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset
-    d |= (uint64_t)1 << 46;                        // descriptor version
-    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// M = 128, N = n.
-__device__ __forceinline__ uint32_t instr_desc_bf16(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(kTileN >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // ------------------------------------------------------------ kernel
 
@@ -383,7 +246,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = instr_desc_bf16(a.bn);
+            const uint32_t idesc = instr_desc_bf16(kTileN, a.bn);
             bool ok = true;
             if (a.force_timeout)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
