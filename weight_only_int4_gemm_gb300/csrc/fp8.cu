@@ -88,6 +88,10 @@ fp8_quant_rows_kernel(const uint16_t* __restrict__ x, int K, uint8_t* __restrict
     const int b = blockIdx.x;
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)b * K);
     const int nv = K / 8;
+    // launched with programmatic dependent launch: x comes from the previous
+    // kernel, and the GEMM that follows may start its weight copies early
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float m = 0.0f;
     for (int i = threadIdx.x; i < nv; i += kRowThreads) {
         const uint4 v = __ldg(row + i);
@@ -541,9 +545,11 @@ size_t fp8_workspace_bytes(const Fp8Plan& p, int B, int N) {
 
 cudaError_t launch_fp8_quantize_rows(const void* x, int B, int K, void* xq, float* sx,
                                      cudaStream_t stream) {
-    fp8_quant_rows_kernel<<<B, kRowThreads, 0, stream>>>(static_cast<const uint16_t*>(x), K,
-                                                         static_cast<uint8_t*>(xq), sx);
-    return cudaGetLastError();
+    const uint16_t* xp = static_cast<const uint16_t*>(x);
+    uint8_t* xqp = static_cast<uint8_t*>(xq);
+    void* args[] = {&xp, &K, &xqp, &sx};
+    return launch_with_pdl(reinterpret_cast<const void*>(fp8_quant_rows_kernel), dim3(B),
+                           dim3(kRowThreads), 0, stream, args);
 }
 
 cudaError_t launch_fp8_quantize_cols(const void* w, int K, int N, void* wq, float* sw,
