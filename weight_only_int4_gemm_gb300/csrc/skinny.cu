@@ -105,6 +105,7 @@ struct Tail {
     uint64_t res_empty[2];
     int slot_unit[8];    // unit of each ring slot (-1: no more work)
     int slot_step[8];    // step of the unit held by the slot
+    int slot_meta[8];    // what the consumers need of it (slot_meta_pack)
     int res_unit[2];
     int abort;
     int total_units;                     // units of this call
@@ -198,6 +199,13 @@ struct Unit {
 __device__ __forceinline__ void store4_bf16(uint16_t* dst, float v0, float v1, float v2, float v3) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(epi_f32_to_bf16(v0) | (epi_f32_to_bf16(v1) << 16),
                                                 epi_f32_to_bf16(v2) | (epi_f32_to_bf16(v3) << 16));
+}
+
+// A slot's unit as the consumers see it, decoded once by the producer (the
+// unit decode's integer divisions would otherwise run in every consumer warp
+// at every step): tile width, groups in the slot, batch rows, last step.
+__device__ __forceinline__ int slot_meta_pack(int width, int ngs, int rows, bool last) {
+    return width | (ngs << 8) | (rows << 12) | ((last ? 1 : 0) << 20);
 }
 
 // Kernel variants (compiled separately so the plain kernel carries no code
@@ -387,6 +395,9 @@ skinny_kernel(const Args a) {
             for (int st = 0; st < pre; ++st) {
                 tail->slot_unit[st] = blockIdx.x;
                 tail->slot_step[st] = st;
+                tail->slot_meta[st] = slot_meta_pack(
+                    first.width, min(kSlotGroups, first.ng - st * kSlotGroups), first.rows,
+                    st == first.nsteps - 1);
                 issue_codes(first, first_codes, st, st);
             }
         }
@@ -421,6 +432,9 @@ skinny_kernel(const Args a) {
                     if (lane == 0) {
                         tail->slot_unit[s] = u;
                         tail->slot_step[s] = st;
+                        tail->slot_meta[s] = slot_meta_pack(
+                            w.width, min(kSlotGroups, w.ng - st * kSlotGroups), w.rows,
+                            st == w.nsteps - 1);
                         issue_codes(w, tile_codes, st, step);
                     }
                     w_issued = step + 1;
@@ -501,25 +515,26 @@ skinny_kernel(const Args a) {
                 }
                 break;
             }
-            const Unit w = decode_unit<NT, kMode>(a, tail, u);
+            const int meta = tail->slot_meta[s];
+            const int width = meta & 0xFF, ngs = (meta >> 8) & 0xF, rows = (meta >> 12) & 0xFF;
+            const bool last = (meta >> 20) & 1;
             if (st == 0) {
 #pragma unroll
                 for (int bt = 0; bt < NT; ++bt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[bt][i] = 0.f;
             }
-            const int ngs = min(kSlotGroups, w.ng - st * kSlotGroups);
             const uint4* codes = reinterpret_cast<const uint4*>(slot_codes(s));
             const uint4* xs = slot_x(s);
             const uint16_t* sc = slot_scales(s);
             const uint32_t* zs = slot_zeros(s);
-            const int cla = min(ca, w.width - 1), clb = min(cb, w.width - 1);
+            const int cla = min(ca, width - 1), clb = min(cb, width - 1);
             const uint4* xq = xs + gid * 4 + tig;  // this lane's fragment column
 #pragma unroll
             for (int gl = 0; gl < kSlotGroups; ++gl) {
                 if (gl < ngs) {
-                    const uint4 qa = codes[(4 * gl + tig) * w.width + cla];
-                    const uint4 qb = codes[(4 * gl + tig) * w.width + clb];
+                    const uint4 qa = codes[(4 * gl + tig) * width + cla];
+                    const uint4 qb = codes[(4 * gl + tig) * width + clb];
                     const float sa = __uint_as_float((uint32_t)sc[gl * kTileCols + cla] << 16);
                     const float sb = __uint_as_float((uint32_t)sc[gl * kTileCols + clb] << 16);
                     uint32_t za = kSymmetricZeroPair, zb = kSymmetricZeroPair;
@@ -549,7 +564,7 @@ skinny_kernel(const Args a) {
                             const uint32_t a3 = code_pair(wB[j], 2 * h + 1, zb);
 #pragma unroll
                             for (int bt = 0; bt < NT; ++bt)
-                                if (bt * 8 < w.rows)  // warp-uniform: skip padding tiles
+                                if (bt * 8 < rows)  // warp-uniform: skip padding tiles
                                     mma_bf16(t[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
                                              h ? xf[bt].w : xf[bt].y);
                         }
@@ -566,7 +581,7 @@ skinny_kernel(const Args a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tail->empty[s]));
 
-            if (st == w.nsteps - 1) {
+            if (last) {
                 // unit finished: hand the accumulators to the epilogue warp
                 if (nunit >= 2 && !warp_wait(smem_u32(&tail->res_empty[buf]), ((nunit >> 1) - 1) & 1,
                                              abort, a.status))
