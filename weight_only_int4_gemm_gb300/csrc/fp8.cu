@@ -280,12 +280,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // ---------------- TMA producer
         if (lane == 0) {
             const uint32_t xbytes = (uint32_t)a.bn * kBlockK;
+            const uint64_t evict_first = l2_evict_first_policy();  // weights are read once
             const Item first = decode_item(a, blockIdx.x);
             const int pre = min(S, first.nkb);
             for (int i = 0; i < pre; ++i) {
                 const uint32_t bar = smem_u32(&tail->full[i]);
                 mbar_arrive_expect_tx(bar, kWTileBytes + xbytes);
-                bulk_g2s(smem_u32(w_tile(i)), w_block(first, first.kb_begin + i), kWTileBytes, bar);
+                bulk_g2s_hint(smem_u32(w_tile(i)), w_block(first, first.kb_begin + i), kWTileBytes,
+                              bar, evict_first);
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             int stage = 0, issued = 0;
@@ -304,7 +306,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                             break;
                         }
                         mbar_arrive_expect_tx(bar, kWTileBytes + xbytes);
-                        bulk_g2s(smem_u32(w_tile(s)), w_block(t, kb), kWTileBytes, bar);
+                        bulk_g2s_hint(smem_u32(w_tile(s)), w_block(t, kb), kWTileBytes, bar,
+                                      evict_first);
                     }
                     tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, t.b0, bar);
                     issued = stage + 1;
