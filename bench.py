@@ -676,7 +676,8 @@ def run_moe(args):
                        "cuda_graph": True},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
-                         "kernel": "skinny (grouped)", "traffic": None,
+                         "kernel": "skinny (grouped)",
+                         "traffic": traffic_from_profiles("skinny", "moe"),
                          "algorithmic_bytes_per_launch": bytes_step / len(shapes)},
             "clocks": clk.summary(), "gpu_launches": steps * len(shapes),
             "e2e": {"value": bytes_step / t_e2e / 1e12, "unit": "TB/s",
