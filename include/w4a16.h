@@ -177,9 +177,11 @@ w4a16_status w4a16_dequant_ref(const void *packed, const void *scales, int has_z
  *   packed     E packed blobs back to back, each w4a16_packed_bytes(K, N,
  *              128, has_zeros) bytes (from w4a16_pack)
  *   scales     bf16 [E][K/128][N]
- *   max_rows   an upper bound on one expert's rows (picks the batch tile:
- *              <= 8, <= 16, else 32 rows); an expert with more rows is still
- *              computed correctly, in more tiles
+ *   max_rows   an upper bound on one expert's rows; with the mean T/E it
+ *              picks the batch tile (8, 16 or 32 rows: 8 when max_rows <= 8
+ *              or T/E <= 5, 16 when max_rows <= 16 or T/E <= 10); an expert
+ *              with more rows than the tile is computed correctly in more
+ *              tiles (reading its weights once per tile)
  *   workspace  w4a16_grouped_workspace_bytes(T, E, max_rows, K, N, 128) bytes,
  *              same contract as w4a16_gemm's (zero-filled once, left zero)
  * Errors: UNSUPPORTED (group_size), SHAPE (K, N, T < 1, E outside 1..256,

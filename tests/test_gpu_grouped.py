@@ -72,6 +72,15 @@ def test_ragged_experts_small(zp, max_rows):
 
 
 @pytest.mark.parametrize("zp", [False, True])
+def test_tall_experts_32_row_tiles(zp):
+    """Few experts with many rows (mean 32): the 32-row batch tile, an expert
+    above it split over several tiles, and an empty expert."""
+    p = inputs.make_grouped_problem(inputs.offsets_from_counts([40, 0, 70, 18]), 1024, 264, 71,
+                                    zero_points=zp)
+    check(run(p, 70), p)
+
+
+@pytest.mark.parametrize("zp", [False, True])
 def test_split_k_and_repeat(zp):
     """Few rows over a deep K: the planner splits K (fp32 partials + arrival
     counters); a second call must find the workspace clean again."""
