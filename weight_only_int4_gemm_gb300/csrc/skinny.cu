@@ -21,13 +21,18 @@
 //    8).  The products (q - z)*x are exact; each 128-row group is summed in
 //    fp32 and multiplied by its scale once (acc += s * sum), which removes the
 //    per-weight bf16 multiply from the CUDA cores -- at decode batch sizes the
-//    issue slots, not the tensor cores, bound the kernel.  The k order inside an mma is
+//    decode instructions and their latency, not the tensor cores, bound the
+//    kernel.  The k order inside an mma is
 //    free, so each lane's four k values per step are consecutive rows of its
 //    own 32-row chunk; the activations are staged in exactly that fragment
 //    order, which makes each fragment load one 16-byte read;
 //  * work units are (batch chunk, column tile, K split), handed out
 //    dynamically (the first unit of each CTA is fixed, later ones come from an
-//    atomic work counter), so slow and fast SMs even out;
+//    atomic work counter), so slow and fast SMs even out; the producer decodes
+//    a unit once and publishes, per slot, what the consumers need;
+//  * grouped mode (mixture-of-experts layers): the batch chunks are counted
+//    over all experts from a device-side routing table, and a unit's codes,
+//    scales and rows are its expert's;
 //  * a dedicated epilogue warp takes each finished unit's accumulators from
 //    shared memory and writes y -- or, for a K split, adds them into an fp32
 //    accumulator with vector reductions (red.global.add.v4.f32), the last
@@ -38,6 +43,8 @@
 //  * programmatic dependent launch: the first ring slots' weight copies are
 //    issued before waiting for the previous kernel on the stream, so
 //    consecutive layers' weight streams overlap.
+// The plain, grouped and fused-epilogue (bias / SiLU gate) forms are separate
+// instantiations, so the plain kernel carries none of the others' code.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT in the device status word and returns.
 #include <cuda_runtime.h>
