@@ -489,10 +489,11 @@ bool encode_operand(EncodeTiledFn enc, CUtensorMap* map, const void* base, int K
            CUDA_SUCCESS;
 }
 
-// Up to 32 batch rows two CTAs share an SM (two independent copy / MMA /
-// epilogue pipelines; measured: the B = 1 linear set 56.4 -> 50.7 us), each
-// with half the shared memory; wider tiles run one CTA per SM.
-int ctas_per_sm(int bn) { return bn <= 32 ? 2 : 1; }
+// Up to 128 batch rows two CTAs share an SM (two independent copy / MMA /
+// epilogue pipelines, each with half the shared memory; measured on the
+// linear set: B = 1 56.4 -> 50.7 us for the GEMMs, B = 64 127.6 -> 112.9 us and
+// B = 128 198.6 -> 175.0 us per step); 256-row tiles run one CTA per SM.
+int ctas_per_sm(int bn) { return bn <= 128 ? 2 : 1; }
 
 int stages_for(int bn) {
     const size_t budget = ctas_per_sm(bn) == 2 ? kSmemBudget / 2 : kSmemBudget;
