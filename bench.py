@@ -1,17 +1,23 @@
 """Benchmark of the W4A16 group-128 linear layer on one GB300 (or N replicas).
 
-Default workload (one JSON line): one Llama-3-8B decoder layer's linear set
-at decode -- qkv 4096->6144, o_proj 4096->4096, gate_up 4096->28672,
-down 14336->4096 -- for every B in {1, 2, 4, 8, 16}.  One step is those
-20 GEMMs (the whole hot path: weight + scale stream, register decode, tensor
-products, split-K reduction, bf16 epilogue).  Synthetic seeded inputs with
-the shapes and value distributions of that workload; the packed weights are
-rotated over enough copies that every GEMM streams them from HBM, not L2.
+Default workload (one JSON line): the full Llama-3-8B decode-step linear
+stream -- 32 decoder layers of qkv 4096->6144, o_proj 4096->4096, gate_up
+4096->28672 and down 14336->4096, plus lm_head 4096->128256: 129 GEMMs and
+7 504 658 432 streamed weights per decode step -- swept over the batch sizes
+B in {1, 4, 16, 64, 128, 256, 270, 384, 512, 1024} that map the
+memory-bound-to-compute-bound crossover.  One bench step is one decode step
+at every B of the sweep (1290 GEMMs: the whole hot path -- weight + scale
+stream, register decode, tensor products, split-K reduction, bf16
+epilogue).  Synthetic seeded inputs with the shapes and value distributions
+of that workload; the 129 distinct weight sets (3.87 GB) exceed L2, so every
+GEMM streams its weights from HBM.
 
-``value`` is algorithmic TB/s over all ranks (bytes = codes + scales + x + y
-per GEMM); ``us_per_step`` is also reported.  Other workloads
-(``--workload``) print the same line format for the prefill, full decode
-step and zero-point shapes.
+``value`` is the time of one sweep step in µs; ``per_batch`` gives, for every
+B, the decode step's µs, TB/s, TFLOP/s, its roofline (bound, fraction of the
+measured peak) and the measured time above max(memory, math) -- the
+dequantisation cost the two-term decode-step model predicts, where it stops
+hiding.  Other workloads (``--workload``) print the same kind of line for the
+decoder-layer set, the prefill, single-step and zero-point shapes.
 
 ``--impl reference`` times the CPU oracle (the slow definition the library is
 checked against) on a bounded sample of the same workload.
@@ -39,6 +45,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 FORCE = -1  # kernel path forced from the command line (-1: the library's choice)
+SWEEP_BATCHES = (1, 4, 16, 64, 128, 256, 270, 384, 512, 1024)
+LM_HEAD = ("lm_head", 4096, 128256)
 
 
 # --------------------------------------------------------------- workloads
@@ -94,7 +102,10 @@ def kernel_source_hash(names):
 
 
 KERNEL_FILES = {"skinny": ["skinny.cu", "dequant.cuh", "epilogue.cuh"],
-                "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "dequant.cuh", "epilogue.cuh"]}
+                "skinny_kernel": ["skinny.cu", "dequant.cuh", "epilogue.cuh"],
+                "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "dequant.cuh", "epilogue.cuh"],
+                "tc_kernel": ["tc_gemm.cu", "dequant.cuh", "epilogue.cuh"],
+                "wide_kernel": ["tc_wide.cu", "dequant.cuh", "epilogue.cuh"]}
 
 
 def traffic_from_profiles(kernel: str, workload_name: str):
@@ -298,9 +309,11 @@ def run_gpu(args, gemms, rank, world, device):
     return ms, clk.summary(), paths, n_copies, e2e, step_pct
 
 
-def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200, path=-1):
+def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200, path=-1,
+                   tflops=None):
     """Each distinct (B, K, N) alone, in a CUDA graph of `reps` launches that
-    rotate over the weight copies; prints one line per GEMM to stderr."""
+    rotate over the weight copies; prints one line per GEMM to stderr, with the
+    roofline fraction against the burst peaks (a kernel timed alone)."""
     import torch
 
     import weight_only_int4_gemm_gb300 as w
@@ -335,10 +348,13 @@ def per_gemm_table(gemms, layers, ws, stream, device, hbm_gbs, reps=200, path=-1
         us = e0.elapsed_time(e1) * 1e3 / reps
         byts = model.linear_bytes(B, K, N, zp)
         fl = model.linear_flops(B, K, N)
-        pname = w.PATH_NAMES[w.w4a16_select_path(B, K, N) if path < 0 else path]
-        print(f"per-gemm B={B:5d} K={K:6d} N={N:6d} zp={int(zp)} path={pname:8s} "
+        pname = w.w4a16_kernel_name(B, K, N) if path < 0 else w.PATH_NAMES[path]
+        tf = tflops or load_peaks()[1]
+        roof = max(byts / (hbm_gbs * 1e3), fl / (tf * 1e6))  # µs
+        print(f"per-gemm B={B:5d} K={K:6d} N={N:6d} zp={int(zp)} kernel={pname:12s} "
               f"{us:9.2f} us  {byts / us / 1e3:8.1f} GB/s ({byts / us / 1e3 / hbm_gbs * 100:5.1f}% hbm)  "
-              f"{fl / us / 1e6:8.1f} TFLOP/s", file=sys.stderr, flush=True)
+              f"{fl / us / 1e6:8.1f} TFLOP/s ({fl / us / 1e6 / tf * 100:5.1f}% bf16 burst)  "
+              f"roofline frac {roof / us:5.3f}", file=sys.stderr, flush=True)
 
 
 def run_e2e(args, gemms, layers, device, ws, pick, n_copies):
@@ -479,6 +495,289 @@ def reduce_times_over_ranks(ms: float, e2e_step_ms: float, world: int, device=No
 def aggregate_value(bytes_per_step: int, world: int, step_s: float) -> float:
     """Whole-job TB/s: every replica streams its own step's bytes."""
     return bytes_per_step * world / step_s / 1e12
+
+
+# --------------------------------------------------------------- decode-step sweep
+
+def sweep_layers():
+    """The 129 GEMM shapes of one Llama-3-8B decode step, in execution order."""
+    return [(f"{lbl}_L{i}", K, N) for i in range(32) for lbl, K, N in LAYER] + [LM_HEAD]
+
+
+def sweep_roofline(byts: float, flops: float, t_s: float, hbm: float, tflops: float):
+    """Bound, achieved, fraction and the time above max(memory, math)."""
+    t_mem = byts / (hbm * 1e9)
+    t_math = flops / (tflops * 1e12)
+    if t_mem >= t_math:
+        r = {"bound": "hbm", "achieved": byts / t_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": tflops,
+             "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["memory_us"] = t_mem * 1e6
+    r["math_us"] = t_math * 1e6
+    r["above_roofline_us"] = (t_s - max(t_mem, t_math)) * 1e6
+    return r
+
+
+class SweepOracleSampler:
+    """Times the CPU oracle on a column sample of every distinct (B, K, N) of the
+    sweep and extrapolates to the whole sweep step (the oracle's cost is linear
+    in columns: each column is dequantised once and dotted with every row)."""
+
+    def __init__(self, batches):
+        import numpy as np
+
+        import oracle
+        from weight_only_int4_gemm_gb300 import inputs
+        self.np, self.oracle = np, oracle
+        self.MAX_COLS = 4096
+        counts = {}
+        for _, K, N in sweep_layers():
+            counts[(K, N)] = counts.get((K, N), 0) + 1
+        self.probs = []
+        for B in batches:
+            for i, ((K, N), cnt) in enumerate(sorted(counts.items())):
+                qw, sc, _ = inputs.make_weights(K, min(N, self.MAX_COLS), seed=i)
+                x = inputs.make_activations(B, K, seed=30_000 + 7 * B + i)
+                self.probs.append((B, x.view(__import__("torch").int16).numpy().view(np.uint16),
+                                   qw.numpy().view(np.uint32),
+                                   sc.view(__import__("torch").int16).numpy().view(np.uint16),
+                                   N, cnt))
+        self.cols = 1
+
+    def step(self) -> float:
+        est = 0.0
+        c = self.np.arange(self.cols, dtype=self.np.int32)
+        for B, x, qw, sc, N, cnt in self.probs:
+            t1 = time.perf_counter()
+            self.oracle.gemm(x, qw, sc, None, cols=c)
+            est += (time.perf_counter() - t1) * N / self.cols * cnt
+        return est
+
+    def calibrate(self, seconds_per_step: float):
+        while self.cols < self.MAX_COLS:
+            t0 = time.perf_counter()
+            self.step()
+            if time.perf_counter() - t0 >= seconds_per_step:
+                break
+            self.cols *= 2
+
+    def describe(self, steps: int, seconds: float) -> str:
+        return (f"{self.cols} column(s) of each of the {len(self.probs)} distinct (B, K, N) "
+                f"GEMMs of the sweep (all rows, all K), timed and extrapolated by N/columns "
+                f"and by the GEMM's count per decode step (32 layers, 1 lm_head); {steps} "
+                f"sampled step(s), {seconds:.1f} s of CPU work")
+
+
+def kernel_name(w, B, K, N):
+    return w.w4a16_kernel_name(B, K, N) if FORCE < 0 else w.PATH_NAMES[FORCE]
+
+
+def run_sweep(args, rank, world, device):
+    """Config 3: one decode step at every B of the sweep, as one CUDA graph per B."""
+    import torch
+
+    import weight_only_int4_gemm_gb300 as w
+    from weight_only_int4_gemm_gb300 import inputs, model
+
+    batches = [args.batch] if args.batch else list(SWEEP_BATCHES)
+    shapes = sweep_layers()
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    # 129 distinct weight sets (3.87 GB > L2): every GEMM streams from HBM
+    weights = []
+    for i, (lbl, K, N) in enumerate(shapes):
+        qw, sc, _ = inputs.make_weights(K, N, seed=1_000 + i, device=device)
+        weights.append((w.w4a16_pack(qw), sc))
+        del qw
+    ws = torch.zeros(max(w.w4a16_workspace_bytes(B, K, N) for B in batches
+                         for _, K, N in shapes) + 256, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+    per_b = []
+    for B in batches:
+        x_tot = sum(B * K for _, K, _ in shapes)
+        y_tot = sum(B * N for _, _, N in shapes)
+        dev_x = torch.empty(x_tot, dtype=torch.bfloat16, device=device)
+        dev_y = torch.empty(y_tot, dtype=torch.bfloat16, device=device)
+        xs, ys, ox, oy = [], [], 0, 0
+        for i, (lbl, K, N) in enumerate(shapes):
+            xs.append(dev_x[ox:ox + B * K].view(B, K))
+            ys.append(dev_y[oy:oy + B * N].view(B, N))
+            xs[-1].copy_(inputs.make_activations(B, K, seed=10_000 + 7 * B + i, device=device))
+            ox += B * K
+            oy += B * N
+        byts = sum(model.linear_bytes(B, K, N) for _, K, N in shapes)
+        flops = sum(model.linear_flops(B, K, N) for _, K, N in shapes)
+        kern = kernel_name(w, B, 4096, 4096)
+        per_b.append({"B": B, "dev_x": dev_x, "dev_y": dev_y, "xs": xs, "ys": ys,
+                      "bytes": byts, "flops": flops, "kernel": kern})
+
+    def decode_step(e):
+        for i, (lbl, K, N) in enumerate(shapes):
+            packed, sc = weights[i]
+            w.w4a16_gemm(e["xs"][i], packed, sc, False, N, out=e["ys"][i], workspace=ws,
+                         stream=stream, path=FORCE)
+
+    with torch.cuda.stream(stream):
+        for e in per_b:
+            decode_step(e)
+    stream.synchronize()
+    for e in per_b:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            decode_step(e)
+        e["graph"] = g
+    stream.synchronize()
+
+    def sweep_step(evs=None):
+        for j, e in enumerate(per_b):
+            if evs is not None:
+                evs[j].record(stream)
+            e["graph"].replay()
+        if evs is not None:
+            evs[-1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            sweep_step()
+    stream.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(per_b) + 1)]
+           for _ in range(args.steps)]
+    with ClockSampler(device.index or 0) as clk:
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                sweep_step(evs[k])
+        evs[-1][-1].synchronize()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
+    ms_total = evs[0][0].elapsed_time(evs[-1][-1])
+    for j, e in enumerate(per_b):
+        times = sorted(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps))
+        e["ms"] = sum(times) / len(times)
+        e["p50_ms"] = times[len(times) // 2]
+
+    # end to end through the public API with host buffers: per B, one H2D
+    # copy of all of the decode step's activations from pinned host memory,
+    # the step's 129 w4a16_gemm calls and one D2H copy of all of its outputs,
+    # captured as one CUDA graph per B and replayed once per sweep step
+    h2d = d2h = 0
+    for e in per_b:
+        e["host_x"] = e["dev_x"].cpu().pin_memory()
+        e["host_y"] = torch.empty(e["dev_y"].numel(), dtype=torch.bfloat16).pin_memory()
+        h2d += e["host_x"].numel() * 2
+        d2h += e["host_y"].numel() * 2
+
+    def e2e_body(e):
+        e["dev_x"].copy_(e["host_x"], non_blocking=True)
+        decode_step(e)
+        e["host_y"].copy_(e["dev_y"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for e in per_b:
+            e2e_body(e)
+    stream.synchronize()
+    for e in per_b:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_body(e)
+        e["e2e_graph"] = g
+    e2e_steps = max(3, min(args.steps, args.e2e_steps, 10))
+    with torch.cuda.stream(stream):
+        for e in per_b:
+            e["e2e_graph"].replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for e in per_b:
+                e["e2e_graph"].replay()
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    assert w.w4a16_device_status() == 0, "device-side wait timed out during the bench"
+    if args.per_gemm:
+        seen = {}
+        for i, (lbl, K, N) in enumerate(shapes):
+            seen.setdefault((K, N), i)
+        for e in per_b:
+            gem = [(f"{shapes[i][0]}_B{e['B']}", e["B"], K, N, False, 0.0)
+                   for (K, N), i in seen.items()]
+            lays = {(K, N, False): [weights[i]] + [weights[j] for j, s2 in enumerate(shapes)
+                                                  if (s2[1], s2[2]) == (K, N) and j != i][:5]
+                    for (K, N), i in seen.items()}
+            per_gemm_table(gem, lays, ws, stream, device, hbm, path=FORCE, tflops=tf_burst)
+    return per_b, ms_total / args.steps, clk.summary(), e2e_ms, h2d, d2h, e2e_steps
+
+
+def sweep_line(args, per_b, step_ms, clocks, e2e_ms, h2d, d2h, e2e_steps, world, device):
+    import weight_only_int4_gemm_gb300 as w
+
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    step_ms, e2e_ms = reduce_times_over_ranks(step_ms, e2e_ms, world, device)
+    rows = []
+    by_kernel = {}
+    for e in per_b:
+        t = e["ms"] / 1e3
+        r = sweep_roofline(e["bytes"], e["flops"], t, hbm, tf_sust)
+        rows.append({"B": e["B"], "kernel": e["kernel"], "us_per_step": e["ms"] * 1e3,
+                     "p50_us": e["p50_ms"] * 1e3, "tb_s": e["bytes"] / t / 1e12,
+                     "tflops": e["flops"] / t / 1e12, "roofline": {
+                         k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac")},
+                     "memory_us": r["memory_us"], "math_us": r["math_us"],
+                     "above_roofline_us": r["above_roofline_us"],
+                     "algorithmic_bytes": e["bytes"], "flops": e["flops"]})
+        k = by_kernel.setdefault(e["kernel"], {"s": 0.0, "bytes": 0, "flops": 0, "launches": 0})
+        k["s"] += t
+        k["bytes"] += e["bytes"]
+        k["flops"] += e["flops"]
+        k["launches"] += len(sweep_layers())
+    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["s"])
+    roof = sweep_roofline(dom["bytes"], dom["flops"], dom["s"], hbm, tf_sust)
+    roof = {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    roof.update({"peak_source": f"{peak_src} " + ("hbm_gbs" if roof["bound"] == "hbm"
+                                                  else "bf16 sustained (timed inside a long step)"),
+                 "kernel": dom_name, "launches_per_step": dom["launches"],
+                 "share_of_step": dom["s"] / (step_ms / 1e3),
+                 "traffic": traffic_from_profiles(dom_name, "decode_sweep"),
+                 "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"],
+                 "flops_per_launch": dom["flops"] / dom["launches"]})
+    sbytes = sum(e["bytes"] for e in per_b)
+    sflops = sum(e["flops"] for e in per_b)
+    launches = len(sweep_layers()) * len(per_b)
+    line = {"metric": METRIC, "value": step_ms * 1e3, "unit": "µs/step",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_ms, "us_per_step": step_ms * 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; Llama-3-8B shapes, no trained weights)",
+            "config": {"workload": "decode_sweep: full Llama-3-8B decode-step linear stream "
+                                   "(32 layers + lm_head, 129 GEMMs) at every B of the sweep",
+                       "batches": [e["B"] for e in per_b], "gemms_per_decode_step": 129,
+                       "streamed_weights": sum(K * N for _, K, N in sweep_layers()),
+                       "shapes_KxN": ["4096x6144", "4096x4096", "4096x28672", "14336x4096",
+                                      "4096x128256"],
+                       "group": 128, "zero_points": False,
+                       "algorithmic_bytes_per_step": sbytes, "flops_per_step": sflops,
+                       "step": "one decode step at every B of the sweep",
+                       "l2": "129 distinct weight sets (3.87 GB) per decode step: inputs larger "
+                             "than L2", "cuda_graph": "one graph per B",
+                       "parallelism": f"replicas{world}"},
+            "throughput": {"tb_s": sbytes * world / (step_ms / 1e3) / 1e12,
+                           "tflops": sflops * world / (step_ms / 1e3) / 1e12},
+            "per_batch": rows, "roofline": roof, "clocks": clocks,
+            "gpu_launches": args.steps * launches,
+            "e2e": {"value": e2e_ms * 1e3, "unit": "µs/step", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "launch": "per B, one CUDA graph of: an H2D copy of all of the decode "
+                              "step's activations from pinned host memory, its 129 w4a16_gemm "
+                              "calls, a D2H copy of all of its outputs"}}
+    return line
 
 
 # --------------------------------------------------------------- offline quantizer
@@ -839,15 +1138,90 @@ def run_fp8(args):
 
 # --------------------------------------------------------------- main
 
+def run_sweep_main(args, rank, world, local):
+    """Default workload: the decode-step sweep (GPU arm, or the oracle as the
+    reference arm)."""
+    from weight_only_int4_gemm_gb300 import model
+    batches = [args.batch] if args.batch else list(SWEEP_BATCHES)
+    sbytes = sum(model.linear_bytes(B, K, N) for B in batches for _, K, N in sweep_layers())
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        sampler = SweepOracleSampler(batches)
+        sampler.calibrate(min(2.0, 60.0 / (args.warmup + args.steps)))
+        per_step, t_begin = [], time.perf_counter()
+        for k in range(args.warmup + args.steps):
+            if k > args.warmup and time.perf_counter() - t_begin > 150:
+                break
+            per_step.append(sampler.step())
+        timed = per_step[args.warmup:] if len(per_step) > args.warmup else per_step[-1:]
+        t_step = sum(timed) / len(timed)
+        sample = sampler.describe(len(timed), time.perf_counter() - t_begin)
+        line = {"impl": "reference", "metric": METRIC, "value": t_step * 1e6, "unit": "µs/step",
+                "n_gpus": 1, "steps": len(timed), "warmup": args.warmup,
+                "ms_per_step": t_step * 1e3, "us_per_step": t_step * 1e6,
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "decode_sweep: full Llama-3-8B decode-step linear stream "
+                                       "(32 layers + lm_head, 129 GEMMs) at every B of the sweep",
+                           "batches": batches, "algorithmic_bytes_per_step": sbytes},
+                "throughput": {"tb_s": sbytes / t_step / 1e12},
+                "cpu_baseline": {"value": t_step * 1e6, "unit": "µs/step",
+                                 "cores": oracle.omp_threads(), "kind": "oracle",
+                                 "sample": sample, "extrapolated": True},
+                "e2e": {"value": t_step * 1e6, "unit": "µs/step", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from __graft_entry__ import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+        build()
+    per_b, step_ms, clocks, e2e_ms, h2d, d2h, e2e_steps = run_sweep(args, rank, world, device)
+    line = sweep_line(args, per_b, step_ms, clocks, e2e_ms, h2d, d2h, e2e_steps, world, device)
+    del per_b
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        sampler = SweepOracleSampler(batches)
+        sampler.calibrate(args.cpu_budget / 4)
+        t0 = time.perf_counter()
+        runs = [sampler.step()]
+        while time.perf_counter() - t0 < args.cpu_budget and len(runs) < 50:
+            runs.append(sampler.step())
+        t_cpu = statistics.median(runs)
+        line["cpu_baseline"] = {"value": t_cpu * 1e6, "unit": "µs/step",
+                                "cores": oracle.omp_threads(), "kind": "oracle",
+                                "extrapolated": True,
+                                "sample": sampler.describe(len(runs), time.perf_counter() - t0),
+                                "tb_s": sbytes / t_cpu / 1e12}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 20 for decode_sweep, 10000 otherwise)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed warm-up steps (default 5 for decode_sweep, 50 otherwise)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_layer",
-                    choices=["decode_layer", "single", "decode_step", "prefill", "zp70b",
-                             "quantize", "moe", "fp8"])
+    ap.add_argument("--workload", default="decode_sweep",
+                    choices=["decode_sweep", "decode_layer", "single", "decode_step", "prefill",
+                             "zp70b", "quantize", "moe", "fp8"])
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--shape", default=None, help="KxN for --workload single (default 4096x4096)")
     ap.add_argument("--e2e-steps", type=int, default=300)
@@ -858,6 +1232,11 @@ def main():
     ap.add_argument("--per-gemm", action="store_true",
                     help="also time each distinct GEMM alone (table on stderr)")
     args = ap.parse_args()
+    sweep = args.workload == "decode_sweep"
+    if args.steps is None:
+        args.steps = 20 if sweep else 10000
+    if args.warmup is None:
+        args.warmup = 5 if sweep else 50
     global FORCE
     FORCE = {"skinny": 0, "tcgen05": 1}.get(args.force_path, -1)
     if args.warmup < 3:
@@ -878,6 +1257,9 @@ def main():
         if args.impl == "reference" or rank != 0:
             raise SystemExit("--workload moe runs our arm on one GPU only")
         run_moe(args)
+        return
+    if sweep:
+        run_sweep_main(args, rank, world, local)
         return
     gemms = workload(args.workload, args.batch, args.shape)
     sbytes, sflops = step_bytes_flops(gemms)

@@ -87,11 +87,15 @@ size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros);
 /* Bytes of device workspace w4a16_gemm needs for this shape (0 if none).
  * The workspace holds arrival counters, the small-batch kernel's work
  * scheduler and an fp32 accumulator for split-K sums.  It must be
- * zero-filled once before its first use; every call leaves it all-zero
- * again, so later calls of any shape on the same stream can reuse it.
- * Calls that run concurrently must use different workspaces.  (Split-K sums
- * are accumulated in arrival order, so outputs may differ in the last bit
- * between calls; every one is within the error bound.)
+ * zero-filled once before its first use; every call that completes (device
+ * status OK) leaves it all-zero again, so later calls of any shape on the
+ * same stream can reuse it.  A call whose bounded wait expired
+ * (w4a16_device_status reports W4A16_ERR_TIMEOUT) stops part-way and may
+ * leave partial sums and counts in it: the caller must zero-fill the
+ * workspace again before reusing it.  Calls that run concurrently must use
+ * different workspaces.  (Split-K sums are accumulated in arrival order, so
+ * outputs may differ in the last bit between calls; every one is within the
+ * error bound.)
  * Returns (size_t)-1 for invalid shapes. */
 size_t w4a16_workspace_bytes(int B, int K, int N, int group_size);
 
@@ -213,8 +217,22 @@ w4a16_status w4a16_quantize_rtn(const void *w, int K, int N, int group_size, uin
                                 void *scales, void *stream);
 
 /* Path w4a16_gemm would take for this shape on the current device
- * (W4A16_PATH_*), or -1 for invalid shapes. */
+ * (W4A16_PATH_*), or -1 for invalid shapes.  The choice is made per shape
+ * because the layer changes regime with the batch: "When quantization pays
+ * -- and when it does not", sections "Model one decode step" and "The three
+ * regimes" (weight-stream-bound at small B, tensor-core-bound past the ridge
+ * batch), and the M-dependent kernel selection that page describes (a
+ * small-batch kernel below a row threshold, the tiled tensor-core kernel
+ * above it). */
 int w4a16_select_path(int B, int K, int N);
+
+/* Name of the kernel w4a16_gemm launches for this shape on the current
+ * device: "skinny_kernel" (small-batch split-K), "tc_kernel" (tensor cores,
+ * weight tile in tensor memory) or "wide_kernel" (tensor cores, weight tile
+ * in shared memory); "invalid" for invalid shapes.  For logs and for
+ * reporting which operator ran ("Quantization quality and performance":
+ * report the operator actually used).  Never NULL; static storage. */
+const char *w4a16_kernel_name(int B, int K, int N);
 
 /* Device-side status word of the tensor-core kernel: 0 when every bounded
  * wait completed, else W4A16_ERR_TIMEOUT.  Synchronises the current device;
@@ -230,10 +248,12 @@ w4a16_status w4a16_device_status(int clear);
  *  - Calls no cudaMalloc, cudaFree or allocating library routine.
  *  - The first call on a device looks the array's device address up for
  *    that device; make that first call before any stream capture.
- *  - Every call shares the one array and clears its arrival counters on
- *    `stream` first; calls that may overlap on the GPU (different streams,
- *    or different host threads) race on it and must be serialised by the
- *    caller.
+ *  - Every call shares the one array and first clears (one memset on
+ *    `stream`) every byte of it that the shape uses -- arrival counters,
+ *    scheduler words and the fp32 split-K accumulator -- so a call whose
+ *    bounded wait expired cannot leave partial sums for the next call; calls
+ *    that may overlap on the GPU (different streams, or different host
+ *    threads) race on it and must be serialised by the caller.
  *  - Returns W4A16_ERR_WORKSPACE when the shape needs more scratch than the
  *    array holds (w4a16_workspace_bytes() tells how much it needs). */
 w4a16_status w4a16_gemm_static_scratch(const void *x, const void *packed, const void *scales,

@@ -41,8 +41,9 @@ def assert_within_bound(y_gpu: torch.Tensor, p: inputs.LinearProblem, cols=None,
 
     Returns the worst ratio |diff| / bound (for reporting)."""
     if rows is not None:
-        p = inputs.LinearProblem(p.x[rows], p.qweight, p.scales, p.qzeros)
-        y_gpu = y_gpu[rows]
+        idx = torch.as_tensor(np.asarray(rows), dtype=torch.long)
+        p = inputs.LinearProblem(p.x[idx], p.qweight, p.scales, p.qzeros)
+        y_gpu = y_gpu[idx]
     y_o, _, bound = oracle_gemm(p, cols)
     yg = bits_to_f64(bits(y_gpu))
     if cols is not None:

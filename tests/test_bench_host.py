@@ -66,3 +66,22 @@ def test_committed_traffic_file_parses():
     path = os.path.join(bench.ROOT, "profiles", "dram_traffic.txt")
     lines = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
     assert lines and all(len(p) == 4 and p[3].isdigit() for p in lines)
+
+
+def test_sweep_is_config_three():
+    """The default workload: the full decode step (32 layers + lm_head) at every
+    batch of the crossover sweep."""
+    layers = bench.sweep_layers()
+    assert len(layers) == 129 and layers[-1][1:] == (4096, 128256)
+    assert sum(K * N for _, K, N in layers) == 7504658432
+    assert bench.SWEEP_BATCHES == (1, 4, 16, 64, 128, 256, 270, 384, 512, 1024)
+
+
+def test_sweep_roofline_bound_and_excess():
+    # memory-bound: 1 GB at 1000 GB/s = 1 ms; 1 TFLOP at 1000 TFLOP/s = 1 ms
+    r = bench.sweep_roofline(1e9, 0.5e12, 2e-3, 1000.0, 1000.0)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-12
+    assert abs(r["above_roofline_us"] - 1000.0) < 1e-6
+    r = bench.sweep_roofline(0.5e9, 1e12, 4e-3, 1000.0, 1000.0)
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.25) < 1e-12
+    assert abs(r["achieved"] - 250.0) < 1e-9 and abs(r["above_roofline_us"] - 3000.0) < 1e-6

@@ -145,6 +145,42 @@ def test_lm_head_sampled_columns(B):
     assert_within_bound(y, p, cols=sample_columns(128256, 96 if B > 64 else 384))
 
 
+def boundary_rows(B: int, step: int = 16) -> np.ndarray:
+    """The first and last row of every `step`-row block of the batch (every
+    batch tile of the tensor-core kernels starts on a multiple of 16 rows),
+    and the last row of the ragged final block."""
+    rows = {0, B - 1}
+    for r in range(0, B, step):
+        rows |= {r, min(B - 1, r + step - 1)}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("B", [17, 64, 128, 256, 270, 384, 512, 1024])
+def test_lm_head_every_column_on_tile_boundary_rows(B):
+    """4096 -> 128256 lm_head on the tensor-core kernels: every one of the
+    128256 columns (every column tile, the persistent scheduler's every item
+    and K split), on the first and last rows of every 16-row block."""
+    p = inputs.make_problem(B, 4096, 128256, seed=77)
+    y = run_gemm(p)
+    assert_within_bound(y, p, rows=boundary_rows(B, 16 if B <= 384 else 32))
+
+
+@pytest.mark.parametrize("name", ["qkv", "gate_up", "down"])
+def test_prefill_m2048_every_column_on_tile_boundary_rows(name):
+    K, N = LAYER_SHAPES[name]
+    p = inputs.make_problem(2048, K, N, seed=4000 + K + N, outlier_frac=0.01)
+    y = run_gemm(p)
+    assert_within_bound(y, p, rows=boundary_rows(2048, 64))
+
+
+@pytest.mark.parametrize("B", [64, 512])
+@pytest.mark.parametrize("K,N", [(8192, 10240), (8192, 57344), (28672, 8192)])
+def test_zero_point_70b_every_column_on_tile_boundary_rows(K, N, B):
+    p = inputs.make_problem(B, K, N, seed=5000 + K + N, zero_points=True)
+    y = run_gemm(p)
+    assert_within_bound(y, p, rows=boundary_rows(B, 16 if B <= 64 else 64))
+
+
 @pytest.mark.parametrize("name", ["qkv", "gate_up", "down"])
 def test_prefill_m2048_with_outliers_sampled(name):
     K, N = LAYER_SHAPES[name]
@@ -237,20 +273,31 @@ def test_workspace_validation_on_tensor_core_split():
 
 def test_bounded_wait_expires_cleanly_and_context_survives():
     """A wait that nothing satisfies expires after ~50 ms: the status word says
-    TIMEOUT, y is untouched, and the next GEMM on the same context is correct."""
+    TIMEOUT, y is untouched, and the next GEMM on the same context is correct.
+    The shape splits K, so the call owns a workspace; after the timeout the
+    workspace is zero-filled again (the header's rule after a TIMEOUT) and
+    reused by the next call, which must then be within the bound."""
     if w.PATH_TCGEN05 not in available_paths():
         pytest.skip("tensor-core kernel unavailable")
     assert w.w4a16_device_status(clear=True) == 0
     B, K, N = 64, 1024, 256
+    need = w.w4a16_workspace_bytes(B, K, N)
+    assert need > 0, "expected a split-K plan for this shape"
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     p = inputs.make_problem(B, K, N, seed=13).to("cuda")
     packed = w.w4a16_pack(p.qweight)
     y = torch.full((B, N), 7.0, dtype=torch.bfloat16, device="cuda")
-    assert w.w4a16_debug_forced_timeout(p.x, packed, p.scales, False, y, wait_ms=50) == 0
+    assert w.w4a16_debug_forced_timeout(p.x, packed, p.scales, False, y, wait_ms=50,
+                                        workspace=ws) == 0
     torch.cuda.synchronize()
     assert w.w4a16_device_status(clear=True) == 7
     assert torch.all(y == 7.0)
     assert w.w4a16_device_status(clear=False) == 0
-    y2 = w.w4a16_gemm(p.x, packed, p.scales, False, path=w.PATH_TCGEN05)
-    torch.cuda.synchronize()
-    assert w.w4a16_device_status() == 0
-    assert_within_bound(y2.cpu(), p.to("cpu"))
+    ws.zero_()
+    for _ in range(2):
+        y2 = w.w4a16_gemm(p.x, packed, p.scales, False, path=w.PATH_TCGEN05, workspace=ws)
+        torch.cuda.synchronize()
+        assert w.w4a16_device_status() == 0
+        assert_within_bound(y2.cpu(), p.to("cpu"))
+    # a completed call leaves its workspace all-zero again
+    assert int(torch.count_nonzero(ws)) == 0

@@ -73,3 +73,31 @@ def test_static_scratch_rejects_problems_larger_than_its_array():
     assert _static_gemm(x, packed, scales, False, y, torch.cuda.current_stream()) == 5
     torch.cuda.synchronize()
     assert torch.all(y == 0)
+
+
+def test_static_scratch_after_an_expired_wait():
+    """A GEMM whose bounded wait expires stops part-way.  The allocation-free
+    entry point clears all of the scratch a shape uses before every call, so
+    the next call through it is still within the error bound -- twice in a
+    row, on a shape that splits K."""
+    if w.w4a16_select_path(64, 4096, 4096) != w.PATH_TCGEN05:
+        pytest.skip("tensor-core kernel unavailable")
+    B, K, N = 64, 1024, 256
+    assert w.w4a16_workspace_bytes(B, K, N) > 0
+    p = inputs.make_problem(B, K, N, seed=613)
+    g = p.to("cuda")
+    packed = w.w4a16_pack(g.qweight)
+    ws = torch.zeros(w.w4a16_workspace_bytes(B, K, N), dtype=torch.uint8, device="cuda")
+    y = torch.zeros((B, N), dtype=torch.bfloat16, device="cuda")
+    assert w.w4a16_device_status(clear=True) == 0
+    assert w.w4a16_debug_forced_timeout(g.x, packed, g.scales, False, y, wait_ms=20,
+                                        workspace=ws) == 0
+    torch.cuda.synchronize()
+    assert w.w4a16_device_status(clear=True) == 7
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        y = torch.full((B, N), 3.0, dtype=torch.bfloat16, device="cuda")
+        assert _static_gemm(g.x, packed, g.scales, False, y, stream) == 0
+        torch.cuda.synchronize()
+        assert w.w4a16_device_status() == 0
+        assert_within_bound(y.cpu(), p)

@@ -38,6 +38,7 @@ SIGNATURES = {
     "w4a16_dequant_ref": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
     "w4a16_gemm_static_scratch": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),
     "w4a16_select_path": (_I, [_I, _I, _I]),
+    "w4a16_kernel_name": (ctypes.c_char_p, [_I, _I, _I]),
     "w4a16_debug_forced_timeout": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_device_status": (_I, [_I]),
     "w4a16_quantize_rtn": (_I, [_P, _I, _I, _I, _P, _P, _P]),
@@ -117,6 +118,10 @@ def w4a16_workspace_bytes(B: int, K: int, N: int) -> int:
 
 def w4a16_select_path(B: int, K: int, N: int) -> int:
     return int(load().w4a16_select_path(B, K, N))
+
+
+def w4a16_kernel_name(B: int, K: int, N: int) -> str:
+    return load().w4a16_kernel_name(B, K, N).decode()
 
 
 def w4a16_pack(qweight: torch.Tensor, qzeros: torch.Tensor | None = None, *,

@@ -329,6 +329,12 @@ int w4a16_select_path(int B, int K, int N) {
     return choose_path(B, K, N);
 }
 
+const char* w4a16_kernel_name(int B, int K, int N) {
+    if (!shape_ok(K, N) || B < 1 || B > kMaxB) return "invalid";
+    if (choose_path(B, K, N) == W4A16_PATH_SKINNY) return "skinny_kernel";
+    return plan_tc(B, K, N, num_sms()).wide ? "wide_kernel" : "tc_kernel";
+}
+
 w4a16_status w4a16_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return W4A16_ERR_CUDA;
     unsigned int v = 0;

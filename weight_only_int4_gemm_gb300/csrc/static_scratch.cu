@@ -62,11 +62,16 @@ extern "C" w4a16_status w4a16_gemm_static_scratch(const void* x, const void* pac
     int err = W4A16_OK;
     void* scratch = static_scratch_address(&err);
     if (scratch == nullptr) return static_cast<w4a16_status>(err);
-    // The array keeps whatever the previous call left; the arrival counters
-    // must start at zero, so clear them (only the counter prefix is read
-    // before being written).
-    if (need > 0 && cudaMemsetAsync(scratch, 0, kCounterBytes,
-                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The array keeps whatever the previous call left.  The kernels expect
+    // all of the scratch they use at zero: the arrival counters and scheduler
+    // words, and the fp32 accumulator the split-K partial sums are added
+    // into (red.global.add reads it).  A normal call leaves it at zero, but a
+    // call whose bounded wait expired (W4A16_ERR_TIMEOUT) can leave partial
+    // sums and counts behind, and the caller cannot reach this array to
+    // repair it -- so every call clears all `need` bytes first (at most the
+    // array's size; one memset on the caller's stream, no allocation).
+    if (need > 0 && cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) !=
+                        cudaSuccess)
         return W4A16_ERR_CUDA;
     return static_cast<w4a16_status>(gemm_entry(x, packed, scales, has_zeros, y, B, K, N,
                                                 group_size, scratch, kStaticScratchBytes,
