@@ -10,38 +10,42 @@
 // longer -- so here it runs in dedicated producer warps, overlapped with the
 // asynchronous tensor pipe.
 //
-// At wide batches every MMA is long (N up to 256), so one issuing thread keeps
-// the tensor pipe busy and the copies are large; this kernel keeps the simple
-// single-issuer pipeline with the weight tile in shared memory.
-//
 // Tile (operands swapped so the weight tile is the 128-row MMA operand):
 //   D[128 weight columns][bn batch rows] (fp32, TMEM)
 //     += W^T[128][64 k] (bf16, smem, dequantised by producer warps)
 //      . X^T[64 k][bn]  (bf16, smem, TMA from x[B][K])
-// Persistent CTAs (one per SM) take work items (column tile, batch tile, K
-// split) round robin and stream K in 64-row blocks through two rings: a ring
-// of packed-code + x stages (as deep as shared memory allows, an even number
-// of slots) and a ring of 4 dequantised weight tiles.  Warp roles:
-//   warp 0      : TMA thread -- bulk-copies the packed codes of the block (one
-//                 contiguous copy) and tensor-copies the x block (128-byte
-//                 swizzle), one mbarrier with the expected byte count per slot;
+// Persistent CTAs (one per SM) take work items (batch tile, column tile, K
+// split; the batch tile varies fastest, so the batch tiles of one weight tile
+// run side by side and its second reading comes from L2) round robin.  Three
+// rings keep the tensor pipe fed:
+//   * codes: one stage per 128-row group of the item (the packed codes of two
+//     64-row blocks, 8 KB, one bulk copy; the group's scale row and, for the
+//     asymmetric format, zero-point row, two more bulk copies).  The weights
+//     come from HBM, so this ring runs furthest ahead; the dequant warps read
+//     scales from it and never wait on a global load;
+//   * x: one 64-row block of the activations per slot (2-D tensor copy with
+//     128-byte swizzle, from L2);
+//   * A: four dequantised 128 x 64 weight tiles (128-byte-swizzled K-major rows).
+// Warp roles:
+//   warp 0      : code copies (one thread);
 //   warp 1      : TMEM allocator + the single MMA-issuing thread
-//                 (tcgen05.mma kind::f16, 4 x K=16 per block, commit per slot
-//                 to "empty" and per item to the accumulator's "full");
-//   warps 2..17 : dequant producers, two groups of 8 warps taking alternate
-//                 stages -- packed codes (smem) -> lop3 magic decode -> bf16
-//                 (q - z) * s -> 128-byte-swizzled K-major rows of the weight
-//                 tile; proxy fence; arrive;
-//   warps 18..21: epilogue (tcgen05.ld 32 lanes x 16 columns -> bf16 y, or
-//                 fp32 split-K reductions), one TMEM lane quadrant each.
-// mbarrier waits test only the parity of a phase, so every waiter must wait
-// for a barrier's uses in order: the groups take alternate stages, so the ring
-// depth is even (a slot's consecutive uses fall to the same group) and the
-// tile ring's depth (4) is too.
+//                 (tcgen05.mma kind::f16, 4 x K=16 per block);
+//   warp 2      : x copies (one thread);
+//   warps 4..7  : epilogue (tcgen05.ld, one TMEM lane quadrant each), through a
+//                 small transpose buffer in shared memory so that every thread
+//                 stores 16 bytes of bf16 y (or reduces four fp32 partial sums
+//                 with one vector reduction when K is split);
+//   warps 8..23 : dequant, two groups of 8 warps taking alternate 64-row blocks
+//                 (packed codes (smem) -> lop3 magic decode -> bf16 (q - z) * s
+//                 -> tile rows; proxy fence; arrive).
+// mbarrier waits test only the parity of a phase, so every waiter waits for a
+// barrier's uses in order: the A ring has four slots, two per dequant group
+// (block b uses slot b mod 4, and the groups take alternate blocks), every
+// group reads every code stage, and each of the other rings has one waiter.
 // Two TMEM accumulators alternate between items, so the epilogue of one item
-// overlaps the main loop of the next.
-// Every mbarrier wait is bounded; on expiry the kernel records
-// W4A16_ERR_TIMEOUT in the device status word, drains and returns.
+// overlaps the main loop of the next.  Every mbarrier wait is bounded; on
+// expiry the kernel records W4A16_ERR_TIMEOUT in the device status word,
+// drains and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,81 +62,121 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBlockK = 64;                  // K rows per pipeline stage
+constexpr int kBlockK = 64;                  // K rows per MMA block (4 x K=16)
 constexpr int kTileN = 128;                  // weight columns per tile (MMA M)
 constexpr int kASlots = 4;                   // ring of dequantised weight tiles
-constexpr int kMaxRawSlots = 32;             // ring of packed codes + x tiles
+constexpr int kMaxCodeSlots = 16;            // ring of packed-code stages (128 rows each)
+constexpr int kMaxXSlots = 16;               // ring of x blocks
 constexpr size_t kSmemBudget = 227 * 1024;
-constexpr int kDequantWarp0 = 2;
-constexpr int kDequantGroups = 2;            // groups of 8 warps take alternate stages
+constexpr int kCodeWarp = 0, kMmaWarp = 1, kXWarp = 2;
+constexpr int kEpilogueWarp0 = 4;            // 4..7: TMEM lane quadrant = warp % 4
+constexpr int kDequantWarp0 = 8;
+constexpr int kDequantGroups = 2;            // groups of 8 warps take alternate blocks
 constexpr int kDequantWarps = 8;             // warps per group (one weight tile each)
-constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;  // 18..21
-constexpr int kNumWarps = kEpilogueWarp0 + 4;
-constexpr int kThreads = 32 * kNumWarps;     // 704
+constexpr int kNumWarps = kDequantWarp0 + kDequantGroups * kDequantWarps;  // 24
+constexpr int kThreads = 32 * kNumWarps;     // 768
 constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
-constexpr uint32_t kRawBytes = kTileN * kBlockK / 2;     // 4 KB of packed codes
+constexpr uint32_t kStageCodeBytes = 2 * kTileN * kBlockK / 2;  // 8 KB: two blocks
+constexpr uint32_t kScaleRowBytes = kTileN * 2;          // 256
+constexpr uint32_t kZeroRowBytes = kTileN / 2;           // 64
+constexpr uint32_t kCodeSlotBytes = kStageCodeBytes + kScaleRowBytes + kZeroRowBytes + 64;  // 8576
+constexpr int kEpiRow = 36;                              // floats per transpose-buffer row (padded)
+constexpr uint32_t kEpiBufBytes = 4 * 16 * kEpiRow * 4;  // 16 rows x 32 columns fp32 per warp
 constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
+
+static_assert(kEpilogueWarp0 % 4 == 0, "TMEM lane quadrant of a warp is warp % 4");
+static_assert(kCodeSlotBytes % 128 == 0, "code slots stay 128-byte aligned");
 
 struct Args {
     const uint8_t* packed;
     const uint16_t* scales;
-    const uint32_t* zeros;
+    const uint32_t* zeros;  // padded zero-point rows after the codes
     uint16_t* y;
     float* partial;      // fp32 accumulator [B][N], zero between calls (split > 1)
     uint32_t* counters;
     unsigned int* status;
     int B, K, N;
     int bn;             // MMA N (batch rows per tile), multiple of 16
-    int kb_per_split;   // K blocks per split
+    int gps;            // 128-row groups per K split
     int split;
-    int nkb;            // total K blocks (K / 64)
+    int ngroups;        // K / 128
     int col_tiles, batch_tiles, items;
     uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= max(32, bn))
-    int raw_slots;      // depth of the codes + x ring
+    int code_slots, x_slots;
+    uint32_t x_slot_bytes;
+    uint32_t x_base, code_base, epi_base;  // shared-memory offsets of the rings
+    int zrow_words;     // words per padded zero-point row
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
-    Epilogue epi;          // fused output epilogue (plain bf16 when mode == 0)
+    Epilogue epi;       // fused output epilogue (plain bf16 when mode == 0)
 };
 
 // ------------------------------------------------------------ kernel
 
 struct SharedTail {
-    uint64_t raw_full[kMaxRawSlots];   // TMA bytes landed (codes + x)
-    uint64_t raw_empty[kMaxRawSlots];  // MMAs of the stage finished (commit)
-    uint64_t a_full[kASlots];          // weight tile dequantised (8 warp arrivals)
-    uint64_t a_empty[kASlots];         // MMAs reading the weight tile finished (commit)
-    uint64_t tmem_full[2];             // accumulator complete (commit)
-    uint64_t tmem_empty[2];            // accumulator drained by the epilogue (4 warps)
-    uint64_t never;                    // test hook: nobody arrives here
+    uint64_t code_full[kMaxCodeSlots];  // codes + scales (+ zero-points) of the stage landed
+    uint64_t code_free[kMaxCodeSlots];  // read by all 16 dequant warps
+    uint64_t x_full[kMaxXSlots];        // x block landed
+    uint64_t x_free[kMaxXSlots];        // MMAs reading it finished (commit)
+    uint64_t a_full[kASlots];           // weight tile dequantised (8 warp arrivals)
+    uint64_t a_free[kASlots];           // MMAs reading the weight tile finished (commit)
+    uint64_t tmem_full[2];              // accumulator complete (commit)
+    uint64_t tmem_empty[2];             // accumulator drained by the epilogue (4 warps)
+    uint64_t mma_done;                  // final drain of the issued MMAs
+    uint64_t never;                     // test hook: nobody arrives here
     uint32_t tmem_base;
     int abort;
+    int s_last;
 };
 
-// Shared memory: [kASlots weight tiles of 16 KB][raw_slots x (x tile bn*128 B,
-// packed codes 4 KB)][tail]; every operand tile starts on a 1024-byte boundary.
-__host__ __device__ constexpr uint32_t raw_slot_bytes(int bn) {
-    return (uint32_t)bn * kBlockK * 2 + kRawBytes;
-}
-
 struct Item {
-    int col_tile, batch_tile, split_idx, n0, b0, nvalid, kb_begin, nkb;
+    int col_tile, batch_tile, split_idx, n0, b0, nvalid, g_begin, ng;
 };
 
 __device__ __forceinline__ Item decode_item(const Args& a, int it) {
     Item t;
-    t.col_tile = it % a.col_tiles;
-    const int rest = it / a.col_tiles;
-    t.batch_tile = rest % a.batch_tiles;
-    t.split_idx = rest / a.batch_tiles;
+    t.batch_tile = it % a.batch_tiles;
+    const int rest = it / a.batch_tiles;
+    t.col_tile = rest % a.col_tiles;
+    t.split_idx = rest / a.col_tiles;
     t.n0 = t.col_tile * kTileN;
     t.b0 = t.batch_tile * a.bn;
     t.nvalid = min(kTileN, a.N - t.n0);
-    t.kb_begin = t.split_idx * a.kb_per_split;
-    t.nkb = min(a.kb_per_split, a.nkb - t.kb_begin);
+    t.g_begin = t.split_idx * a.gps;
+    t.ng = min(a.gps, a.ngroups - t.g_begin);
     return t;
 }
 
+// Ring position (slot, parity of the slot's current use), stepped without
+// divisions.
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ void epilogue_bar() {  // the 4 epilogue warps only
     asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+// The packed codes, scale row and zero-point row of group g of item t.
+template <bool kHasZeros>
+__device__ __forceinline__ void issue_code_stage(const Args& a, const Item& t, int g,
+                                                 uint8_t* slot, uint32_t bar) {
+    const uint32_t cb = 4u * (uint32_t)t.nvalid * 16u;      // 4 chunks of 32 rows
+    const uint32_t sb = (uint32_t)t.nvalid * 2u;            // multiple of 16 (N % 8 == 0)
+    const uint32_t zb = kHasZeros ? (((uint32_t)t.nvalid / 2u + 15u) & ~15u) : 0u;
+    mbar_arrive_expect_tx(bar, cb + sb + zb);
+    bulk_g2s(smem_u32(slot), a.packed + packed_tile_base(a.K, t.col_tile) +
+                                 (size_t)(4 * g) * t.nvalid * 16, cb, bar);
+    bulk_g2s(smem_u32(slot + kStageCodeBytes), a.scales + (size_t)g * a.N + t.n0, sb, bar);
+    if (kHasZeros)
+        bulk_g2s(smem_u32(slot + kStageCodeBytes + kScaleRowBytes),
+                 a.zeros + (size_t)g * a.zrow_words + t.n0 / 8, zb, bar);
 }
 
 template <bool kHasZeros, bool kFused>
@@ -141,38 +185,42 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const int R = a.raw_slots;
-    const uint32_t rbytes = raw_slot_bytes(a.bn);
-    uint8_t* raw_base = smem + kASlots * kATileBytes;
-    SharedTail* tail = reinterpret_cast<SharedTail*>(raw_base + R * rbytes);
+    const int RC = a.code_slots;
+    const int RX = a.x_slots;
+    SharedTail* tail = reinterpret_cast<SharedTail*>(smem + a.epi_base + kEpiBufBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = &tail->abort;
 
     auto a_tile = [&](int sa) { return smem + sa * kATileBytes; };
-    auto x_tile = [&](int s) { return raw_base + s * rbytes; };
-    auto raw_tile = [&](int s) { return raw_base + s * rbytes + a.bn * kBlockK * 2; };
+    auto x_tile = [&](int s) { return smem + a.x_base + (size_t)s * a.x_slot_bytes; };
+    auto code_slot = [&](int s) { return smem + a.code_base + (size_t)s * kCodeSlotBytes; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < R; ++s) {
-            mbar_init(smem_u32(&tail->raw_full[s]), 1);
-            mbar_init(smem_u32(&tail->raw_empty[s]), 1);
+        for (int s = 0; s < RC; ++s) {
+            mbar_init(smem_u32(&tail->code_full[s]), 1);
+            mbar_init(smem_u32(&tail->code_free[s]), kDequantGroups * kDequantWarps);
+        }
+        for (int s = 0; s < RX; ++s) {
+            mbar_init(smem_u32(&tail->x_full[s]), 1);
+            mbar_init(smem_u32(&tail->x_free[s]), 1);
         }
         for (int s = 0; s < kASlots; ++s) {
             mbar_init(smem_u32(&tail->a_full[s]), kDequantWarps);
-            mbar_init(smem_u32(&tail->a_empty[s]), 1);
+            mbar_init(smem_u32(&tail->a_free[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tail->tmem_full[b]), 1);
             mbar_init(smem_u32(&tail->tmem_empty[b]), 4);
         }
+        mbar_init(smem_u32(&tail->mma_done), 1);
         mbar_init(smem_u32(&tail->never), 1);
         tail->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(&tail->tmem_base)), "r"(2 * a.acc_cols)
                      : "memory");
@@ -182,68 +230,69 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tail->tmem_base;
-    // The next kernel on the stream may start now.  This one writes y and the
-    // workspace, and reads x, only after the previous kernel has finished: the
-    // TMA thread waits before its first x copy, and everything else is ordered
-    // after that through mbarriers.  The packed codes do not depend on the
-    // previous kernel, so the first stages' code copies go out before.
+    // The next kernel on the stream may start now.  This one reads x, and
+    // writes y and the workspace, only after the previous kernel has finished:
+    // the x thread waits before its first copy, and everything else that
+    // touches x, y or the workspace is ordered after that through mbarriers.
+    // The packed weights do not depend on the previous kernel (weights are
+    // written by kernels that do not trigger early launches), so the code ring
+    // starts filling at once.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        // ---------------- TMA producer
+    if (warp == kCodeWarp) {
+        // ---------------- code stages: one per 128-row group
         if (lane == 0) {
-            const uint32_t xbytes = (uint32_t)a.bn * kBlockK * 2;
-            const Item first = decode_item(a, blockIdx.x);
-            const int pre = min(R, first.nkb);
-            for (int i = 0; i < pre; ++i) {
-                const uint32_t bar = smem_u32(&tail->raw_full[i]);
-                const uint32_t cb = 2u * (uint32_t)first.nvalid * 16;  // two 32-row chunks
-                mbar_arrive_expect_tx(bar, cb + xbytes);
-                bulk_g2s(smem_u32(raw_tile(i)),
-                         a.packed + packed_tile_base(a.K, first.col_tile) +
-                             (size_t)(2 * (first.kb_begin + i)) * first.nvalid * 16,
-                         cb, bar);
-            }
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            int stage = 0, issued = 0;
+            Ring q;
+            int issued = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
                 const Item t = decode_item(a, it);
-                const uint32_t cb = 2u * (uint32_t)t.nvalid * 16;
-                const uint8_t* tile_codes = a.packed + packed_tile_base(a.K, t.col_tile);
-                for (int i = 0; i < t.nkb; ++i, ++stage) {
-                    const int s = stage % R;
-                    const uint32_t bar = smem_u32(&tail->raw_full[s]);
-                    const int kb = t.kb_begin + i;
-                    if (stage >= pre) {
-                        if (stage >= R &&
-                            !wait_bounded(smem_u32(&tail->raw_empty[s]), ((stage / R) - 1) & 1,
-                                          abort, a.status, kTimeoutNs)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(bar, cb + xbytes);
-                        bulk_g2s(smem_u32(raw_tile(s)), tile_codes + (size_t)(2 * kb) * t.nvalid * 16,
-                                 cb, bar);
+                for (int c = 0; c < t.ng; ++c, ++issued, q.next(RC)) {
+                    if (issued >= RC &&
+                        !wait_fast(smem_u32(&tail->code_free[q.s]), q.ph ^ 1u, abort, a.status,
+                                   kTimeoutNs)) {
+                        ok = false;
+                        break;
                     }
-                    tma_load_2d(smem_u32(x_tile(s)), &xmap, kb * kBlockK, t.b0, bar);
-                    issued = stage + 1;
+                    issue_code_stage<kHasZeros>(a, t, t.g_begin + c, code_slot(q.s),
+                                                smem_u32(&tail->code_full[q.s]));
                 }
             }
             // After an expired wait, every copy in flight must land before the
-            // CTA exits; stages whose code copy went out early still need their
-            // x copy for the barrier to complete.
-            if (!ok) {
-                for (int i = issued; i < pre; ++i)
-                    tma_load_2d(smem_u32(x_tile(i)), &xmap, (first.kb_begin + i) * kBlockK, first.b0,
-                                smem_u32(&tail->raw_full[i]));
-                const int last = max(issued, pre);
-                for (int i = max(0, last - R); i < last; ++i)
-                    wait_bounded(smem_u32(&tail->raw_full[i % R]), (i / R) & 1, abort, a.status,
-                                 kTimeoutNs);
-            }
+            // CTA exits: wait for the latest use of every slot.
+            if (!ok)
+                for (int i = max(0, issued - RC); i < issued; ++i)
+                    wait_bounded(smem_u32(&tail->code_full[i % RC]), (i / RC) & 1, abort,
+                                 a.status, kTimeoutNs);
         }
-    } else if (warp == 1) {
+    } else if (warp == kXWarp) {
+        // ---------------- x blocks
+        if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            Ring q;
+            int issued = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
+                const Item t = decode_item(a, it);
+                const int kb0 = 2 * t.g_begin;
+                for (int i = 0; i < 2 * t.ng; ++i, ++issued, q.next(RX)) {
+                    if (issued >= RX &&
+                        !wait_fast(smem_u32(&tail->x_free[q.s]), q.ph ^ 1u, abort, a.status,
+                                   kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_u32(&tail->x_full[q.s]);
+                    mbar_arrive_expect_tx(bar, a.x_slot_bytes);
+                    tma_load_2d(smem_u32(x_tile(q.s)), &xmap, (kb0 + i) * kBlockK, t.b0, bar);
+                }
+            }
+            if (!ok)
+                for (int i = max(0, issued - RX); i < issued; ++i)
+                    wait_bounded(smem_u32(&tail->x_full[i % RX]), (i / RX) & 1, abort, a.status,
+                                 kTimeoutNs);
+        }
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = instr_desc_bf16(kTileN, a.bn);
@@ -251,7 +300,9 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             if (a.force_timeout)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
                                   (unsigned long long)a.force_timeout * 1000000ull);
-            int stage = 0, j = 0;
+            Ring qx;
+            int gb = 0;  // blocks walked (block gb uses A slot gb % 4)
+            int j = 0;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x, ++j) {
                 const Item t = decode_item(a, it);
                 const int acc = j & 1;
@@ -262,26 +313,26 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 }
                 tc_fence_after();
                 const uint32_t tmem_d = tmem_base + acc * a.acc_cols;
-                for (int i = 0; i < t.nkb; ++i, ++stage) {
-                    const int s = stage % R;
-                    const int sa = stage % kASlots;
-                    if (!wait_fast(smem_u32(&tail->raw_full[s]), (stage / R) & 1, abort, a.status,
+                for (int i = 0; i < 2 * t.ng; ++i, ++gb, qx.next(RX)) {
+                    const int sa = gb & (kASlots - 1);
+                    if (!wait_fast(smem_u32(&tail->x_full[qx.s]), qx.ph, abort, a.status,
                                    kTimeoutNs) ||
-                        !wait_fast(smem_u32(&tail->a_full[sa]), (stage / kASlots) & 1, abort,
+                        !wait_fast(smem_u32(&tail->a_full[sa]), (uint32_t)(gb >> 2) & 1u, abort,
                                    a.status, kTimeoutNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t abase = smem_u32(a_tile(sa));
-                    const uint32_t xbase = smem_u32(x_tile(s));
+                    const uint32_t xbase = smem_u32(x_tile(qx.s));
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk)
                         mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
                                     smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
-                    mma_commit(smem_u32(&tail->a_empty[sa]));
-                    mma_commit(smem_u32(&tail->raw_empty[s]));
+                    mma_commit(smem_u32(&tail->a_free[sa]));
+                    mma_commit(smem_u32(&tail->x_free[qx.s]));
                 }
+                if (!ok) break;
                 mma_commit(smem_u32(&tail->tmem_full[acc]));  // fires once this item's MMAs are done
             }
             if (!ok) {
@@ -290,39 +341,50 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 mma_commit(smem_u32(&tail->tmem_full[0]));
                 mma_commit(smem_u32(&tail->tmem_full[1]));
             }
+            // every issued MMA has finished before TMEM is released, also after
+            // an abort (issued MMAs wait on nothing, so this wait is short)
+            mma_commit(smem_u32(&tail->mma_done));
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&tail->mma_done), 0) && globaltimer() - t0 < kTimeoutNs) {
+            }
         }
-    } else if (warp < kEpilogueWarp0) {
-        // ---------------- dequant producers (warps 2..17): two groups of 8 warps
-        // take alternate stages, so two weight tiles are decoded at a time
+    } else if (warp >= kDequantWarp0) {
+        // ---------------- dequant (warps 8..23): group grp takes blocks grp,
+        // grp + 2, ... -- block grp of every code stage -- into A slots
+        // grp and grp + 2 in turn
         const int dw = warp - kDequantWarp0;
-        const int grp = dw / kDequantWarps;                  // stage parity handled
-        const int t256 = (dw % kDequantWarps) * 32 + lane;   // 0..255 within the group
-        const int r = t256 & (kTileN - 1);                   // weight column within the tile
-        const int h = t256 >> 7;                             // which 32-row chunk of the block
-        int stage = 0;
+        const int grp = dw / kDequantWarps;
+        const int t256 = (dw % kDequantWarps) * 32 + lane;  // 0..255 within the group
+        const int r = t256 & (kTileN - 1);                  // weight column within the tile
+        const int h = t256 >> 7;                            // which 32-row chunk of the block
+        Ring q;
+        int own = 0;  // blocks of this group so far
         bool ok = true;
         for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
             const Item t = decode_item(a, it);
-            const int n = min(t.n0 + r, a.N - 1);
-            for (int i = 0; i < t.nkb; ++i, ++stage) {
-                if ((stage & 1) != grp) continue;
-                const int s = stage % R;
-                const int sa = stage % kASlots;
-                const int g = (t.kb_begin + i) >> 1;  // two 64-row blocks per group of 128
-                const uint32_t s2 = scale_pair(__ldg(a.scales + (size_t)g * a.N + n));
-                const uint32_t z2 = kHasZeros ? zero_pair(load_zero(a.zeros, a.N, g, n))
-                                              : kSymmetricZeroPair;
-                bool landed = wait_fast(smem_u32(&tail->raw_full[s]), (stage / R) & 1, abort,
-                                        a.status, kTimeoutNs);
-                if (landed && stage >= kASlots)
-                    landed = wait_fast(smem_u32(&tail->a_empty[sa]), ((stage / kASlots) - 1) & 1,
+            const int rr = min(r, t.nvalid - 1);  // lanes past a ragged edge repeat a column
+            for (int c = 0; c < t.ng; ++c, ++own, q.next(RC)) {
+                const int sa = grp + 2 * (own & 1);
+                bool landed = wait_fast(smem_u32(&tail->code_full[q.s]), q.ph, abort, a.status,
+                                        kTimeoutNs);
+                if (landed && own >= 2)
+                    landed = wait_fast(smem_u32(&tail->a_free[sa]), (uint32_t)((own >> 1) - 1) & 1u,
                                        abort, a.status, kTimeoutNs);
                 if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
                     ok = false;
                     break;
                 }
-                const uint4 q = reinterpret_cast<const uint4*>(raw_tile(s))[h * t.nvalid + min(r, t.nvalid - 1)];
-                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                const uint8_t* slot = code_slot(q.s);
+                const uint4 qw = reinterpret_cast<const uint4*>(slot)[(2 * grp + h) * t.nvalid + rr];
+                const uint32_t s2 = scale_pair(
+                    reinterpret_cast<const uint16_t*>(slot + kStageCodeBytes)[rr]);
+                uint32_t z2 = kSymmetricZeroPair;
+                if (kHasZeros) {
+                    const uint32_t zw = reinterpret_cast<const uint32_t*>(
+                        slot + kStageCodeBytes + kScaleRowBytes)[rr >> 3];
+                    z2 = zero_pair((zw >> (4 * (rr & 7))) & 0xFu);
+                }
+                const uint32_t words[4] = {qw.x, qw.y, qw.z, qw.w};
                 uint8_t* row = a_tile(sa) + r * 128;
 #pragma unroll
                 for (int jw = 0; jw < 4; ++jw) {
@@ -333,12 +395,16 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&tail->a_full[sa]));
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&tail->a_full[sa]));
+                    mbar_arrive(smem_u32(&tail->code_free[q.s]));
+                }
             }
         }
-    } else {
-        // ---------------- epilogue (warps 10..13; TMEM lane quadrant = warp % 4)
+    } else if (warp >= kEpilogueWarp0) {
+        // ---------------- epilogue (warps 4..7; TMEM lane quadrant = warp % 4)
         const int quad = warp & 3;
+        float* buf = reinterpret_cast<float*>(smem + a.epi_base) + quad * 16 * kEpiRow;
         int j = 0;
         for (int it = blockIdx.x; it < a.items; it += gridDim.x, ++j) {
             const Item t = decode_item(a, it);
@@ -348,33 +414,56 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             tc_fence_after();
             const bool live = __all_sync(0xffffffffu, done && !*abort);
             if (live) {  // tcgen05.ld is warp-collective
-                const int nn = t.n0 + quad * 32 + lane;
+                const int nq = t.n0 + quad * 32;  // this warp's 32 columns
                 const uint32_t taddr = tmem_base + acc * a.acc_cols + ((uint32_t)(quad * 32) << 16);
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
                     tmem_ld_16(taddr + c0, v);
-                    if (kFused && a.split == 1) {
-                        // fused epilogue; b is the same in every lane (the
-                        // SiLU form pairs lanes)
+                    // transpose through shared memory: row i of the chunk, 32 columns
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int b = t.b0 + c0 + jj;
-                            if (b < a.B) epi_store_lane_fused(a.y, a.N, b, nn, v[jj], nn < a.N, a.epi);
-                        }
-                    } else if (nn < a.N) {
+                    for (int i = 0; i < 16; ++i) buf[i * kEpiRow + lane] = v[i];
+                    __syncwarp();
+                    if (a.split == 1) {
+                        // 8 consecutive columns of one row per thread
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int b = t.b0 + c0 + jj;
-                            if (b < a.B) {
-                                if (a.split == 1)
-                                    a.y[(size_t)b * a.N + nn] = (uint16_t)epi_f32_to_bf16(v[jj]);
-                                else
-                                    asm volatile("red.global.add.f32 [%0], %1;"
-                                                 ::"l"(a.partial + (size_t)b * a.N + nn), "f"(v[jj])
-                                                 : "memory");
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int i = 8 * rr + (lane >> 2);
+                            const int c8 = 8 * (lane & 3);
+                            const int b = t.b0 + c0 + i;
+                            const int n = nq + c8;
+                            const float4 lo = *reinterpret_cast<const float4*>(buf + i * kEpiRow + c8);
+                            const float4 hi =
+                                *reinterpret_cast<const float4*>(buf + i * kEpiRow + c8 + 4);
+                            if (b < a.B && n < a.N) {
+                                if constexpr (kFused) {
+                                    epi_store4_fused(a.y, a.N, b, n, lo.x, lo.y, lo.z, lo.w, a.epi);
+                                    epi_store4_fused(a.y, a.N, b, n + 4, hi.x, hi.y, hi.z, hi.w, a.epi);
+                                } else {
+                                    *reinterpret_cast<uint4*>(a.y + (size_t)b * a.N + n) = make_uint4(
+                                        epi_f32_to_bf16(lo.x) | (epi_f32_to_bf16(lo.y) << 16),
+                                        epi_f32_to_bf16(lo.z) | (epi_f32_to_bf16(lo.w) << 16),
+                                        epi_f32_to_bf16(hi.x) | (epi_f32_to_bf16(hi.y) << 16),
+                                        epi_f32_to_bf16(hi.z) | (epi_f32_to_bf16(hi.w) << 16));
+                                }
                             }
                         }
+                    } else {
+                        // 4 consecutive columns of one row per thread: one vector reduction
+#pragma unroll
+                        for (int rr = 0; rr < 4; ++rr) {
+                            const int i = 4 * rr + (lane >> 3);
+                            const int c4 = 4 * (lane & 7);
+                            const int b = t.b0 + c0 + i;
+                            const int n = nq + c4;
+                            const float4 p = *reinterpret_cast<const float4*>(buf + i * kEpiRow + c4);
+                            if (b < a.B && n < a.N)
+                                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                                             ::"l"(a.partial + (size_t)b * a.N + n), "f"(p.x),
+                                             "f"(p.y), "f"(p.z), "f"(p.w)
+                                             : "memory");
+                        }
                     }
+                    __syncwarp();  // the buffer is rewritten by the next chunk
                 }
             }
             tc_fence_before();
@@ -387,17 +476,16 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 __threadfence();
                 epilogue_bar();
                 uint32_t* counter = a.counters + (size_t)t.batch_tile * a.col_tiles + t.col_tile;
-                __shared__ int s_last;
                 if (warp == kEpilogueWarp0 && lane == 0) {
                     uint32_t prev;
                     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
                                  : "=r"(prev)
                                  : "l"(counter)
                                  : "memory");
-                    s_last = (prev == (uint32_t)(a.split - 1));
+                    tail->s_last = (prev == (uint32_t)(a.split - 1));
                 }
                 epilogue_bar();
-                if (s_last) {
+                if (tail->s_last) {
                     __threadfence();
                     // 4 columns per thread and 8 loads in flight: the sums come
                     // back from L2, so latency, not bandwidth, sets the pace
@@ -408,26 +496,26 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     for (int e0 = et; e0 < total; e0 += 128 * 8) {
                         float4 v[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int e = e0 + 128 * j;
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int e = e0 + 128 * jj;
                             if (e < total) {
-                                const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
-                                v[j] = __ldcg(reinterpret_cast<const float4*>(
+                                const int rr = e / c4n, cc = 4 * (e - rr * c4n);
+                                v[jj] = __ldcg(reinterpret_cast<const float4*>(
                                     a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
                             }
                         }
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int e = e0 + 128 * j;
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int e = e0 + 128 * jj;
                             if (e < total) {
-                                const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
+                                const int rr = e / c4n, cc = 4 * (e - rr * c4n);
                                 const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
                                 if constexpr (kFused)
-                                    epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[j].x, v[j].y,
-                                           v[j].z, v[j].w, a.epi);
+                                    epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x,
+                                                     v[jj].y, v[jj].z, v[jj].w, a.epi);
                                 else
-                                    epi_store4_plain(a.y, a.N, t.b0 + rr, t.n0 + cc, v[j].x, v[j].y,
-                                           v[j].z, v[j].w, a.epi);
+                                    epi_store4_plain(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x,
+                                                     v[jj].y, v[jj].z, v[jj].w, a.epi);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
                             }
@@ -440,8 +528,9 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         }
     }
 
+    tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(2 * a.acc_cols)
@@ -470,16 +559,34 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Even: the two dequant groups take alternate stages, so a slot's consecutive
-// uses fall to the same group.
-int raw_slots_for(int bn) {
-    const size_t avail = kSmemBudget - 1024 - sizeof(SharedTail) - (size_t)kASlots * kATileBytes;
-    return (int)std::min<size_t>(kMaxRawSlots, avail / raw_slot_bytes(bn)) & ~1;
-}
+// Shared memory: [A ring: 4 x 16 KB][x ring][code ring][epilogue buffer][tail]
+// (+ 1 KB of alignment slack).  The x ring takes what the code ring leaves,
+// with at least 3 slots; the code ring is as deep as the rest allows.
+struct WideLayout {
+    int x_slots, code_slots;
+    uint32_t x_slot_bytes, x_base, code_base, epi_base;
+    size_t smem;
+};
 
-size_t smem_bytes(int bn) {
-    return (size_t)kASlots * kATileBytes + (size_t)raw_slots_for(bn) * raw_slot_bytes(bn) +
-           sizeof(SharedTail) + 1024;
+WideLayout wide_layout(int bn) {
+    WideLayout l;
+    l.x_slot_bytes = (uint32_t)bn * kBlockK * 2;  // multiple of 1024 (bn % 8 == 0)
+    const size_t fixed = 1024 + (size_t)kASlots * kATileBytes + kEpiBufBytes + sizeof(SharedTail);
+    const size_t avail = kSmemBudget - fixed;
+    // six code stages (twelve blocks ahead of the tensor pipe: the weights
+    // come from HBM), then as many x slots as fit (3 .. 6: x comes from L2),
+    // then the rest to the code ring
+    const size_t want_code = 6 * (size_t)kCodeSlotBytes;
+    int xs = avail > want_code ? (int)((avail - want_code) / l.x_slot_bytes) : 0;
+    xs = std::max(3, std::min(6, xs));
+    const size_t left = avail > (size_t)xs * l.x_slot_bytes ? avail - (size_t)xs * l.x_slot_bytes : 0;
+    l.code_slots = (int)std::min<size_t>(kMaxCodeSlots, left / kCodeSlotBytes);
+    l.x_slots = xs;
+    l.x_base = (uint32_t)kASlots * kATileBytes;
+    l.code_base = l.x_base + (uint32_t)xs * l.x_slot_bytes;
+    l.epi_base = l.code_base + (uint32_t)l.code_slots * kCodeSlotBytes;
+    l.smem = 1024 + (size_t)l.epi_base + kEpiBufBytes + sizeof(SharedTail);
+    return l;
 }
 
 uint32_t acc_cols_for(int bn) {
@@ -490,36 +597,56 @@ uint32_t acc_cols_for(int bn) {
 
 }  // namespace
 
+// Work decomposition for batches above 128 rows.  A work item is one
+// 128-column tile of W for one batch tile of bn rows, over a range of whole
+// 128-row groups of K; persistent CTAs (one per SM) take items round robin.
+// The choice trades three costs, estimated in SM cycles per CTA:
+//   * tensor pipe: 4 MMAs of M = 128, N = bn, K = 16 per 64-row block, about
+//     bn / 2 cycles each;
+//   * dequantisation: every weight tile is decoded once per batch tile, about
+//     200 cycles per block at the CUDA cores' rate -- the block takes the
+//     longer of the two;
+//   * K split: partial sums are added into an fp32 accumulator with vector
+//     reductions (bn x 128 floats per item) and converted by the last item of
+//     the tile, a few thousand cycles per item.
+// Every CTA runs ceil(items / SMs) items, so the decomposition that gives the
+// busiest CTA the least work wins.
 TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
-    TcPlan p{};
-    p.batch_tiles = (B + 255) / 256;
-    const int per = (B + p.batch_tiles - 1) / p.batch_tiles;
-    p.bn = std::min(256, (per + 15) / 16 * 16);
-    p.col_tiles = (N + kTileN - 1) / kTileN;
-    const int nkb = K / kBlockK;
-    const long long tiles = (long long)p.col_tiles * p.batch_tiles;
-    // persistent CTAs (one per SM) take items round robin; choose the K split
-    // minimising the busiest CTA's K blocks plus a fixed cost per item and a
-    // small cost per split (accumulator traffic)
-    double best = 1e300;
-    int best_split = 1, best_kbps = nkb;
-    for (int split = 1; split <= std::min(16, nkb); ++split) {
-        const int kbps = (nkb + split - 1) / split;
-        if (split > 1 && (kbps < 8 || tiles > kMaxCounters)) break;
-        const int s = (nkb + kbps - 1) / kbps;
-        const long long items = tiles * s;
-        const long long per_cta = (items + num_sms - 1) / num_sms;
-        const double cost = (double)per_cta * (kbps + 4) * (1.0 + 0.02 * (s - 1));
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_split = s;
-            best_kbps = kbps;
+    TcPlan best{};
+    double best_cost = 1e300;
+    const int G = K / kGroup;
+    const int col_tiles = (N + kTileN - 1) / kTileN;
+    const int min_bt = (B + 255) / 256;
+    for (int bt = min_bt; bt <= min_bt + 6; ++bt) {
+        const int per = (B + bt - 1) / bt;
+        const int bn = std::min(256, (per + 15) / 16 * 16);
+        if (bn < 32 && bt > min_bt) break;
+        const int batch_tiles = (B + bn - 1) / bn;
+        const long long tiles = (long long)col_tiles * batch_tiles;
+        const double block = std::max(2.0 * bn, 200.0) + 40.0;
+        for (int split = 1; split <= std::min(16, G); ++split) {
+            const int gps = (G + split - 1) / split;
+            const int s = (G + gps - 1) / gps;  // no empty splits
+            if (s != split) continue;
+            if (s > 1 && tiles > kMaxCounters - 2) break;
+            const long long items = tiles * s;
+            const long long per_cta = (items + num_sms - 1) / num_sms;
+            const double item = 2.0 * gps * block + 1500.0 + (s > 1 ? 12.0 * bn + 3000.0 : 0.0);
+            const double cost = (double)per_cta * item;
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.bn = bn;
+                best.batch_tiles = batch_tiles;
+                best.split = s;
+                best.kb_per_split = 2 * gps;
+            }
         }
     }
-    p.split = best_split;
-    p.kb_per_split = best_kbps;
-    p.grid = (int)std::min<long long>(tiles * p.split, num_sms);
-    return p;
+    best.col_tiles = col_tiles;
+    best.grid = (int)std::min<long long>((long long)col_tiles * best.batch_tiles * best.split,
+                                         num_sms);
+    best.wide = true;
+    return best;
 }
 
 static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
@@ -538,6 +665,9 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
+    const WideLayout lay = wide_layout(p.bn);
+    if (lay.x_slots < 3 || lay.code_slots < 2 || lay.smem > kSmemBudget)
+        return cudaErrorInvalidConfiguration;
     Args a;
     a.packed = static_cast<const uint8_t*>(packed);
     a.scales = static_cast<const uint16_t*>(scales);
@@ -551,18 +681,24 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.K = K;
     a.N = N;
     a.bn = p.bn;
-    a.kb_per_split = p.kb_per_split;
+    a.gps = p.kb_per_split / 2;
     a.split = p.split;
-    a.nkb = K / kBlockK;
+    a.ngroups = K / kGroup;
     a.col_tiles = p.col_tiles;
     a.batch_tiles = p.batch_tiles;
     a.items = p.col_tiles * p.batch_tiles * p.split;
     a.acc_cols = acc_cols_for(p.bn);
-    a.raw_slots = raw_slots_for(p.bn);
+    a.code_slots = lay.code_slots;
+    a.x_slots = lay.x_slots;
+    a.x_slot_bytes = lay.x_slot_bytes;
+    a.x_base = lay.x_base;
+    a.code_base = lay.code_base;
+    a.epi_base = lay.epi_base;
+    a.zrow_words = packed_zero_row_words(N);
     a.force_timeout = force_timeout_ms;
     a.epi = epi;
 
-    const size_t smem = smem_bytes(p.bn);
+    const size_t smem = lay.smem;
     const bool fused = epi.mode != 0;
     const void* kern =
         has_zeros ? (fused ? reinterpret_cast<const void*>(wide_kernel<true, true>)
