@@ -47,6 +47,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-suspending test of a phase (acquire, CTA scope): cheaper than try_wait
+// when the phase is usually complete already.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: true when the phase with this parity completed; false when the
 // CTA is aborting (another wait expired) or this wait expired (then it sets
 // the abort flag and the device status word).
@@ -63,6 +77,15 @@ __device__ __noinline__ inline bool wait_bounded(uint32_t bar, uint32_t parity,
             return false;
         }
     }
+}
+
+// As wait_fast, testing the phase without suspending first (for a thread on
+// the critical path whose barrier is usually complete when it gets there).
+__device__ __forceinline__ bool wait_test_first(uint32_t bar, uint32_t parity,
+                                                volatile int* abort, unsigned int* status,
+                                                unsigned long long limit_ns = 2000000000ull) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, abort, status, limit_ns);
 }
 
 // Inline fast path: one try_wait, the bounded loop only if the phase is not

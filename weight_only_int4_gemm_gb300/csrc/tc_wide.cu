@@ -1,5 +1,6 @@
 // tc_wide.cu -- W4A16 GEMM on the tcgen05 tensor cores for wide batches
-// (more than 128 rows of x), with the dequantised weight tile in shared memory.
+// (more than 64 rows of x), one MMA-issuing thread, the dequantised weight
+// tile in tensor memory.
 //
 // "Give Me BF16 or Give Me Death" (summary), "Inference with W4A16": the
 // 4-bit weights are rebuilt to 16-bit values inside the matrix
@@ -12,40 +13,53 @@
 //
 // Tile (operands swapped so the weight tile is the 128-row MMA operand):
 //   D[128 weight columns][bn batch rows] (fp32, TMEM)
-//     += W^T[128][64 k] (bf16, smem, dequantised by producer warps)
+//     += W^T[128][64 k] (bf16, TMEM: lane = weight column, 32-bit column j =
+//                        the k pair (2j, 2j+1), written by the dequant warps
+//                        with tcgen05.st)
 //      . X^T[64 k][bn]  (bf16, smem, TMA from x[B][K])
+// The tile lives in tensor memory: through shared memory its store and its
+// operand read would add a third to the shared-memory traffic of a block
+// (the x copy, the tensor core's x reads, the code copies), and the shared
+// memory goes to deeper rings instead.  A block is 128 rows of K (one scale
+// group, 8 MMAs of K = 16): the MMA-issuing thread's per-block waits and
+// commits cost about as much as 4 short MMAs, so longer blocks keep more of
+// its time on MMAs.
 // Persistent CTAs (one per SM) take work items (batch tile, column tile, K
 // split; the batch tile varies fastest, so the batch tiles of one weight tile
 // run side by side and its second reading comes from L2) round robin.  Three
 // rings keep the tensor pipe fed:
-//   * codes: one stage per 128-row group of the item (the packed codes of two
-//     64-row blocks, 8 KB, one bulk copy; the group's scale row and, for the
-//     asymmetric format, zero-point row, two more bulk copies).  The weights
-//     come from HBM, so this ring runs furthest ahead; the dequant warps read
-//     scales from it and never wait on a global load;
-//   * x: one 64-row block of the activations per slot (2-D tensor copy with
-//     128-byte swizzle, from L2);
-//   * A: four dequantised 128 x 64 weight tiles (128-byte-swizzled K-major rows).
+//   * codes: one stage per block (its packed codes, 8 KB, one bulk copy; the
+//     group's scale row and, for the asymmetric format, zero-point row, two
+//     more bulk copies).  The weights come from HBM, so this ring runs
+//     furthest ahead; the dequant warps read scales from it and never wait on
+//     a global load;
+//   * x: the block's activations per slot (two 2-D tensor copies of 64 K
+//     rows, 128-byte swizzle, from L2);
+//   * A: dequantised 128 x 128 weight tiles in TMEM, 64 columns each (4 to 8,
+//     what the accumulators leave of the 512 columns).
 // Warp roles:
 //   warp 0      : code copies (one thread);
-//   warp 1      : TMEM allocator + the single MMA-issuing thread
-//                 (tcgen05.mma kind::f16, 4 x K=16 per block);
-//   warp 2      : x copies (one thread);
+//   warp 1      : x copies (one thread);
+//   warp 3      : TMEM allocator + the single MMA-issuing thread
+//                 (tcgen05.mma kind::f16, A from TMEM, 8 x K=16 per block);
 //   warps 4..7  : epilogue (tcgen05.ld, one TMEM lane quadrant each), through a
 //                 small transpose buffer in shared memory so that every thread
 //                 stores 16 bytes of bf16 y (or reduces four fp32 partial sums
 //                 with one vector reduction when K is split);
-//   warps 8..23 : dequant, two groups of 8 warps taking alternate 64-row blocks
-//                 (packed codes (smem) -> lop3 magic decode -> bf16 (q - z) * s
-//                 -> tile rows; proxy fence; arrive).
+//   warps 8..15 : dequant, two groups of four warps (one per TMEM lane
+//                 quadrant) taking blocks in turn: each thread decodes the 128
+//                 codes of its weight column (lop3 magic decode -> bf16
+//                 (q - z) * s) and stores them to its TMEM lane.
 // mbarrier waits test only the parity of a phase, so every waiter waits for a
-// barrier's uses in order: the A ring has four slots, two per dequant group
-// (block b uses slot b mod 4, and the groups take alternate blocks), every
-// group reads every code stage, and each of the other rings has one waiter.
-// Two TMEM accumulators alternate between items, so the epilogue of one item
-// overlaps the main loop of the next.  Every mbarrier wait is bounded; on
-// expiry the kernel records W4A16_ERR_TIMEOUT in the device status word,
-// drains and returns.
+// barrier's uses in order: block b uses code slot b mod RC, A slot b mod SA
+// and x slot b mod RX, all three even, and the two dequant groups take
+// alternate blocks, so every slot always serves one group; the MMA thread
+// waits once per block (a block's tile is announced only once its x has
+// landed too) and commits twice (the A slot, the x slot).  Two TMEM
+// accumulators alternate between items when TMEM has room for them
+// (bn <= 128), so the epilogue of one item overlaps the main loop of the next.
+// Every mbarrier wait is bounded; on expiry the kernel records
+// W4A16_ERR_TIMEOUT in the device status word, drains and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -62,21 +76,24 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBlockK = 64;                  // K rows per MMA block (4 x K=16)
+constexpr int kGroupK = 128;                 // K rows per code stage (one scale group)
+constexpr int kSubK = 64;                    // K rows per sub-block (4 MMAs of K = 16; one
+                                             // 128-byte-swizzled x sub-tile, 32 TMEM columns)
 constexpr int kTileN = 128;                  // weight columns per tile (MMA M)
-constexpr int kASlots = 4;                   // ring of dequantised weight tiles
+constexpr int kMaxASlots = 8;                // ring of dequantised weight tiles (TMEM)
+constexpr int kSubCols = kSubK / 2;          // TMEM columns per weight sub-tile (32)
+constexpr int kTmemCols = 512;               // all of TMEM (one CTA per SM)
 constexpr int kMaxCodeSlots = 16;            // ring of packed-code stages (128 rows each)
 constexpr int kMaxXSlots = 16;               // ring of x blocks
 constexpr size_t kSmemBudget = 227 * 1024;
-constexpr int kCodeWarp = 0, kMmaWarp = 1, kXWarp = 2;
+constexpr int kCodeWarp = 0, kXWarp = 1, kMmaWarp = 3;  // warp 2 has no role
 constexpr int kEpilogueWarp0 = 4;            // 4..7: TMEM lane quadrant = warp % 4
-constexpr int kDequantWarp0 = 8;
-constexpr int kDequantGroups = 2;            // groups of 8 warps take alternate blocks
-constexpr int kDequantWarps = 8;             // warps per group (one weight tile each)
-constexpr int kNumWarps = kDequantWarp0 + kDequantGroups * kDequantWarps;  // 24
-constexpr int kThreads = 32 * kNumWarps;     // 768
-constexpr uint32_t kATileBytes = kTileN * kBlockK * 2;   // 16 KB
-constexpr uint32_t kStageCodeBytes = 2 * kTileN * kBlockK / 2;  // 8 KB: two blocks
+constexpr int kDequantWarp0 = 8;             // 8..15
+constexpr int kDequantGroups = 2;            // groups of four warps take alternate blocks
+constexpr int kDequantWarps = 4;             // one per TMEM lane quadrant
+constexpr int kNumWarps = kDequantWarp0 + kDequantGroups * kDequantWarps;  // 16
+constexpr int kThreads = 32 * kNumWarps;     // 512
+constexpr uint32_t kStageCodeBytes = kTileN * kGroupK / 2;  // 8 KB: one group
 constexpr uint32_t kScaleRowBytes = kTileN * 2;          // 256
 constexpr uint32_t kZeroRowBytes = kTileN / 2;           // 64
 constexpr uint32_t kCodeSlotBytes = kStageCodeBytes + kScaleRowBytes + kZeroRowBytes + 64;  // 8576
@@ -84,7 +101,8 @@ constexpr int kEpiRow = 36;                              // floats per transpose
 constexpr uint32_t kEpiBufBytes = 4 * 16 * kEpiRow * 4;  // 16 rows x 32 columns fp32 per warp
 constexpr unsigned long long kTimeoutNs = 2000000000ull; // 2 s per wait
 
-static_assert(kEpilogueWarp0 % 4 == 0, "TMEM lane quadrant of a warp is warp % 4");
+static_assert(kEpilogueWarp0 % 4 == 0 && kDequantWarp0 % 4 == 0,
+              "TMEM lane quadrant of a warp is warp % 4");
 static_assert(kCodeSlotBytes % 128 == 0, "code slots stay 128-byte aligned");
 
 struct Args {
@@ -101,10 +119,13 @@ struct Args {
     int split;
     int ngroups;        // K / 128
     int col_tiles, batch_tiles, items;
-    uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= max(32, bn))
+    uint32_t acc_stride;  // TMEM columns per accumulator (bn rounded up to 32)
+    int bufs;           // accumulators alternating between items (1 or 2)
+    int a_slots;        // dequantised tiles in TMEM (even, 4 .. 8)
+    uint32_t a_col0;    // first TMEM column of the tile ring (after the accumulators)
     int code_slots, x_slots;
     uint32_t x_slot_bytes;
-    uint32_t x_base, code_base, epi_base;  // shared-memory offsets of the rings
+    uint32_t code_base, epi_base;  // shared-memory offsets (the x ring starts at 0)
     int zrow_words;     // words per padded zero-point row
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
     Epilogue epi;       // fused output epilogue (plain bf16 when mode == 0)
@@ -114,11 +135,12 @@ struct Args {
 
 struct SharedTail {
     uint64_t code_full[kMaxCodeSlots];  // codes + scales (+ zero-points) of the stage landed
-    uint64_t code_free[kMaxCodeSlots];  // read by all 16 dequant warps
+    uint64_t code_free[kMaxCodeSlots];  // read by every dequant warp
     uint64_t x_full[kMaxXSlots];        // x block landed
-    uint64_t x_free[kMaxXSlots];        // MMAs reading it finished (commit)
-    uint64_t a_full[kASlots];           // weight tile dequantised (8 warp arrivals)
-    uint64_t a_free[kASlots];           // MMAs reading the weight tile finished (commit)
+    uint64_t x_free[kMaxXSlots];        // MMAs of its block finished (commit)
+    uint64_t a_full[kMaxASlots];        // weight tile in TMEM and its x landed (one arrival
+                                        // per warp of the dequant group)
+    uint64_t a_free[kMaxASlots];        // MMAs reading the weight tile finished (commit)
     uint64_t tmem_full[2];              // accumulator complete (commit)
     uint64_t tmem_empty[2];             // accumulator drained by the epilogue (4 warps)
     uint64_t mma_done;                  // final drain of the issued MMAs
@@ -179,34 +201,40 @@ __device__ __forceinline__ void issue_code_stage(const Args& a, const Item& t, i
                  a.zeros + (size_t)g * a.zrow_words + t.n0 / 8, zb, bar);
 }
 
-template <bool kHasZeros, bool kFused>
+// kSub: 64-row sub-blocks per block (1 or 2).  A block is the unit of the
+// MMA thread's waits and commits and of the dequant groups' turns.
+template <bool kHasZeros, bool kFused, int kSub>
 __global__ void __launch_bounds__(kThreads, 1)
 wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+    constexpr int kACols = kSubCols * kSub;         // TMEM columns per weight tile
+    constexpr int kBlocksPerStage = 2 / kSub;       // blocks per code stage
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled operand tiles
+    // 1024-byte alignment for the swizzled x tiles
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const int RC = a.code_slots;
     const int RX = a.x_slots;
+    const int SA = a.a_slots;
     SharedTail* tail = reinterpret_cast<SharedTail*>(smem + a.epi_base + kEpiBufBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = &tail->abort;
 
-    auto a_tile = [&](int sa) { return smem + sa * kATileBytes; };
-    auto x_tile = [&](int s) { return smem + a.x_base + (size_t)s * a.x_slot_bytes; };
+    auto x_tile = [&](int s) { return smem + (size_t)s * a.x_slot_bytes; };
     auto code_slot = [&](int s) { return smem + a.code_base + (size_t)s * kCodeSlotBytes; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < RC; ++s) {
             mbar_init(smem_u32(&tail->code_full[s]), 1);
-            mbar_init(smem_u32(&tail->code_free[s]), kDequantGroups * kDequantWarps);
+            // a stage is read by every group that has a block in it
+            mbar_init(smem_u32(&tail->code_free[s]),
+                      kDequantWarps * (kBlocksPerStage == 2 ? kDequantGroups : 1));
         }
         for (int s = 0; s < RX; ++s) {
             mbar_init(smem_u32(&tail->x_full[s]), 1);
             mbar_init(smem_u32(&tail->x_free[s]), 1);
         }
-        for (int s = 0; s < kASlots; ++s) {
+        for (int s = 0; s < SA; ++s) {
             mbar_init(smem_u32(&tail->a_full[s]), kDequantWarps);
             mbar_init(smem_u32(&tail->a_free[s]), 1);
         }
@@ -222,7 +250,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(&tail->tmem_base)), "r"(2 * a.acc_cols)
+                     ::"r"(smem_u32(&tail->tmem_base)), "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -274,8 +302,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             bool ok = true;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
                 const Item t = decode_item(a, it);
-                const int kb0 = 2 * t.g_begin;
-                for (int i = 0; i < 2 * t.ng; ++i, ++issued, q.next(RX)) {
+                for (int i = 0; i < t.ng * kBlocksPerStage; ++i, ++issued, q.next(RX)) {
                     if (issued >= RX &&
                         !wait_fast(smem_u32(&tail->x_free[q.s]), q.ph ^ 1u, abort, a.status,
                                    kTimeoutNs)) {
@@ -284,7 +311,11 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     }
                     const uint32_t bar = smem_u32(&tail->x_full[q.s]);
                     mbar_arrive_expect_tx(bar, a.x_slot_bytes);
-                    tma_load_2d(smem_u32(x_tile(q.s)), &xmap, (kb0 + i) * kBlockK, t.b0, bar);
+                    const int k0 = t.g_begin * kGroupK + i * kSub * kSubK;
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u)
+                        tma_load_2d(smem_u32(x_tile(q.s) + (uint32_t)u * (a.x_slot_bytes / kSub)),
+                                    &xmap, k0 + u * kSubK, t.b0, bar);
                 }
             }
             if (!ok)
@@ -293,44 +324,63 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                                  kTimeoutNs);
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer.  A block's weight tile is announced only
+        // once its x block has landed too (the dequant warps check it), so
+        // there is one wait per block, made for block i + 1 while block i's
+        // last MMA is still to be issued: the tensor pipe's queue holds about
+        // one MMA, and the wait would otherwise leave it idle.
         if (lane == 0) {
             const uint32_t idesc = instr_desc_bf16(kTileN, a.bn);
             bool ok = true;
             if (a.force_timeout)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
                                   (unsigned long long)a.force_timeout * 1000000ull);
-            Ring qx;
-            int gb = 0;  // blocks walked (block gb uses A slot gb % 4)
+            // descriptor of x slot 0; slot and K step add to its start-address
+            // field (16-byte units, no carry out of it)
+            const uint64_t xdesc0 = smem_desc_sw128(smem_u32(x_tile(0)));
+            const uint32_t xslot16 = a.x_slot_bytes >> 4;
+            const uint32_t a_tmem0 = tmem_base + a.a_col0;
+            Ring qx, qa;
             int j = 0;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x, ++j) {
                 const Item t = decode_item(a, it);
-                const int acc = j & 1;
-                if (j >= 2 && !wait_bounded(smem_u32(&tail->tmem_empty[acc]), ((j >> 1) - 1) & 1,
-                                            abort, a.status, kTimeoutNs)) {
+                const int acc = a.bufs == 2 ? (j & 1) : 0;
+                const int use = a.bufs == 2 ? (j >> 1) : j;
+                if (use >= 1 && !wait_bounded(smem_u32(&tail->tmem_empty[acc]), (use - 1) & 1,
+                                              abort, a.status, kTimeoutNs)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t tmem_d = tmem_base + (uint32_t)acc * a.acc_stride;
+                const int nb = t.ng * kBlocksPerStage;
+                const uint32_t xsub16 = (uint32_t)a.bn * 8;  // one x sub-tile (bn x 128 B), 16-byte units
+                if (!wait_test_first(smem_u32(&tail->a_full[qa.s]), qa.ph, abort, a.status,
+                                     kTimeoutNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tmem_d = tmem_base + acc * a.acc_cols;
-                for (int i = 0; i < 2 * t.ng; ++i, ++gb, qx.next(RX)) {
-                    const int sa = gb & (kASlots - 1);
-                    if (!wait_fast(smem_u32(&tail->x_full[qx.s]), qx.ph, abort, a.status,
-                                   kTimeoutNs) ||
-                        !wait_fast(smem_u32(&tail->a_full[sa]), (uint32_t)(gb >> 2) & 1u, abort,
-                                   a.status, kTimeoutNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t abase = smem_u32(a_tile(sa));
-                    const uint32_t xbase = smem_u32(x_tile(qx.s));
+                for (int i = 0; i < nb; ++i) {
+                    const uint32_t ta = a_tmem0 + (uint32_t)(qa.s * kACols);
+                    const uint64_t xd = xdesc0 + (uint64_t)((uint32_t)qx.s * xslot16);
+                    mma_bf16_ts(tmem_d, ta, xd, idesc, i != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        mma_bf16_ss(tmem_d, smem_desc_sw128(abase + 32 * kk),
-                                    smem_desc_sw128(xbase + 32 * kk), idesc, (i | kk) != 0);
+                    for (int kk = 1; kk < 4 * kSub - 1; ++kk)
+                        mma_bf16_ts(tmem_d, ta + 8 * kk,
+                                    xd + (uint64_t)((kk >> 2) * xsub16 + 2 * (kk & 3)), idesc, 1u);
+                    const int sa = qa.s, xs = qx.s;
+                    qa.next(SA);
+                    qx.next(RX);
+                    if (i + 1 < nb) {
+                        ok = wait_test_first(smem_u32(&tail->a_full[qa.s]), qa.ph, abort, a.status,
+                                             kTimeoutNs);
+                        tc_fence_after();
+                    }
+                    mma_bf16_ts(tmem_d, ta + 8 * (4 * kSub - 1),
+                                xd + (uint64_t)((kSub - 1) * xsub16 + 6), idesc, 1u);
                     mma_commit(smem_u32(&tail->a_free[sa]));
-                    mma_commit(smem_u32(&tail->x_free[qx.s]));
+                    mma_commit(smem_u32(&tail->x_free[xs]));
+                    if (!ok) break;
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&tail->tmem_full[acc]));  // fires once this item's MMAs are done
@@ -349,33 +399,42 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             }
         }
     } else if (warp >= kDequantWarp0) {
-        // ---------------- dequant (warps 8..23): group grp takes blocks grp,
-        // grp + 2, ... -- block grp of every code stage -- into A slots
-        // grp and grp + 2 in turn
-        const int dw = warp - kDequantWarp0;
-        const int grp = dw / kDequantWarps;
-        const int t256 = (dw % kDequantWarps) * 32 + lane;  // 0..255 within the group
-        const int r = t256 & (kTileN - 1);                  // weight column within the tile
-        const int h = t256 >> 7;                            // which 32-row chunk of the block
-        Ring q;
-        int own = 0;  // blocks of this group so far
+        // ---------------- dequant: group grp (four warps, one per TMEM lane
+        // quadrant) takes blocks grp, grp + 2, ...: block b is 64 kSub-row
+        // block b % kBlocksPerStage of code stage b / kBlocksPerStage, A slot
+        // b % SA and x slot b % RX -- SA and RX are even, so every A and x slot
+        // serves one group; with one block per stage RC is even too, and with
+        // two each group reads every stage.  Each thread owns one weight
+        // column = one TMEM lane and decodes its 64 kSub codes.
+        const int grp = (warp - kDequantWarp0) / kDequantWarps;
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // weight column within the tile
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + a.a_col0;
+        constexpr int kCodeStep = kBlocksPerStage == 2 ? 1 : kDequantGroups;
+        int cs = kBlocksPerStage == 2 ? 0 : grp;  // code slot of this group's current block
+        int sa = grp, xs = grp;                   // its A and x slots
+        uint32_t cph = 0, aph = 0, xph = 0;
+        int own = 0;                       // blocks of this group so far
+        int gb = 0;                        // blocks walked by the CTA
         bool ok = true;
         for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x) {
             const Item t = decode_item(a, it);
             const int rr = min(r, t.nvalid - 1);  // lanes past a ragged edge repeat a column
-            for (int c = 0; c < t.ng; ++c, ++own, q.next(RC)) {
-                const int sa = grp + 2 * (own & 1);
-                bool landed = wait_fast(smem_u32(&tail->code_full[q.s]), q.ph, abort, a.status,
+            for (int c = 0; c < t.ng * kBlocksPerStage; ++c, ++gb) {
+                if ((gb & 1) != grp) continue;
+                const int jb = kBlocksPerStage == 2 ? (c & 1) : 0;  // block within the stage
+                bool landed = wait_fast(smem_u32(&tail->code_full[cs]), cph, abort, a.status,
                                         kTimeoutNs);
-                if (landed && own >= 2)
-                    landed = wait_fast(smem_u32(&tail->a_free[sa]), (uint32_t)((own >> 1) - 1) & 1u,
-                                       abort, a.status, kTimeoutNs);
+                // the tile slot is free once the MMAs of its previous block are done
+                if (landed && gb >= SA)
+                    landed = wait_fast(smem_u32(&tail->a_free[sa]), aph ^ 1u, abort, a.status,
+                                       kTimeoutNs);
                 if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
                     ok = false;
                     break;
                 }
-                const uint8_t* slot = code_slot(q.s);
-                const uint4 qw = reinterpret_cast<const uint4*>(slot)[(2 * grp + h) * t.nvalid + rr];
+                tc_fence_after();
+                const uint8_t* slot = code_slot(cs);
                 const uint32_t s2 = scale_pair(
                     reinterpret_cast<const uint16_t*>(slot + kStageCodeBytes)[rr]);
                 uint32_t z2 = kSymmetricZeroPair;
@@ -384,38 +443,70 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                         slot + kStageCodeBytes + kScaleRowBytes)[rr >> 3];
                     z2 = zero_pair((zw >> (4 * (rr & 7))) & 0xFu);
                 }
-                const uint32_t words[4] = {qw.x, qw.y, qw.z, qw.w};
-                uint8_t* row = a_tile(sa) + r * 128;
+                const uint4* codes = reinterpret_cast<const uint4*>(slot) + (size_t)(2 * jb) * t.nvalid;
+                // chunk h (rows 32h .. 32h+31 of the block) -> TMEM columns 16h .. 16h+15
+                const uint32_t col = lane_addr + (uint32_t)(sa * kACols);
 #pragma unroll
-                for (int jw = 0; jw < 4; ++jw) {
-                    uint32_t p[4];
-                    dequant_word(words[jw], z2, s2, p);
-                    const int chunk = (4 * h + jw) ^ (r & 7);  // 128-byte swizzle
-                    *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(p[0], p[1], p[2], p[3]);
+                for (int h = 0; h < 2 * kSub; ++h) {
+                    const uint4 qw = codes[h * t.nvalid + rr];
+                    const uint32_t words[4] = {qw.x, qw.y, qw.z, qw.w};
+                    uint32_t v[16];
+#pragma unroll
+                    for (int jw = 0; jw < 4; ++jw)
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp)
+                            v[4 * jw + pp] = dequant_pair(words[jw], pp, z2, s2);
+                    tmem_st_16(col + 16 * h, v);
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
+                bool xok = true;
                 if (lane == 0) {
-                    mbar_arrive(smem_u32(&tail->a_full[sa]));
-                    mbar_arrive(smem_u32(&tail->code_free[q.s]));
+                    mbar_arrive(smem_u32(&tail->code_free[cs]));  // this warp read the stage
+                    // the tile is announced once the block's x has landed too
+                    xok = wait_fast(smem_u32(&tail->x_full[xs]), xph, abort, a.status, kTimeoutNs);
+                    if (xok) mbar_arrive(smem_u32(&tail->a_full[sa]));
+                }
+                cs += kCodeStep;
+                if (cs >= RC) {
+                    cs -= RC;
+                    cph ^= 1u;
+                }
+                sa += kDequantGroups;
+                if (sa >= SA) {
+                    sa -= SA;
+                    aph ^= 1u;
+                }
+                xs += kDequantGroups;
+                if (xs >= RX) {
+                    xs -= RX;
+                    xph ^= 1u;
+                }
+                ++own;
+                if (!__shfl_sync(0xffffffffu, xok ? 1 : 0, 0)) {  // warp-uniform exit
+                    ok = false;
+                    break;
                 }
             }
         }
-    } else if (warp >= kEpilogueWarp0) {
+    } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
         // ---------------- epilogue (warps 4..7; TMEM lane quadrant = warp % 4)
         const int quad = warp & 3;
         float* buf = reinterpret_cast<float*>(smem + a.epi_base) + quad * 16 * kEpiRow;
         int j = 0;
         for (int it = blockIdx.x; it < a.items; it += gridDim.x, ++j) {
             const Item t = decode_item(a, it);
-            const int acc = j & 1;
-            const bool done = wait_bounded(smem_u32(&tail->tmem_full[acc]), (j >> 1) & 1, abort,
+            const int acc = a.bufs == 2 ? (j & 1) : 0;
+            const int use = a.bufs == 2 ? (j >> 1) : j;
+            const bool done = wait_bounded(smem_u32(&tail->tmem_full[acc]), use & 1, abort,
                                            a.status, kTimeoutNs);
             tc_fence_after();
             const bool live = __all_sync(0xffffffffu, done && !*abort);
             if (live) {  // tcgen05.ld is warp-collective
                 const int nq = t.n0 + quad * 32;  // this warp's 32 columns
-                const uint32_t taddr = tmem_base + acc * a.acc_cols + ((uint32_t)(quad * 32) << 16);
+                const uint32_t taddr =
+                    tmem_base + (uint32_t)acc * a.acc_stride + ((uint32_t)(quad * 32) << 16);
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
                     tmem_ld_16(taddr + c0, v);
@@ -533,7 +624,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(2 * a.acc_cols)
+                     "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -559,86 +650,110 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Shared memory: [A ring: 4 x 16 KB][x ring][code ring][epilogue buffer][tail]
-// (+ 1 KB of alignment slack).  The x ring takes what the code ring leaves,
-// with at least 3 slots; the code ring is as deep as the rest allows.
+// 64-row sub-blocks per block: two (longer blocks, half the MMA thread's
+// per-block waits and commits per MMA) while both accumulators fit in TMEM
+// beside the tile ring (bn <= 128); one at wider tiles, where the single
+// accumulator and the smaller rings that twice-as-long blocks leave made them
+// slower (measured on the decode shapes at B = 384 .. 1024).
+int sub_blocks(int bn) { return bn <= 128 ? 2 : 1; }
+
+// Shared memory: [x ring][code ring][epilogue buffer][tail] (+ 1 KB of
+// alignment slack).  Six code stages (the weights come from HBM), then as
+// many x slots as fit (an even 2 .. 8: x comes from L2), then the rest to the
+// code ring (an even number).
 struct WideLayout {
     int x_slots, code_slots;
-    uint32_t x_slot_bytes, x_base, code_base, epi_base;
+    uint32_t x_slot_bytes, code_base, epi_base;
     size_t smem;
 };
 
-WideLayout wide_layout(int bn) {
+WideLayout wide_layout(int bn, int sub) {
     WideLayout l;
-    l.x_slot_bytes = (uint32_t)bn * kBlockK * 2;  // multiple of 1024 (bn % 8 == 0)
-    const size_t fixed = 1024 + (size_t)kASlots * kATileBytes + kEpiBufBytes + sizeof(SharedTail);
+    // kSub sub-tiles of bn x 128 B, each a multiple of 1024 (bn % 8 == 0)
+    l.x_slot_bytes = (uint32_t)bn * kSubK * 2 * (uint32_t)sub;
+    const size_t fixed = 1024 + kEpiBufBytes + sizeof(SharedTail);
     const size_t avail = kSmemBudget - fixed;
-    // six code stages (twelve blocks ahead of the tensor pipe: the weights
-    // come from HBM), then as many x slots as fit (3 .. 6: x comes from L2),
-    // then the rest to the code ring
     const size_t want_code = 6 * (size_t)kCodeSlotBytes;
     int xs = avail > want_code ? (int)((avail - want_code) / l.x_slot_bytes) : 0;
-    xs = std::max(3, std::min(6, xs));
+    xs = std::max(2, std::min(8, xs)) & ~1;  // even: a slot serves one dequant group
     const size_t left = avail > (size_t)xs * l.x_slot_bytes ? avail - (size_t)xs * l.x_slot_bytes : 0;
-    l.code_slots = (int)std::min<size_t>(kMaxCodeSlots, left / kCodeSlotBytes);
+    l.code_slots = (int)std::min<size_t>(kMaxCodeSlots, left / kCodeSlotBytes) & ~1;  // even
     l.x_slots = xs;
-    l.x_base = (uint32_t)kASlots * kATileBytes;
-    l.code_base = l.x_base + (uint32_t)xs * l.x_slot_bytes;
+    l.code_base = (uint32_t)xs * l.x_slot_bytes;
     l.epi_base = l.code_base + (uint32_t)l.code_slots * kCodeSlotBytes;
     l.smem = 1024 + (size_t)l.epi_base + kEpiBufBytes + sizeof(SharedTail);
     return l;
 }
 
-uint32_t acc_cols_for(int bn) {
-    uint32_t c = 32;
-    while (c < (uint32_t)bn) c <<= 1;
-    return c;
+// TMEM: [accumulator 0][accumulator 1, when both fit with 4 tile slots][tiles].
+struct TmemLayout {
+    uint32_t acc_stride, a_col0;
+    int bufs, a_slots;
+};
+
+TmemLayout tmem_layout(int bn, int sub) {
+    TmemLayout t;
+    const uint32_t acols = (uint32_t)(kSubCols * sub);
+    t.acc_stride = (uint32_t)((bn + 31) / 32 * 32);
+    t.bufs = 2 * t.acc_stride + 4 * acols <= (uint32_t)kTmemCols ? 2 : 1;
+    t.a_col0 = (uint32_t)t.bufs * t.acc_stride;
+    t.a_slots = std::min(kMaxASlots, (int)((kTmemCols - t.a_col0) / acols)) & ~1;
+    return t;
 }
 
 }  // namespace
 
-// Work decomposition for batches above 128 rows.  A work item is one
+// Work decomposition for batches above 64 rows.  A work item is one
 // 128-column tile of W for one batch tile of bn rows, over a range of whole
-// 128-row groups of K; persistent CTAs (one per SM) take items round robin.
-// The choice trades three costs, estimated in SM cycles per CTA:
-//   * tensor pipe: 4 MMAs of M = 128, N = bn, K = 16 per 64-row block, about
-//     bn / 2 cycles each;
-//   * dequantisation: every weight tile is decoded once per batch tile, about
-//     200 cycles per block at the CUDA cores' rate -- the block takes the
-//     longer of the two;
-//   * K split: partial sums are added into an fp32 accumulator with vector
-//     reductions (bn x 128 floats per item) and converted by the last item of
-//     the tile, a few thousand cycles per item.
-// Every CTA runs ceil(items / SMs) items, so the decomposition that gives the
-// busiest CTA the least work wins.
+// 128-row groups of K; persistent CTAs (one per SM) take items round robin,
+// so the time is that of the busiest CTA: ceil(items / SMs) items.  Every
+// weight tile is decoded once per batch tile, so smaller batch tiles cost
+// dequantisation, larger ones leave SMs idle; a K split adds the partial
+// sums' reductions.  The cost of an item, in SM cycles, is a fit to the
+// measured times of the decode shapes (qkv 4096 -> 6144, o_proj 4096 -> 4096,
+// gate_up 4096 -> 28672, down 14336 -> 4096, lm_head 4096 -> 128256 at
+// B = 128 .. 1024, every batch tile, K split and block length), which picks
+// plans within 5 % of the fastest measured one on each of them:
+//   per 64 rows of K:  bn <= 128: about 560 cycles (the per-block waits,
+//                      commits and the decode, not the MMAs, set the pace);
+//                      wider:     about 360 + 2.6 bn;
+//   per item:          about 6300 (bn <= 128) or 120 cycles, plus, with a K
+//                      split, about 96 bn - 8900 (at least 1000) for the
+//                      reductions of its bn x 128 partial sums.
+// The search stays inside the range the fit was made on -- the smallest
+// batch-tile count and the two above it, K splits of 1 to 4 -- where the
+// fit is checked against measurements; outside it the fit extrapolates.
 TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
     TcPlan best{};
     double best_cost = 1e300;
     const int G = K / kGroup;
     const int col_tiles = (N + kTileN - 1) / kTileN;
     const int min_bt = (B + 255) / 256;
-    for (int bt = min_bt; bt <= min_bt + 6; ++bt) {
+    for (int bt = min_bt; bt <= min_bt + 2; ++bt) {
         const int per = (B + bt - 1) / bt;
         const int bn = std::min(256, (per + 15) / 16 * 16);
         if (bn < 32 && bt > min_bt) break;
         const int batch_tiles = (B + bn - 1) / bn;
         const long long tiles = (long long)col_tiles * batch_tiles;
-        const double block = std::max(2.0 * bn, 200.0) + 40.0;
-        for (int split = 1; split <= std::min(16, G); ++split) {
+        const double rows64 =
+            bn <= 128 ? std::max(560.0 - 0.7 * bn, 2.2 * bn) : 356.5 + 2.6 * bn;
+        const double fixed = bn <= 128 ? 6290.0 : 120.0;
+        for (int split = 1; split <= std::min(4, G); ++split) {
             const int gps = (G + split - 1) / split;
             const int s = (G + gps - 1) / gps;  // no empty splits
             if (s != split) continue;
             if (s > 1 && tiles > kMaxCounters - 2) break;
             const long long items = tiles * s;
             const long long per_cta = (items + num_sms - 1) / num_sms;
-            const double item = 2.0 * gps * block + 1500.0 + (s > 1 ? 12.0 * bn + 3000.0 : 0.0);
-            const double cost = (double)per_cta * item;
+            const double reduce = s > 1 ? std::max(1000.0, 96.3 * bn - 8871.0) : 0.0;
+            const double cost = (double)per_cta * (2.0 * gps * rows64 + fixed + reduce);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.bn = bn;
                 best.batch_tiles = batch_tiles;
                 best.split = s;
                 best.kb_per_split = 2 * gps;
+                best.sub = sub_blocks(bn);
             }
         }
     }
@@ -658,15 +773,17 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     CUtensorMap xmap;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)B};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)p.bn};
+    const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)p.bn};  // 128-byte rows (swizzle span)
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
-    const WideLayout lay = wide_layout(p.bn);
-    if (lay.x_slots < 3 || lay.code_slots < 2 || lay.smem > kSmemBudget)
+    const WideLayout lay = wide_layout(p.bn, p.sub);
+    const TmemLayout tm = tmem_layout(p.bn, p.sub);
+    if (lay.x_slots < 2 || (lay.x_slots & 1) || lay.code_slots < 2 || lay.smem > kSmemBudget ||
+        tm.a_slots < 4)
         return cudaErrorInvalidConfiguration;
     Args a;
     a.packed = static_cast<const uint8_t*>(packed);
@@ -687,11 +804,13 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.col_tiles = p.col_tiles;
     a.batch_tiles = p.batch_tiles;
     a.items = p.col_tiles * p.batch_tiles * p.split;
-    a.acc_cols = acc_cols_for(p.bn);
+    a.acc_stride = tm.acc_stride;
+    a.bufs = tm.bufs;
+    a.a_slots = tm.a_slots;
+    a.a_col0 = tm.a_col0;
     a.code_slots = lay.code_slots;
     a.x_slots = lay.x_slots;
     a.x_slot_bytes = lay.x_slot_bytes;
-    a.x_base = lay.x_base;
     a.code_base = lay.code_base;
     a.epi_base = lay.epi_base;
     a.zrow_words = packed_zero_row_words(N);
@@ -700,11 +819,17 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
 
     const size_t smem = lay.smem;
     const bool fused = epi.mode != 0;
-    const void* kern =
-        has_zeros ? (fused ? reinterpret_cast<const void*>(wide_kernel<true, true>)
-                           : reinterpret_cast<const void*>(wide_kernel<true, false>))
-                  : (fused ? reinterpret_cast<const void*>(wide_kernel<false, true>)
-                           : reinterpret_cast<const void*>(wide_kernel<false, false>));
+    const void* kern = nullptr;
+    switch ((p.sub == 2 ? 4 : 0) + (has_zeros ? 2 : 0) + (fused ? 1 : 0)) {
+        case 0: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 1>); break;
+        case 1: kern = reinterpret_cast<const void*>(wide_kernel<false, true, 1>); break;
+        case 2: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 1>); break;
+        case 3: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 1>); break;
+        case 4: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 2>); break;
+        case 5: kern = reinterpret_cast<const void*>(wide_kernel<false, true, 2>); break;
+        case 6: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 2>); break;
+        default: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 2>); break;
+    }
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
