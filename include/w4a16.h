@@ -74,9 +74,10 @@ typedef enum {
 typedef enum {
     W4A16_PATH_AUTO = -1,
     W4A16_PATH_SKINNY = 0,  /* small-batch split-K kernel (mma.sync), B <= 16 */
-    W4A16_PATH_TCGEN05 = 1  /* tcgen05 tensor-core kernels: up to 64 batch rows the
-                               multi-issuer kernel, above it the wide-batch kernel
-                               (both keep the dequantised weight tile in TMEM) */
+    W4A16_PATH_TCGEN05 = 1  /* tcgen05 tensor-core kernels: the wide-batch kernel
+                               above 16 batch rows, the multi-issuer kernel when
+                               forced at 16 or fewer (both keep the dequantised
+                               weight tile in TMEM) */
 } w4a16_path;
 
 /* Bytes of the packed blob for a K x N layer (codes, plus zero-points when

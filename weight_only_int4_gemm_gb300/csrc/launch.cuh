@@ -88,7 +88,7 @@ struct TcPlan {
     int bufs;        // accumulator sets alternating between items (1, 2)
     int a_slots;     // dequantised weight tiles held in TMEM
     int nsub;        // 64-row K blocks per copy stage
-    bool wide;       // more than 64 batch rows: the single-issuer kernel (tc_wide.cu)
+    bool wide;       // more than 16 batch rows: the single-issuer kernel (tc_wide.cu)
     int sub;         // wide kernel: 64-row sub-blocks per block (1 or 2)
 };
 TcPlan plan_tc(int B, int K, int N, int num_sms);

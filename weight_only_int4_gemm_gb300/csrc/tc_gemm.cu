@@ -69,10 +69,12 @@ constexpr int kMaxASlots = 12;               // ring of weight tiles in TMEM
 constexpr int kTmemCols = 512;               // the whole of TMEM (one CTA per SM)
 constexpr int kACols = kBlockK / 2;          // TMEM columns per weight tile
 constexpr int kMaxIssuers = 4;
-// Wider batches go to tc_wide.cu: measured on the decoder-layer and lm_head
-// shapes, the single-issuer wide-batch kernel with 128-row blocks is even with
-// this one at 64 rows and 1.1-1.4x faster at 128.
-constexpr int kMaxTmemBatch = 64;
+// Wider batches go to tc_wide.cu: measured on the Llama-3-8B decode step
+// (129 GEMMs), the single-issuer wide-batch kernel is faster from 17 rows on
+// (B = 24 / 32 / 48 / 64: 2655 / 2714 / 2903 / 3046 us per step against
+// 2801 / 2897 / 3566 / 3969 us here).  This kernel serves the tensor-core path
+// when it is forced at 16 rows or fewer.
+constexpr int kMaxTmemBatch = 16;
 constexpr int kEpilogueWarp0 = 4;            // 4..7
 constexpr int kDequantWarp0 = 8;             // 8..23
 constexpr int kDequantGroups = 4;            // groups of 4 warps (one per quadrant)

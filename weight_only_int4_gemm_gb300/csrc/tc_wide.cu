@@ -1,6 +1,6 @@
-// tc_wide.cu -- W4A16 GEMM on the tcgen05 tensor cores for wide batches
-// (more than 64 rows of x), one MMA-issuing thread, the dequantised weight
-// tile in tensor memory.
+// tc_wide.cu -- W4A16 GEMM on the tcgen05 tensor cores for batches of more
+// than 16 rows of x: one MMA-issuing thread, the dequantised weight tile in
+// tensor memory.
 //
 // "Give Me BF16 or Give Me Death" (summary), "Inference with W4A16": the
 // 4-bit weights are rebuilt to 16-bit values inside the matrix
@@ -703,7 +703,7 @@ TmemLayout tmem_layout(int bn, int sub) {
 
 }  // namespace
 
-// Work decomposition for batches above 64 rows.  A work item is one
+// Work decomposition for batches above 16 rows.  A work item is one
 // 128-column tile of W for one batch tile of bn rows, over a range of whole
 // 128-row groups of K; persistent CTAs (one per SM) take items round robin,
 // so the time is that of the busiest CTA: ceil(items / SMs) items.  Every
