@@ -43,7 +43,10 @@
  *  - x                 bf16 [B][K], row-major (row stride K).
  *  - y                 bf16 [B][N], row-major (row stride N).
  *  - packed blob       opaque, w4a16_packed_bytes() bytes, written by
- *                      w4a16_pack(); layout tag W4A16_PACKED_LAYOUT.
+ *                      w4a16_pack(); its last 16 bytes are a tag (a magic
+ *                      word, the layout version W4A16_PACKED_LAYOUT, K, and
+ *                      N with the zero-point flag in bit 31) that
+ *                      w4a16_packed_check and every GEMM check.
  */
 #ifndef W4A16_H_
 #define W4A16_H_
@@ -81,8 +84,14 @@ typedef enum {
 } w4a16_path;
 
 /* Bytes of the packed blob for a K x N layer (codes, plus zero-points when
- * has_zeros != 0): K*N/2 [+ (K/128)*R*4], where R = N/8 rounded up to a
- * multiple of 4 (each group's row of zero-point words is padded to 16 bytes).
+ * has_zeros != 0, plus the 16-byte layout tag): K*N/2 [+ (K/128)*R*4] + 16,
+ * where R = N/8 rounded up to a multiple of 4 (each group's row of zero-point
+ * words is padded to 16 bytes).  Storage per weight at group 128: 4 bits of
+ * code + 16/128 bits of scale = 4.125 bits ("When quantization pays -- and
+ * when it does not", section "The three regimes": 0.5156 bytes per weight;
+ * "Give Me BF16 or Give Me Death", "W4A16-INT Quantization", paragraph
+ * "Group-wise quantization granularity": 0.125 bit of scale overhead), plus
+ * 0.03125 bit with zero-points; the tag is a fixed 16 bytes.
  * Returns 0 for invalid shapes. */
 size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros);
 
@@ -163,6 +172,10 @@ w4a16_status w4a16_gemm_path(const void *x, const void *packed, const void *scal
 /* Materialise the dequantised weights W[K][N] (bf16, row-major) from the
  * packed blob with the same device decode routine the GEMM kernels use, so
  * that every weight can be compared bit for bit with RNE_bf16((q - z) * s).
+ * "When quantization pays -- and when it does not", section "Counting c from
+ * the kernel, not from intuition": the magic-number decode gives the exact
+ * integer (q - 8) before one bf16 multiply by the group scale; "Give Me BF16
+ * or Give Me Death", "W4A16-INT Quantization": w = s * q per group of 128.
  *   w  device bf16 [K][N] (written) */
 w4a16_status w4a16_dequant_ref(const void *packed, const void *scales, int has_zeros, void *w,
                                int K, int N, int group_size, void *stream);
@@ -236,10 +249,13 @@ int w4a16_select_path(int B, int K, int N);
  * report the operator actually used).  Never NULL; static storage. */
 const char *w4a16_kernel_name(int B, int K, int N);
 
-/* Device-side status word of the tensor-core kernel: 0 when every bounded
- * wait completed, else W4A16_ERR_TIMEOUT.  Synchronises the current device;
- * clears the word when `clear` != 0.  Returns W4A16_ERR_CUDA if the query
- * itself fails. */
+/* Device-side status word of the GEMM kernels: W4A16_OK when every bounded
+ * wait completed and every packed blob's tag matched its call, else
+ * W4A16_ERR_TIMEOUT (a bounded wait ran out) or W4A16_ERR_UNSUPPORTED (a GEMM
+ * was given a blob whose tag does not describe it: another layout version,
+ * shape or zero-point flag -- its output is then meaningless).  Synchronises
+ * the current device; clears the word when `clear` != 0.  Returns
+ * W4A16_ERR_CUDA if the query itself fails. */
 w4a16_status w4a16_device_status(int clear);
 
 /* w4a16_gemm for callers that cannot allocate device memory (the pages have
@@ -275,6 +291,17 @@ w4a16_status w4a16_debug_forced_timeout(const void *x, const void *packed, const
                                         int has_zeros, void *y, int B, int K, int N,
                                         int group_size, void *workspace, size_t ws_bytes,
                                         int wait_ms, void *stream);
+
+/* Checks a packed blob's tag against the layout version this library reads
+ * and the call's shape: W4A16_OK, W4A16_ERR_UNSUPPORTED when the blob was
+ * written for another layout version (or is not a packed blob), or
+ * W4A16_ERR_SHAPE when K, N or the zero-point flag differ; NULL / ALIGN /
+ * SHAPE / UNSUPPORTED for invalid arguments as everywhere.  For validating
+ * stored weights when they are loaded: it copies the 16-byte tag to the host
+ * and synchronises `stream`.  (The GEMMs check the tag on the device on every
+ * call, see w4a16_device_status.) */
+w4a16_status w4a16_packed_check(const void *packed, int K, int N, int group_size, int has_zeros,
+                                void *stream);
 
 /* Static description of a status code; never NULL. */
 const char *w4a16_status_string(w4a16_status status);

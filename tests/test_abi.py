@@ -41,11 +41,12 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_packed_bytes():
-    assert w.w4a16_packed_bytes(4096, 4096, False) == 4096 * 4096 // 2
-    assert w.w4a16_packed_bytes(4096, 4096, True) == 4096 * 4096 // 2 + 32 * 512 * 4
+    tag = 16  # the layout tag at the end of every blob
+    assert w.w4a16_packed_bytes(4096, 4096, False) == 4096 * 4096 // 2 + tag
+    assert w.w4a16_packed_bytes(4096, 4096, True) == 4096 * 4096 // 2 + 32 * 512 * 4 + tag
     # zero-point rows are padded to a multiple of 4 words (16 bytes)
-    assert w.w4a16_packed_bytes(128, 8, True) == 128 * 8 // 2 + 1 * 4 * 4
-    assert w.w4a16_packed_bytes(256, 4104, True) == 256 * 4104 // 2 + 2 * 516 * 4
+    assert w.w4a16_packed_bytes(128, 8, True) == 128 * 8 // 2 + 1 * 4 * 4 + tag
+    assert w.w4a16_packed_bytes(256, 4104, True) == 256 * 4104 // 2 + 2 * 516 * 4 + tag
     lib = _lib.load()
     assert lib.w4a16_packed_bytes(100, 4096, 128, 0) == 0
     assert lib.w4a16_packed_bytes(128, 12, 128, 0) == 0
@@ -212,3 +213,11 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load()
+
+
+def test_packed_check_validation(lib):
+    """Argument errors of the blob-tag check are reported before any copy."""
+    assert lib.w4a16_packed_check(FAKE, 256, 8, 64, 0, None) == ERR_UNSUP
+    assert lib.w4a16_packed_check(FAKE, 100, 8, 128, 0, None) == ERR_SHAPE
+    assert lib.w4a16_packed_check(None, 256, 8, 128, 0, None) == ERR_NULL
+    assert lib.w4a16_packed_check(FAKE + 4, 256, 8, 128, 0, None) == ERR_ALIGN

@@ -41,6 +41,7 @@ SIGNATURES = {
     "w4a16_kernel_name": (ctypes.c_char_p, [_I, _I, _I]),
     "w4a16_debug_forced_timeout": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_device_status": (_I, [_I]),
+    "w4a16_packed_check": (_I, [_P, _I, _I, _I, _I, _P]),
     "w4a16_quantize_rtn": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "w4a16_grouped_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "w4a16_gemm_grouped": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
@@ -302,6 +303,14 @@ def w4a16_debug_forced_timeout(x: torch.Tensor, packed: torch.Tensor, scales: to
 
 def w4a16_device_status(clear: bool = True) -> int:
     return int(load().w4a16_device_status(1 if clear else 0))
+
+
+def w4a16_packed_check(packed: torch.Tensor, K: int, N: int, has_zeros: bool,
+                       stream=None) -> int:
+    """Status of a packed blob's tag against (K, N, has_zeros) and the
+    library's layout version (0 = OK); synchronises the stream."""
+    return int(load().w4a16_packed_check(packed.data_ptr(), K, N, GROUP, 1 if has_zeros else 0,
+                                         _stream(stream)))
 
 
 # ---- W8A8-FP8 comparison path (include/w8a8_fp8.h)

@@ -67,6 +67,50 @@ int num_sms() {
     return s > 0 ? s : 152;
 }
 
+// Per-shape plan cache: the planners are pure functions of (B, K, N, SM
+// count), and an eager caller repeats the same few shapes; one mutex guards
+// it (the library is otherwise stateless).
+struct PlanKey {
+    int dev, B, K, N;
+    bool operator==(const PlanKey& o) const {
+        return dev == o.dev && B == o.B && K == o.K && N == o.N;
+    }
+};
+struct PlanKeyHash {
+    size_t operator()(const PlanKey& k) const {
+        return ((size_t)k.dev * 1000003u ^ (size_t)k.B * 7919u) * 131u ^ (size_t)k.K * 31u ^
+               (size_t)k.N;
+    }
+};
+constexpr size_t kMaxCachedPlans = 4096;
+
+template <typename Plan, typename Make>
+Plan cached_plan(std::unordered_map<PlanKey, Plan, PlanKeyHash>& cache, std::mutex& mu, int B,
+                 int K, int N, Make make) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const PlanKey key{dev, B, K, N};
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const Plan p = make();
+    if (cache.size() >= kMaxCachedPlans) cache.clear();  // bounded: many distinct shapes
+    cache.emplace(key, p);
+    return p;
+}
+
+SkinnyPlan skinny_plan(int B, int K, int N) {
+    static std::mutex mu;
+    static std::unordered_map<PlanKey, SkinnyPlan, PlanKeyHash> cache;
+    return cached_plan(cache, mu, B, K, N, [&] { return plan_skinny(B, K, N, num_sms()); });
+}
+
+TcPlan tc_plan(int B, int K, int N) {
+    static std::mutex mu;
+    static std::unordered_map<PlanKey, TcPlan, PlanKeyHash> cache;
+    return cached_plan(cache, mu, B, K, N, [&] { return plan_tc(B, K, N, num_sms()); });
+}
+
 // Batch above which the tensor-core kernel takes over from the split-K
 // kernel.  Measured on GB300 (decoder-layer shapes): the mma.sync kernel is
 // faster up to 8 rows, the two are even at 16, and from 17 rows (where the
@@ -84,8 +128,8 @@ int choose_path(int B, int K, int N) {
 
 size_t path_workspace(int path, int B, int K, int N) {
     if (path == W4A16_PATH_SKINNY)
-        return skinny_workspace_bytes(plan_skinny(B, K, N, num_sms()), B, N);
-    return tc_workspace_bytes(plan_tc(B, K, N, num_sms()), B, N);
+        return skinny_workspace_bytes(skinny_plan(B, K, N), B, N);
+    return tc_workspace_bytes(tc_plan(B, K, N), B, N);
 }
 
 w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
@@ -112,13 +156,13 @@ w4a16_status gemm_impl(const void* x, const void* packed, const void* scales, in
     unsigned int* status = device_status_word();
     if (status == nullptr) return W4A16_ERR_CUDA;
     if (path == W4A16_PATH_SKINNY)
-        return from_cuda(launch_skinny(plan_skinny(B, K, N, num_sms()), x, packed, scales,
+        return from_cuda(launch_skinny(skinny_plan(B, K, N), x, packed, scales,
                                        has_zeros != 0, y, B, K, N, workspace, status, epi, s));
     if (forced_timeout_ms > 0)
-        return from_cuda(launch_tc_forced_timeout(plan_tc(B, K, N, num_sms()), x, packed, scales,
+        return from_cuda(launch_tc_forced_timeout(tc_plan(B, K, N), x, packed, scales,
                                                   has_zeros != 0, y, B, K, N, workspace, status,
                                                   forced_timeout_ms, s));
-    return from_cuda(launch_tc(plan_tc(B, K, N, num_sms()), x, packed, scales, has_zeros != 0,
+    return from_cuda(launch_tc(tc_plan(B, K, N), x, packed, scales, has_zeros != 0,
                                y, B, K, N, workspace, status, epi, s));
 }
 
@@ -134,6 +178,23 @@ int gemm_entry(const void* x, const void* packed, const void* scales, int has_ze
 size_t auto_workspace_bytes(int B, int K, int N, int group_size) {
     if (group_size != kGroup || !shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
     return path_workspace(choose_path(B, K, N), B, K, N);
+}
+
+cudaError_t set_smem_limit(const void* kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, size_t> set[64];  // per device: the limit set
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64)
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = set[dev].find(kernel);
+    if (it != set[dev].end() && it->second >= bytes) return cudaSuccess;
+    const cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess) set[dev][kernel] = bytes;
+    return err;
 }
 
 cudaError_t launch_with_pdl(const void* func, dim3 grid, dim3 block, size_t smem,
@@ -159,7 +220,7 @@ extern "C" {
 
 size_t w4a16_packed_bytes(int K, int N, int group_size, int has_zeros) {
     if (group_size != kGroup || !shape_ok(K, N)) return 0;
-    return packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);
+    return packed_total_bytes(K, N, has_zeros != 0);
 }
 
 size_t w4a16_workspace_bytes(int B, int K, int N, int group_size) {
@@ -332,7 +393,7 @@ int w4a16_select_path(int B, int K, int N) {
 const char* w4a16_kernel_name(int B, int K, int N) {
     if (!shape_ok(K, N) || B < 1 || B > kMaxB) return "invalid";
     if (choose_path(B, K, N) == W4A16_PATH_SKINNY) return "skinny_kernel";
-    return plan_tc(B, K, N, num_sms()).wide ? "wide_kernel" : "tc_kernel";
+    return tc_plan(B, K, N).wide ? "wide_kernel" : "tc_kernel";
 }
 
 w4a16_status w4a16_device_status(int clear) {
@@ -344,7 +405,26 @@ w4a16_status w4a16_device_status(int clear) {
         if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
             return W4A16_ERR_CUDA;
     }
-    return v == 0 ? W4A16_OK : W4A16_ERR_TIMEOUT;
+    if (v == 0) return W4A16_OK;
+    return v == kStatusBadBlob ? W4A16_ERR_UNSUPPORTED : W4A16_ERR_TIMEOUT;
+}
+
+w4a16_status w4a16_packed_check(const void* packed, int K, int N, int group_size, int has_zeros,
+                                void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (packed == nullptr) return W4A16_ERR_NULL;
+    if (!aligned16(packed)) return W4A16_ERR_ALIGN;
+    uint32_t got[4] = {0, 0, 0, 0};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const char* tag = static_cast<const char*>(packed) + packed_tag_offset(K, N, has_zeros != 0);
+    if (cudaMemcpyAsync(got, tag, sizeof got, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    const BlobTag want = blob_tag(K, N, has_zeros != 0);
+    if (got[0] != want.w[0] || got[1] != want.w[1]) return W4A16_ERR_UNSUPPORTED;
+    if (got[2] != want.w[2] || got[3] != want.w[3]) return W4A16_ERR_SHAPE;
+    return W4A16_OK;
 }
 
 const char* w4a16_status_string(w4a16_status status) {

@@ -107,6 +107,12 @@ __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t zero2, uint
     for (int i = 0; i < 4; ++i) out[i] = dequant_pair(word, i, zero2, scale2);
 }
 
+// Device check of a packed blob's tag (see launch.cuh): one 16-byte load.
+__device__ __forceinline__ bool blob_tag_matches(const uint8_t* tag, const uint32_t (&want)[4]) {
+    const uint4 t = *reinterpret_cast<const uint4*>(tag);
+    return t.x == want[0] && t.y == want[1] && t.z == want[2] && t.w == want[3];
+}
+
 // Words per group row of the packed zero-points (N/8 rounded up to 4).
 __host__ __device__ inline int packed_zero_row_words(int N) { return ((N >> 3) + 3) & ~3; }
 

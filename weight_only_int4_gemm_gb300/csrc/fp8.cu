@@ -614,7 +614,7 @@ cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx,
     const size_t smem = smem_bytes(p.bn);
     const void* kern = reinterpret_cast<const void*>(fp8_gemm_kernel);
     cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_smem_limit(kern, smem);
     if (err != cudaSuccess) return err;
     void* args[] = {&xmap, &a};
     return launch_with_pdl(kern, dim3(std::min(a.items, p.grid)), dim3(kThreads), smem, stream,

@@ -16,6 +16,30 @@ inline size_t packed_zero_bytes(int K, int N) {
 }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Every packed blob ends with a 16-byte tag, written by the repack kernel:
+// {kBlobMagic, layout version, K, N | has_zeros << 31}.  A GEMM kernel reads
+// it once per CTA and records W4A16_ERR_UNSUPPORTED in the device status word
+// if it does not describe the call (a blob from another layout version or
+// another shape); w4a16_packed_check reads it on the host.
+constexpr size_t kBlobTagBytes = 16;
+constexpr uint32_t kBlobMagic = 0x70413457u;  // bytes 'W' '4' 'A' 'p'
+constexpr uint32_t kBlobLayout = 3;           // W4A16_PACKED_LAYOUT
+constexpr unsigned int kStatusBadBlob = 4;    // W4A16_ERR_UNSUPPORTED
+inline size_t packed_tag_offset(int K, int N, bool has_zeros) {
+    return packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);
+}
+inline size_t packed_total_bytes(int K, int N, bool has_zeros) {
+    return packed_tag_offset(K, N, has_zeros) + kBlobTagBytes;
+}
+// The tag a (K, N, has_zeros) call expects.
+struct BlobTag {
+    uint32_t w[4];
+};
+inline BlobTag blob_tag(int K, int N, bool has_zeros) {
+    return BlobTag{{kBlobMagic, kBlobLayout, (uint32_t)K,
+                    (uint32_t)N | (has_zeros ? 0x80000000u : 0u)}};
+}
+
 // Workspace layout shared by every kernel: a fixed prefix of counters
 // (per-tile arrival counters and the small-batch kernel's work-scheduler
 // words) and, after it, one fp32 accumulator [B][N] that split-K kernels add
@@ -38,6 +62,10 @@ struct Epilogue {
     const uint16_t* bias = nullptr;  // bf16 [N] with kEpiBias
     int mode = 0;
 };
+
+// Sets a kernel's dynamic shared-memory limit once per (device, kernel):
+// repeated calls with a size it already allows return at once.
+cudaError_t set_smem_limit(const void* kernel, size_t bytes);
 
 // Programmatic dependent launch: kernels may start (and prefetch weights)
 // while the previous kernel on the stream finishes; they wait before reading

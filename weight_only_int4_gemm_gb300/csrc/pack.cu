@@ -13,9 +13,11 @@ constexpr int kPackThreads = 256;
 // One thread per (chunk c, column n): gathers the four canonical words of rows
 // 32c .. 32c+31 of column n and moves every code to its packed nibble.
 __global__ void __launch_bounds__(kPackThreads)
-repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, int K, int N) {
+repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, int K, int N,
+              uint4* __restrict__ tag, uint4 tag_value) {
     const int n = blockIdx.x * kPackThreads + threadIdx.x;
     const int c = blockIdx.y;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *tag = tag_value;
     if (n >= N) return;
     uint32_t out[4];
 #pragma unroll
@@ -61,7 +63,11 @@ dequant_ref_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict_
 cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K, int N,
                           void* packed, cudaStream_t stream) {
     dim3 grid((N + kPackThreads - 1) / kPackThreads, K / 32);
-    repack_kernel<<<grid, kPackThreads, 0, stream>>>(qweight, static_cast<uint4*>(packed), K, N);
+    const BlobTag t = blob_tag(K, N, qzeros != nullptr);
+    uint4* tag = reinterpret_cast<uint4*>(static_cast<char*>(packed) +
+                                          packed_tag_offset(K, N, qzeros != nullptr));
+    repack_kernel<<<grid, kPackThreads, 0, stream>>>(qweight, static_cast<uint4*>(packed), K, N,
+                                                     tag, make_uint4(t.w[0], t.w[1], t.w[2], t.w[3]));
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || qzeros == nullptr) return err;
     // zero-points: one group per row, rows padded with zero words to 16 bytes

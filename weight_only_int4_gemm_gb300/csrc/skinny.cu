@@ -101,6 +101,8 @@ struct Args {
     int E;
     size_t w_stride, s_stride;
     Epilogue epi;        // fused output epilogue (plain bf16 when mode == 0)
+    const uint8_t* tag;  // the packed blob's tag (the first expert's when grouped)
+    uint32_t tag_want[4];
 };
 
 constexpr int kMaxExperts = 256;
@@ -376,6 +378,8 @@ skinny_kernel(const Args a) {
         int issued = 0;      // ring positions fully issued
         int w_issued = 0;    // ring positions whose code copy is issued
         bool ok = true;
+        if (lane == 0 && !blob_tag_matches(a.tag, a.tag_want))
+            atomicExch(a.status, kStatusBadBlob);  // not a blob of this layout / shape
         // The first unit is fixed (blockIdx.x): its first slots' code copies go
         // out before waiting for the previous kernel on the stream.
         const bool has_first = (int)blockIdx.x < total_units;
@@ -696,8 +700,7 @@ cudaError_t launch_t(const SkinnyPlan& p, Args a, cudaStream_t stream) {
         a.offsets != nullptr ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kGrouped>)
         : a.epi.mode != 0    ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kFusedEpi>)
                              : reinterpret_cast<const void*>(skinny_kernel<NT, Z, kPlain>);
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    cudaError_t err = set_smem_limit(kern, smem);
     if (err != cudaSuccess) return err;
     void* args[] = {&a};
     return launch_with_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, args);
@@ -807,7 +810,10 @@ static cudaError_t launch_skinny_impl(const SkinnyPlan& p, const void* x, const 
     a.units = p.units;
     a.offsets = offsets;
     a.E = E;
-    a.w_stride = packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);
+    a.w_stride = packed_total_bytes(K, N, has_zeros);
+    a.tag = a.packed + packed_tag_offset(K, N, has_zeros);
+    const BlobTag want = blob_tag(K, N, has_zeros);
+    for (int i = 0; i < 4; ++i) a.tag_want[i] = want.w[i];
     a.s_stride = (size_t)(K / kGroup) * N;
     a.epi = epi;
     switch (p.nt * 2 + (has_zeros ? 1 : 0)) {

@@ -115,6 +115,8 @@ struct Args {
     int x3d;               // x of a stage is one 3-D box (else one 2-D box per block)
     int force_timeout;     // test hook: wait on a barrier nobody arrives at
     Epilogue epi;          // fused output epilogue (plain bf16 when mode == 0)
+    const uint8_t* tag;    // the packed blob's tag
+    uint32_t tag_want[4];
 };
 
 // ------------------------------------------------------------ kernel
@@ -283,6 +285,8 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
     if (warp == 0 || warp == kProducer1Warp) {
         // ---------------- TMA producers: producer pr takes copy stages pr, pr+2, ...
         const int pr = warp == 0 ? 0 : 1;
+        if (lane == 0 && pr == 0 && !blob_tag_matches(a.tag, a.tag_want))
+            atomicExch(a.status, kStatusBadBlob);  // not a blob of this layout / shape
         if (lane == 0) {
             const Item first = decode_item(a, blockIdx.x);
             const int pre = min(RC, first.ncs);
@@ -862,6 +866,11 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     a.x3d = x3d;
     a.force_timeout = force_timeout_ms;
     a.epi = epi;
+    a.tag = a.packed + packed_tag_offset(K, N, has_zeros);
+    {
+        const BlobTag want = blob_tag(K, N, has_zeros);
+        for (int i = 0; i < 4; ++i) a.tag_want[i] = want.w[i];
+    }
     if (a.a_slots < 4 || a.code_slots < 2 || a.x_slots < 2) return cudaErrorInvalidConfiguration;
 
     const size_t smem = lay.smem;
@@ -872,7 +881,7 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
                   : (fused ? reinterpret_cast<const void*>(tc_kernel<false, true>)
                            : reinterpret_cast<const void*>(tc_kernel<false, false>));
     cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_smem_limit(kern, smem);
     if (err != cudaSuccess) return err;
     void* args[] = {&xmap, &smap, &zmap, &a};
     const int grid = std::min(a.items, p.grid);

@@ -129,6 +129,8 @@ struct Args {
     int zrow_words;     // words per padded zero-point row
     int force_timeout;  // test hook: wait on a barrier nobody arrives at
     Epilogue epi;       // fused output epilogue (plain bf16 when mode == 0)
+    const uint8_t* tag; // the packed blob's tag
+    uint32_t tag_want[4];
 };
 
 // ------------------------------------------------------------ kernel
@@ -269,6 +271,8 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
 
     if (warp == kCodeWarp) {
         // ---------------- code stages: one per 128-row group
+        if (lane == 0 && !blob_tag_matches(a.tag, a.tag_want))
+            atomicExch(a.status, kStatusBadBlob);  // not a blob of this layout / shape
         if (lane == 0) {
             Ring q;
             int issued = 0;
@@ -816,6 +820,11 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.zrow_words = packed_zero_row_words(N);
     a.force_timeout = force_timeout_ms;
     a.epi = epi;
+    a.tag = a.packed + packed_tag_offset(K, N, has_zeros);
+    {
+        const BlobTag want = blob_tag(K, N, has_zeros);
+        for (int i = 0; i < 4; ++i) a.tag_want[i] = want.w[i];
+    }
 
     const size_t smem = lay.smem;
     const bool fused = epi.mode != 0;
@@ -831,7 +840,7 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
         default: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 2>); break;
     }
     cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_smem_limit(kern, smem);
     if (err != cudaSuccess) return err;
     void* args[] = {&xmap, &a};
     const int grid = std::min(a.items, p.grid);
