@@ -69,8 +69,11 @@ typedef enum {
     W4A16_ERR_UNSUPPORTED = 4, /* group_size != 128, or an unknown path id */
     W4A16_ERR_WORKSPACE = 5,   /* workspace smaller than w4a16_workspace_bytes() */
     W4A16_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
-    W4A16_ERR_TIMEOUT = 7      /* a device-side bounded wait ran out (see
+    W4A16_ERR_TIMEOUT = 7,     /* a device-side bounded wait ran out (see
                                   w4a16_device_status) */
+    W4A16_ERR_BOUNDS = 8       /* a device-side bounds check failed; only the
+                                  debug build (W4A16_DEBUG) checks, reported by
+                                  w4a16_device_status */
 } w4a16_status;
 
 /* Kernel paths the dispatcher chooses from (w4a16_select_path, forcing). */
@@ -251,9 +254,11 @@ const char *w4a16_kernel_name(int B, int K, int N);
 
 /* Device-side status word of the GEMM kernels: W4A16_OK when every bounded
  * wait completed and every packed blob's tag matched its call, else
- * W4A16_ERR_TIMEOUT (a bounded wait ran out) or W4A16_ERR_UNSUPPORTED (a GEMM
+ * W4A16_ERR_TIMEOUT (a bounded wait ran out), W4A16_ERR_UNSUPPORTED (a GEMM
  * was given a blob whose tag does not describe it: another layout version,
- * shape or zero-point flag -- its output is then meaningless).  Synchronises
+ * shape or zero-point flag -- its output is then meaningless) or, in the
+ * debug build only, W4A16_ERR_BOUNDS (an index check failed; the access was
+ * skipped).  Synchronises
  * the current device; clears the word when `clear` != 0.  Returns
  * W4A16_ERR_CUDA if the query itself fails. */
 w4a16_status w4a16_device_status(int clear);
@@ -291,6 +296,23 @@ w4a16_status w4a16_debug_forced_timeout(const void *x, const void *packed, const
                                         int has_zeros, void *y, int B, int K, int N,
                                         int group_size, void *workspace, size_t ws_bytes,
                                         int wait_ms, void *stream);
+
+/* 1 for the debug build of the library (compiled with W4A16_DEBUG), else 0.
+ * In the debug build every global load, copy and store of the GEMM kernels is
+ * preceded by a check of its index against the extent of the buffer it
+ * touches; a failed check skips that access (so no wait is left hanging and
+ * no memory outside the buffer is touched) and records W4A16_ERR_BOUNDS in
+ * the device status word instead of trapping.  Same C ABI, same results. */
+int w4a16_debug_build(void);
+
+/* Test hook of the debug build (no counterpart on the pages): later GEMM
+ * launches on this process tell their kernels that the packed codes end
+ * `bytes` bytes earlier than they do (0 restores the true extent), so the
+ * kernels' own checks skip the last copies and report W4A16_ERR_BOUNDS; the
+ * memory touched stays inside the real blob and every wait still ends, but
+ * the outputs of those launches are meaningless.  Returns
+ * W4A16_ERR_UNSUPPORTED in the release build. */
+w4a16_status w4a16_debug_shrink_code_bound(size_t bytes);
 
 /* Checks a packed blob's tag against the layout version this library reads
  * and the call's shape: W4A16_OK, W4A16_ERR_UNSUPPORTED when the blob was

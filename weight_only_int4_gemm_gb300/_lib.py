@@ -8,6 +8,7 @@ fallback of any kind -- if the library is missing, loading fails loudly.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -24,7 +25,7 @@ PATH_NAMES = {PATH_SKINNY: "skinny", PATH_TCGEN05: "tcgen05"}
 
 _STATUS = {0: "W4A16_OK", 1: "W4A16_ERR_NULL", 2: "W4A16_ERR_SHAPE", 3: "W4A16_ERR_ALIGN",
            4: "W4A16_ERR_UNSUPPORTED", 5: "W4A16_ERR_WORKSPACE", 6: "W4A16_ERR_CUDA",
-           7: "W4A16_ERR_TIMEOUT"}
+           7: "W4A16_ERR_TIMEOUT", 8: "W4A16_ERR_BOUNDS"}
 
 # (name, restype, argtypes) of every exported symbol, in header order.
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -46,6 +47,8 @@ SIGNATURES = {
     "w4a16_grouped_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "w4a16_gemm_grouped": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
+    "w4a16_debug_build": (_I, []),
+    "w4a16_debug_shrink_code_bound": (_I, [_S]),
     # include/w8a8_fp8.h
     "w8a8_fp8_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
     "w8a8_fp8_quantize_weight": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -64,10 +67,19 @@ class W4A16Error(RuntimeError):
 
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
+DEBUG_LIB_PATH = os.path.join(_HERE, "libw4a16_debug.so")
+
+
+_active = threading.local()
 
 
 def load() -> ctypes.CDLL:
-    """Load the CUDA library (raises if it has not been built)."""
+    """Load the CUDA library (raises if it has not been built); inside
+    `debug_library()` the debug build instead."""
+    lib = getattr(_active, "lib", None)
+    if lib is not None:
+        return lib
     global _lib
     with _lock:
         if _lib is not None:
@@ -83,6 +95,36 @@ def load() -> ctypes.CDLL:
             fn.argtypes = args
         _lib = lib
         return lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """The debug build of the library (W4A16_DEBUG: device-side bounds checks
+    that report W4A16_ERR_BOUNDS through w4a16_device_status), with the same
+    C ABI; raises if it has not been built (build.build_library(debug=True))."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is not None:
+            return _debug_lib
+        if not os.path.exists(DEBUG_LIB_PATH):
+            raise RuntimeError(f"debug library not built: {DEBUG_LIB_PATH} is missing")
+        lib = ctypes.CDLL(DEBUG_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _debug_lib = lib
+        return lib
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Route this thread's calls of the binding to the debug build."""
+    prev = getattr(_active, "lib", None)
+    _active.lib = load_debug()
+    try:
+        yield _active.lib
+    finally:
+        _active.lib = prev
 
 
 def _check(fn: str, status: int):

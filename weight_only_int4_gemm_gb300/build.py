@@ -15,6 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libw4a16.so")
+DEBUG_OUT_DIR = os.path.join(ROOT, "_build", "debug")
+DEBUG_LIB = os.path.join(PKG, "libw4a16_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -37,10 +39,11 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, extra: list[str], verbose: bool) -> str:
-    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], verbose: bool, out_dir: str = OUT_DIR,
+             cacheable: bool = True) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src) + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()) \
-            and not extra:
+            and cacheable:
         return obj
     cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
@@ -53,24 +56,33 @@ def _compile(src: str, extra: list[str], verbose: bool) -> str:
     return obj
 
 
-def build_library(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+                  debug: bool = False) -> str:
+    """Compile libw4a16.so (or, with debug=True, libw4a16_debug.so: the same
+    sources with -DW4A16_DEBUG, whose kernels bounds-check their global
+    accesses and report W4A16_ERR_BOUNDS instead of trapping)."""
+    out_dir, lib = (DEBUG_OUT_DIR, DEBUG_LIB) if debug else (OUT_DIR, LIB)
+    os.makedirs(out_dir, exist_ok=True)
     extra = list(extra or [])
+    cacheable = not extra
+    if debug:
+        extra.append("-DW4A16_DEBUG")
     srcs = sources()
     newest = max([os.path.getmtime(s) for s in srcs] + [_headers_mtime()])
-    if not force and not extra and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
+    if not force and cacheable and os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return lib
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra, verbose), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, verbose, out_dir, cacheable), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build_library(force="--force" in sys.argv, verbose=True,
-                        extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None))
+                        extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None,
+                        debug="--debug" in sys.argv))

@@ -3,11 +3,13 @@
 // w4a16_device_status, which is documented to).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
 #include "w4a16.h"
 #include "w8a8_fp8.h"
+#include "checks.cuh"
 #include "launch.cuh"
 
 namespace w4a16 {
@@ -178,6 +180,20 @@ int gemm_entry(const void* x, const void* packed, const void* scales, int has_ze
 size_t auto_workspace_bytes(int B, int K, int N, int group_size) {
     if (group_size != kGroup || !shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
     return path_workspace(choose_path(B, K, N), B, K, N);
+}
+
+#ifdef W4A16_DEBUG
+static std::atomic<size_t> g_code_bound_cut{0};
+#endif
+
+size_t code_bound_bytes(int K, int N) {
+    const size_t full = packed_code_bytes(K, N);
+#ifdef W4A16_DEBUG
+    const size_t cut = g_code_bound_cut.load(std::memory_order_relaxed);
+    return cut < full ? full - cut : 0;
+#else
+    return full;
+#endif
 }
 
 cudaError_t set_smem_limit(const void* kernel, size_t bytes) {
@@ -406,7 +422,26 @@ w4a16_status w4a16_device_status(int clear) {
             return W4A16_ERR_CUDA;
     }
     if (v == 0) return W4A16_OK;
-    return v == kStatusBadBlob ? W4A16_ERR_UNSUPPORTED : W4A16_ERR_TIMEOUT;
+    if (v == kStatusBadBlob) return W4A16_ERR_UNSUPPORTED;
+    return v == kStatusBounds ? W4A16_ERR_BOUNDS : W4A16_ERR_TIMEOUT;
+}
+
+int w4a16_debug_build(void) {
+#ifdef W4A16_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+w4a16_status w4a16_debug_shrink_code_bound(size_t bytes) {
+#ifdef W4A16_DEBUG
+    g_code_bound_cut.store(bytes, std::memory_order_relaxed);
+    return W4A16_OK;
+#else
+    (void)bytes;
+    return W4A16_ERR_UNSUPPORTED;
+#endif
 }
 
 w4a16_status w4a16_packed_check(const void* packed, int K, int N, int group_size, int has_zeros,
@@ -437,6 +472,7 @@ const char* w4a16_status_string(w4a16_status status) {
         case W4A16_ERR_WORKSPACE: return "workspace too small";
         case W4A16_ERR_CUDA: return "CUDA error";
         case W4A16_ERR_TIMEOUT: return "device-side wait timed out";
+        case W4A16_ERR_BOUNDS: return "device-side bounds check failed (debug build)";
     }
     return "unknown status";
 }

@@ -63,6 +63,11 @@ struct Epilogue {
     int mode = 0;
 };
 
+// Extent of the packed codes the kernels' bounds checks compare against:
+// packed_code_bytes(K, N), less the debug build's test cut
+// (w4a16_debug_shrink_code_bound).
+size_t code_bound_bytes(int K, int N);
+
 // Sets a kernel's dynamic shared-memory limit once per (device, kernel):
 // repeated calls with a size it already allows return at once.
 cudaError_t set_smem_limit(const void* kernel, size_t bytes);

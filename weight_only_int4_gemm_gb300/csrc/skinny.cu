@@ -51,6 +51,7 @@
 
 #include <algorithm>
 
+#include "checks.cuh"
 #include "dequant.cuh"
 #include "epilogue.cuh"
 #include "launch.cuh"
@@ -103,6 +104,8 @@ struct Args {
     Epilogue epi;        // fused output epilogue (plain bf16 when mode == 0)
     const uint8_t* tag;  // the packed blob's tag (the first expert's when grouped)
     uint32_t tag_want[4];
+    size_t code_bytes;   // packed codes of one expert (bounds checks)
+    int zrow_words;      // words per padded zero-point row (bounds checks)
 };
 
 constexpr int kMaxExperts = 256;
@@ -389,15 +392,19 @@ skinny_kernel(const Args a) {
             const int s = pos % S;
             const int g0 = w.g_begin + st * kSlotGroups;
             const int ngs = min(kSlotGroups, w.g_begin + w.ng - g0);
-            const uint32_t bytes = (uint32_t)ngs * 4 * w.width * 16;
+            uint32_t bytes = (uint32_t)ngs * 4 * w.width * 16;
+            const uint8_t* src = tile_codes + (size_t)(4 * g0) * w.width * 16;
+            if (!in_bounds(src >= w.packed && src + bytes <= w.packed + a.code_bytes, a.status))
+                bytes = 0;  // debug build: skip the copy (the barrier still completes)
             const uint32_t full = smem_u32(&tail->full[s]);
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full),
                          "r"(bytes)
                          : "memory");
+            if (bytes == 0) return;
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
                 "[%0], [%1], %2, [%3], %4;"
-                ::"r"(smem_u32(slot_codes(s))), "l"(tile_codes + (size_t)(4 * g0) * w.width * 16),
+                ::"r"(smem_u32(slot_codes(s))), "l"(src),
                 "r"(bytes), "r"(full), "l"(evict_first)
                 : "memory");
         };
@@ -460,16 +467,19 @@ skinny_kernel(const Args a) {
                 const int p = lane & 15;
                 for (int gl = 0; gl < ngs; ++gl)
                     for (int r = lane >> 4; r < w.rows; r += 2)
-                        cp_async_16(xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
-                                    a.x + (size_t)(w.b0 + r) * a.K + (size_t)kGroup * (g0 + gl) +
-                                        8 * p);
+                        if (in_bounds(w.b0 + r < a.B && kGroup * (g0 + gl) + 8 * p + 8 <= a.K,
+                                      a.status))
+                            cp_async_16(
+                                xbase + 16u * (((gl * 4 + (p & 3)) * kRows + r) * 4 + (p >> 2)),
+                                a.x + (size_t)(w.b0 + r) * a.K + (size_t)kGroup * (g0 + gl) + 8 * p);
                 const int gl = lane >> 4;
-                if (gl < ngs && p < w.width / 8) {
+                if (gl < ngs && p < w.width / 8 &&
+                    in_bounds(g0 + gl < a.K / kGroup && w.n0 + 8 * p + 8 <= a.N, a.status)) {
                     cp_async_16(smem_u32(slot_scales(s)) + 2u * (gl * kTileCols + 8 * p),
                                 w.scales + (size_t)(g0 + gl) * a.N + w.n0 + 8 * p);
-                    if (kHasZeros)
+                    if (kHasZeros && in_bounds(w.n0 / 8 + p < a.zrow_words, a.status))
                         cp_async_4(smem_u32(slot_zeros(s)) + 4u * (gl * (kTileCols / 8) + p),
-                                   w.zeros + (size_t)(g0 + gl) * packed_zero_row_words(a.N) + w.n0 / 8 + p);
+                                   w.zeros + (size_t)(g0 + gl) * a.zrow_words + w.n0 / 8 + p);
                 }
                 cp_async_arrive_noinc(full);
                 issued = step + 1;
@@ -635,6 +645,7 @@ skinny_kernel(const Args a) {
                 const float v0 = elem(c4, b), v1 = elem(c4 + 1, b), v2 = elem(c4 + 2, b),
                             v3 = elem(c4 + 3, b);
                 const size_t off = (size_t)(w.b0 + b) * a.N + w.n0 + c4;
+                if (!in_bounds(w.b0 + b < a.B && w.n0 + c4 + 4 <= a.N, a.status)) continue;
                 if (a.split == 1) {
                     if constexpr (kMode == kFusedEpi)
                         epi_store4_fused(a.y, a.N, w.b0 + b, w.n0 + c4, v0, v1, v2, v3, a.epi);
@@ -654,6 +665,8 @@ skinny_kernel(const Args a) {
                 __threadfence();
                 __syncwarp();
                 uint32_t* counter = a.counters + (size_t)w.bc * a.tiles + w.tile;
+                if (!in_bounds((size_t)w.bc * a.tiles + w.tile < (size_t)kWorkCounter, a.status))
+                    continue;
                 uint32_t prev = 0;
                 if (lane == 0)
                     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
@@ -667,12 +680,13 @@ skinny_kernel(const Args a) {
                         float4 v[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            if (b0 + j < w.rows)
+                            if (b0 + j < w.rows &&
+                                in_bounds(w.b0 + b0 + j < a.B && w.n0 + c4 + 4 <= a.N, a.status))
                                 v[j] = __ldcg(reinterpret_cast<const float4*>(
                                     a.partial + (size_t)(w.b0 + b0 + j) * a.N + w.n0 + c4));
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            if (b0 + j < w.rows) {
+                            if (b0 + j < w.rows && w.b0 + b0 + j < a.B && w.n0 + c4 + 4 <= a.N) {
                                 const size_t off = (size_t)(w.b0 + b0 + j) * a.N + w.n0 + c4;
                                 if constexpr (kMode == kFusedEpi)
                                     epi_store4_fused(a.y, a.N, w.b0 + b0 + j, w.n0 + c4, v[j].x,
@@ -812,6 +826,8 @@ static cudaError_t launch_skinny_impl(const SkinnyPlan& p, const void* x, const 
     a.E = E;
     a.w_stride = packed_total_bytes(K, N, has_zeros);
     a.tag = a.packed + packed_tag_offset(K, N, has_zeros);
+    a.code_bytes = code_bound_bytes(K, N);
+    a.zrow_words = packed_zero_row_words(N);
     const BlobTag want = blob_tag(K, N, has_zeros);
     for (int i = 0; i < 4; ++i) a.tag_want[i] = want.w[i];
     a.s_stride = (size_t)(K / kGroup) * N;

@@ -51,6 +51,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "checks.cuh"
 #include "dequant.cuh"
 #include "epilogue.cuh"
 #include "launch.cuh"
@@ -117,6 +118,7 @@ struct Args {
     Epilogue epi;          // fused output epilogue (plain bf16 when mode == 0)
     const uint8_t* tag;    // the packed blob's tag
     uint32_t tag_want[4];
+    size_t code_bytes;     // packed codes (bounds checks)
 };
 
 // ------------------------------------------------------------ kernel
@@ -187,12 +189,12 @@ __device__ __forceinline__ void issue_weight_copies(const Args& a, const CUtenso
                                                     int c, uint8_t* slot, uint32_t bar) {
     const int kb0 = t.kb_begin + c * a.nsub;
     const int ng = a.nsub > 1 ? a.nsub >> 1 : 1;
-    const uint32_t cb = (uint32_t)a.nsub * 2u * (uint32_t)t.nvalid * 16u;
+    uint32_t cb = (uint32_t)a.nsub * 2u * (uint32_t)t.nvalid * 16u;
+    const size_t off = packed_tile_base(a.K, t.col_tile) + (size_t)(2 * kb0) * t.nvalid * 16;
+    if (!in_bounds(off + cb <= a.code_bytes, a.status)) cb = 0;  // debug build: skip the copy
     const uint32_t zbytes = kHasZeros ? (uint32_t)ng * kZeroRowBytes : 0u;
     mbar_arrive_expect_tx(bar, cb + (uint32_t)ng * kScaleRowBytes + zbytes);
-    bulk_g2s(smem_u32(slot),
-             a.packed + packed_tile_base(a.K, t.col_tile) + (size_t)(2 * kb0) * t.nvalid * 16, cb,
-             bar);
+    if (cb != 0) bulk_g2s(smem_u32(slot), a.packed + off, cb, bar);
     tma_load_2d(smem_u32(slot + a.scale_off), smap, t.n0, kb0 >> 1, bar);
     if (kHasZeros) tma_load_2d(smem_u32(slot + a.zero_off), zmap, t.n0 >> 3, kb0 >> 1, bar);
 }
@@ -570,6 +572,9 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                 __threadfence();
                 epilogue_bar();
                 uint32_t* counter = a.counters + (size_t)t.batch_tile * a.col_tiles + t.col_tile;
+                if (!in_bounds((size_t)t.batch_tile * a.col_tiles + t.col_tile < (size_t)kMaxCounters,
+                               a.status))
+                    counter = a.counters;  // debug build: a valid word (the sum is then wrong)
                 if (warp == kEpilogueWarp0 && lane == 0) {
                     uint32_t prev;
                     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
@@ -594,8 +599,9 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                             const int e = e0 + 128 * jj;
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
-                                v[jj] = __ldcg(reinterpret_cast<const float4*>(
-                                    a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
+                                if (in_bounds(t.b0 + rr < a.B && t.n0 + cc + 4 <= a.N, a.status))
+                                    v[jj] = __ldcg(reinterpret_cast<const float4*>(
+                                        a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
                             }
                         }
 #pragma unroll
@@ -604,6 +610,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - (e / c4n) * c4n);
                                 const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
+                                if (t.b0 + rr >= a.B || t.n0 + cc + 4 > a.N) continue;
                                 if constexpr (kFused)
                                     epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x, v[jj].y,
                                            v[jj].z, v[jj].w, a.epi);
@@ -867,6 +874,7 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     a.force_timeout = force_timeout_ms;
     a.epi = epi;
     a.tag = a.packed + packed_tag_offset(K, N, has_zeros);
+    a.code_bytes = code_bound_bytes(K, N);
     {
         const BlobTag want = blob_tag(K, N, has_zeros);
         for (int i = 0; i < 4; ++i) a.tag_want[i] = want.w[i];

@@ -66,6 +66,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "checks.cuh"
 #include "dequant.cuh"
 #include "epilogue.cuh"
 #include "launch.cuh"
@@ -131,6 +132,7 @@ struct Args {
     Epilogue epi;       // fused output epilogue (plain bf16 when mode == 0)
     const uint8_t* tag; // the packed blob's tag
     uint32_t tag_want[4];
+    size_t code_bytes;  // packed codes (bounds checks)
 };
 
 // ------------------------------------------------------------ kernel
@@ -194,9 +196,14 @@ __device__ __forceinline__ void issue_code_stage(const Args& a, const Item& t, i
     const uint32_t cb = 4u * (uint32_t)t.nvalid * 16u;      // 4 chunks of 32 rows
     const uint32_t sb = (uint32_t)t.nvalid * 2u;            // multiple of 16 (N % 8 == 0)
     const uint32_t zb = kHasZeros ? (((uint32_t)t.nvalid / 2u + 15u) & ~15u) : 0u;
-    mbar_arrive_expect_tx(bar, cb + sb + zb);
-    bulk_g2s(smem_u32(slot), a.packed + packed_tile_base(a.K, t.col_tile) +
-                                 (size_t)(4 * g) * t.nvalid * 16, cb, bar);
+    const size_t off = packed_tile_base(a.K, t.col_tile) + (size_t)(4 * g) * t.nvalid * 16;
+    const bool ok = in_bounds(off + cb <= a.code_bytes && g < a.ngroups &&
+                                  t.n0 + t.nvalid <= a.N &&
+                                  (!kHasZeros || (size_t)(t.n0 / 8) * 4 + zb <= (size_t)a.zrow_words * 4),
+                              a.status);
+    mbar_arrive_expect_tx(bar, ok ? cb + sb + zb : 0u);  // debug build: skip the copies
+    if (!ok) return;
+    bulk_g2s(smem_u32(slot), a.packed + off, cb, bar);
     bulk_g2s(smem_u32(slot + kStageCodeBytes), a.scales + (size_t)g * a.N + t.n0, sb, bar);
     if (kHasZeros)
         bulk_g2s(smem_u32(slot + kStageCodeBytes + kScaleRowBytes),
@@ -529,7 +536,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                             const float4 lo = *reinterpret_cast<const float4*>(buf + i * kEpiRow + c8);
                             const float4 hi =
                                 *reinterpret_cast<const float4*>(buf + i * kEpiRow + c8 + 4);
-                            if (b < a.B && n < a.N) {
+                            if (b < a.B && n < a.N && in_bounds(n + 8 <= a.N, a.status)) {
                                 if constexpr (kFused) {
                                     epi_store4_fused(a.y, a.N, b, n, lo.x, lo.y, lo.z, lo.w, a.epi);
                                     epi_store4_fused(a.y, a.N, b, n + 4, hi.x, hi.y, hi.z, hi.w, a.epi);
@@ -551,7 +558,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                             const int b = t.b0 + c0 + i;
                             const int n = nq + c4;
                             const float4 p = *reinterpret_cast<const float4*>(buf + i * kEpiRow + c4);
-                            if (b < a.B && n < a.N)
+                            if (b < a.B && n < a.N && in_bounds(n + 4 <= a.N, a.status))
                                 asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                                              ::"l"(a.partial + (size_t)b * a.N + n), "f"(p.x),
                                              "f"(p.y), "f"(p.z), "f"(p.w)
@@ -571,6 +578,9 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 __threadfence();
                 epilogue_bar();
                 uint32_t* counter = a.counters + (size_t)t.batch_tile * a.col_tiles + t.col_tile;
+                if (!in_bounds((size_t)t.batch_tile * a.col_tiles + t.col_tile < (size_t)kMaxCounters,
+                               a.status))
+                    counter = a.counters;  // debug build: a valid word (the sum is then wrong)
                 if (warp == kEpilogueWarp0 && lane == 0) {
                     uint32_t prev;
                     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
@@ -595,8 +605,9 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                             const int e = e0 + 128 * jj;
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - rr * c4n);
-                                v[jj] = __ldcg(reinterpret_cast<const float4*>(
-                                    a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
+                                if (in_bounds(t.b0 + rr < a.B && t.n0 + cc + 4 <= a.N, a.status))
+                                    v[jj] = __ldcg(reinterpret_cast<const float4*>(
+                                        a.partial + (size_t)(t.b0 + rr) * a.N + t.n0 + cc));
                             }
                         }
 #pragma unroll
@@ -605,6 +616,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                             if (e < total) {
                                 const int rr = e / c4n, cc = 4 * (e - rr * c4n);
                                 const size_t off = (size_t)(t.b0 + rr) * a.N + t.n0 + cc;
+                                if (t.b0 + rr >= a.B || t.n0 + cc + 4 > a.N) continue;
                                 if constexpr (kFused)
                                     epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x,
                                                      v[jj].y, v[jj].z, v[jj].w, a.epi);
@@ -821,6 +833,7 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.force_timeout = force_timeout_ms;
     a.epi = epi;
     a.tag = a.packed + packed_tag_offset(K, N, has_zeros);
+    a.code_bytes = code_bound_bytes(K, N);
     {
         const BlobTag want = blob_tag(K, N, has_zeros);
         for (int i = 0; i < 4; ++i) a.tag_want[i] = want.w[i];
