@@ -17,6 +17,10 @@ Sources, by page title and section:
     its own rows (``gemm_grouped``).
   * "Give Me BF16 or Give Me Death", "W4A16-INT Quantization": round to
     nearest with MSE-optimal clipping (``quantize_rtn_mse``).
+  * "Give Me BF16 or Give Me Death", "W4A16-INT Quantization", paragraph
+    "Inference with W4A16": the same layer with fp16 activations, scales,
+    weights and output (``f16_*``, ``dequant_f16``, ``gemm_f16``; C source
+    ``w4a16_f16_oracle.c``).
   * "Give Me BF16 or Give Me Death", "W8A8-FP Quantization": per-channel FP8
     weights, dynamic per-token FP8 activations, their product
     (``fp8_quantize_rows``, ``fp8_quantize_cols``, ``fp8_gemm``; C source
@@ -30,7 +34,9 @@ force, invariants, hand-built unpack cases, the 4.125-bit accounting),
 bias and SiLU-gate cases, an independent tanh route to silu) and
 ``tests/test_fp8_pins.py`` (E4M3 codec
 against the format's published constants and brute-force nearest search,
-scale invariants, exact integer GEMM).
+scale invariants, exact integer GEMM) and ``tests/test_f16_pins.py`` (binary16
+codec against numpy's float16 and an exhaustive tie enumeration, every code
+times every finite fp16 scale against numpy, exact-rational brute force).
 """
 from __future__ import annotations
 
@@ -43,7 +49,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "w4a16_oracle.c")
-_SRCS = [_SRC, os.path.join(_HERE, "w8a8_fp8_oracle.c")]
+_SRCS = [_SRC, os.path.join(_HERE, "w8a8_fp8_oracle.c"), os.path.join(_HERE, "w4a16_f16_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -108,6 +114,19 @@ def _load():
         lib.oracle_fp8_gemm_cols.argtypes = [u8p, f32p, u8p, f32p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
         lib.oracle_fp8_gemm_cols.restype = None
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_double.restype = ctypes.c_double
+        lib.oracle_f16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_f16_from_double.restype = ctypes.c_uint16
+        lib.oracle_f16_from_double_array.argtypes = [f64p, ctypes.c_longlong, u16p]
+        lib.oracle_f16_from_double_array.restype = None
+        lib.oracle_dequant_one_f16.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint16]
+        lib.oracle_dequant_one_f16.restype = ctypes.c_uint16
+        lib.oracle_dequant_f16.argtypes = [u32p, u16p, u32p, ctypes.c_int, ctypes.c_int, u16p]
+        lib.oracle_dequant_f16.restype = None
+        lib.oracle_gemm_cols_f16.argtypes = [u16p, u32p, u16p, u32p, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, i32p, ctypes.c_int, u16p, f64p, f64p]
+        lib.oracle_gemm_cols_f16.restype = None
         lib.oracle_format_bits_per_weight.argtypes = [ctypes.c_longlong, ctypes.c_longlong,
                                                       ctypes.c_int]
         lib.oracle_format_bits_per_weight.restype = ctypes.c_double
@@ -208,6 +227,73 @@ def bf16_round(v) -> np.ndarray:
     _load().oracle_bf16_from_double_array(_ptr(a, ctypes.c_double), a.size,
                                           _ptr(out, ctypes.c_uint16))
     return out
+
+
+# ---- fp16-activation variant (w4a16_f16_oracle.c)
+
+def f16_to_double(bits: int) -> float:
+    return _load().oracle_f16_to_double(int(bits) & 0xFFFF)
+
+
+def f16_from_double(v: float) -> int:
+    return int(_load().oracle_f16_from_double(float(v)))
+
+
+def f16_round(v) -> np.ndarray:
+    """RNE_f16 of every element of a float64 array (bit patterns)."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().oracle_f16_from_double_array(_ptr(a, ctypes.c_double), a.size,
+                                         _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def dequant_one_f16(q: int, z: int, scale_bits: int) -> int:
+    return int(_load().oracle_dequant_one_f16(int(q), int(z), int(scale_bits) & 0xFFFF))
+
+
+def dequant_f16(qweight, scales, qzeros=None) -> np.ndarray:
+    """W[K][N] as fp16 bit patterns (uint16), scales fp16 bits [K/128][N]."""
+    q = _as_u32(qweight)
+    s = _as_u16(scales)
+    z = None if qzeros is None else _as_u32(qzeros)
+    K = q.shape[0] * 8
+    N = q.shape[1]
+    assert s.shape == (K // GROUP, N)
+    if z is not None:
+        assert z.shape == (K // GROUP, N // 8)
+    out = np.empty((K, N), dtype=np.uint16)
+    _load().oracle_dequant_f16(_ptr(q, ctypes.c_uint32), _ptr(s, ctypes.c_uint16),
+                               _ptr(z, ctypes.c_uint32), K, N, _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def gemm_f16(x, qweight, scales, qzeros=None, cols=None):
+    """fp16 reference GEMM (x, scales, y fp16 bits) on the listed columns.
+
+    Returns ``(y_bits uint16 [B][ncols], acc float64, bound float64)`` with
+    bound = 2e-3 * sum|x*w| + 2^-24 * (1 + sum|x|)."""
+    xb = _as_u16(x)
+    q = _as_u32(qweight)
+    s = _as_u16(scales)
+    z = None if qzeros is None else _as_u32(qzeros)
+    B, K = xb.shape
+    N = q.shape[1]
+    assert q.shape[0] * 8 == K
+    assert s.shape == (K // GROUP, N)
+    if z is not None:
+        assert z.shape == (K // GROUP, N // 8)
+    c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, dtype=np.int32)
+    nc = int(c.shape[0])
+    y = np.empty((B, nc), dtype=np.uint16)
+    acc = np.empty((B, nc), dtype=np.float64)
+    bound = np.empty((B, nc), dtype=np.float64)
+    _load().oracle_gemm_cols_f16(_ptr(xb, ctypes.c_uint16), _ptr(q, ctypes.c_uint32),
+                                 _ptr(s, ctypes.c_uint16), _ptr(z, ctypes.c_uint32),
+                                 B, K, N, _ptr(c, ctypes.c_int), nc,
+                                 _ptr(y, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
+                                 _ptr(bound, ctypes.c_double))
+    return y, acc, bound
 
 
 EPI_BIAS, EPI_SILU_MUL = 1, 2
