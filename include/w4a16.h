@@ -183,6 +183,35 @@ w4a16_status w4a16_gemm_path(const void *x, const void *packed, const void *scal
 w4a16_status w4a16_dequant_ref(const void *packed, const void *scales, int has_zeros, void *w,
                                int K, int N, int group_size, void *stream);
 
+/* fp16-activation variant ("Give Me BF16 or Give Me Death", "W4A16-INT
+ * Quantization", paragraph "Inference with W4A16": fp16 weights, scales and
+ * tensor-core products).  Same packed blob (w4a16_pack), same layouts,
+ * shapes, workspace size (w4a16_workspace_bytes), path choice, errors and
+ * device status as w4a16_gemm / w4a16_gemm_path, but
+ *   x       device fp16 (IEEE binary16) [B][K]
+ *   scales  device fp16 [K/128][N]
+ *   y       device fp16 [B][N]
+ * The weights are decoded with the fp16 magic number (1024.0, 0x6400: a code
+ * OR-ed into its 10 fraction bits gives 1024 + q exactly) to
+ * w = RNE_f16((q - z) * s), multiplied with fp16 tensor-core operands and
+ * accumulated in fp32; y = RNE_f16 of the sum.  (The small-batch path scales
+ * the fp32 sum of each 128-row group instead of each weight, which changes
+ * the rounding of w, not the bound: |y - y_exact| stays within
+ * 2e-3 * sum|x*w| + 2^-24 * (1 + sum|x|).)  No fused epilogue or grouped
+ * form. */
+w4a16_status w4a16_gemm_f16(const void *x, const void *packed, const void *scales, int has_zeros,
+                            void *y, int B, int K, int N, int group_size, void *workspace,
+                            size_t ws_bytes, void *stream);
+w4a16_status w4a16_gemm_f16_path(const void *x, const void *packed, const void *scales,
+                                 int has_zeros, void *y, int B, int K, int N, int group_size,
+                                 void *workspace, size_t ws_bytes, int path, void *stream);
+
+/* w4a16_dequant_ref for fp16 scales: W[K][N] as fp16, w = RNE_f16((q - z) *
+ * s), through the fp16 GEMM kernels' decode routine.
+ *   scales  device fp16 [K/128][N];  w  device fp16 [K][N] (written) */
+w4a16_status w4a16_dequant_ref_f16(const void *packed, const void *scales, int has_zeros, void *w,
+                                   int K, int N, int group_size, void *stream);
+
 /* Grouped GEMM for mixture-of-experts layers: one launch computes, for every
  * expert e, y[r] = x[r] . dequant(W_e) for the rows r of x that belong to e.
  * Rows are grouped by expert: offsets (device int32 [E+1], non-decreasing,

@@ -11,9 +11,10 @@ from weight_only_int4_gemm_gb300 import inputs
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """Host numpy view of a tensor's bit pattern (uint16 for bf16, uint32 for int32)."""
+    """Host numpy view of a tensor's bit pattern (uint16 for bf16 and fp16,
+    uint32 for int32)."""
     t = t.detach().contiguous().cpu()
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.int32:
         return t.numpy().view(np.uint32)

@@ -48,6 +48,9 @@ SIGNATURES = {
     "w4a16_gemm_grouped": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
     "w4a16_debug_build": (_I, []),
+    "w4a16_gemm_f16": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "w4a16_gemm_f16_path": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
+    "w4a16_dequant_ref_f16": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
     "w4a16_debug_shrink_code_bound": (_I, [_S]),
     # include/w8a8_fp8.h
     "w8a8_fp8_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -233,6 +236,46 @@ def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, has_
                                  1 if has_zeros else 0, out.data_ptr(), B, K, N, GROUP,
                                  ws_ptr, ws_bytes, int(path), _stream(stream))
         _check("w4a16_gemm_path", st)
+    return out
+
+
+def w4a16_gemm_f16(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, has_zeros: bool,
+                   N: int | None = None, *, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, path: int = PATH_AUTO,
+                   stream=None) -> torch.Tensor:
+    """fp16-activation variant: y[B][N] (fp16) = x[B][K] (fp16) . dequant(packed,
+    scales (fp16))."""
+    B, K = x.shape
+    N = scales.shape[1] if N is None else N
+    _need(x, torch.float16, (B, K), "x")
+    _need(scales, torch.float16, (K // GROUP, N), "scales")
+    if packed.numel() * packed.element_size() < w4a16_packed_bytes(K, N, has_zeros):
+        raise ValueError("packed: too small for this shape")
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, (B, N), "out")
+    need = w4a16_workspace_bytes(B, K, N)
+    if workspace is None:
+        workspace = _default_ws.get(need, x.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w4a16_gemm_f16_path", load().w4a16_gemm_f16_path(
+        x.data_ptr(), packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0,
+        out.data_ptr(), B, K, N, GROUP, ws_ptr, ws_bytes, int(path), _stream(stream)))
+    return out
+
+
+def w4a16_dequant_ref_f16(packed: torch.Tensor, scales: torch.Tensor, has_zeros: bool, K: int, *,
+                          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Dequantised W[K][N] (fp16) from fp16 scales, through the fp16 decode."""
+    N = scales.shape[1]
+    _need(scales, torch.float16, (K // GROUP, N), "scales")
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float16, device=scales.device)
+    _need(out, torch.float16, (K, N), "out")
+    _check("w4a16_dequant_ref_f16", load().w4a16_dequant_ref_f16(
+        packed.data_ptr(), scales.data_ptr(), 1 if has_zeros else 0, out.data_ptr(), K, N,
+        GROUP, _stream(stream)))
     return out
 
 

@@ -280,8 +280,36 @@ w4a16_status w4a16_dequant_ref(const void* packed, const void* scales, int has_z
     if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
     if (!packed || !scales || !w) return W4A16_ERR_NULL;
     if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return W4A16_ERR_ALIGN;
-    return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N,
+    return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N, false,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_dequant_ref_f16(const void* packed, const void* scales, int has_zeros, void* w,
+                                   int K, int N, int group_size, void* stream) {
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N)) return W4A16_ERR_SHAPE;
+    if (!packed || !scales || !w) return W4A16_ERR_NULL;
+    if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return W4A16_ERR_ALIGN;
+    return from_cuda(launch_dequant_ref(packed, scales, has_zeros != 0, w, K, N, true,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_gemm_f16(const void* x, const void* packed, const void* scales, int has_zeros,
+                            void* y, int B, int K, int N, int group_size, void* workspace,
+                            size_t ws_bytes, void* stream) {
+    Epilogue epi;
+    epi.f16 = true;
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     W4A16_PATH_AUTO, stream, 0, epi);
+}
+
+w4a16_status w4a16_gemm_f16_path(const void* x, const void* packed, const void* scales,
+                                 int has_zeros, void* y, int B, int K, int N, int group_size,
+                                 void* workspace, size_t ws_bytes, int path, void* stream) {
+    Epilogue epi;
+    epi.f16 = true;
+    return gemm_impl(x, packed, scales, has_zeros, y, B, K, N, group_size, workspace, ws_bytes,
+                     path, stream, 0, epi);
 }
 
 w4a16_status w4a16_gemm_fused(const void* x, const void* packed, const void* scales,

@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "fmt16.cuh"
+
 namespace w4a16 {
 
 constexpr int kPackTileCols = 128;
@@ -74,37 +76,42 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return d;
 }
 
-// bf16(128 + z) in both halves: the value subtracted after the magic OR.
+// (P + z) in both halves (P = 128 for bf16, 1024 for fp16, fmt16.cuh): the
+// value subtracted after the magic OR.
+template <class Fmt = Bf16>
 __device__ __forceinline__ uint32_t zero_pair(uint32_t z) {
-    return 0x43004300u | (z * 0x00010001u);
+    return Fmt::kMagic2 | (z * 0x00010001u);
 }
-constexpr uint32_t kSymmetricZeroPair = 0x43084308u;  // bf16 136.0 = 128 + 8, twice
+constexpr uint32_t kSymmetricZeroPair = Bf16::kSymZero2;  // bf16 136.0 = 128 + 8, twice
 
 // Scale broadcast to both halves.
 __device__ __forceinline__ uint32_t scale_pair(uint16_t s) {
     return (uint32_t)s * 0x00010001u;
 }
 
-// Pair i (0..3) of a packed word: rows (2i, 2i+1) as bf16x2, exact
-// RNE_bf16((q - z) * s) in each half.
+// Pair i (0..3) of a packed word: rows (2i, 2i+1) as two 16-bit values,
+// exact RNE((q - z) * s) in each half (bf16 or fp16).
+template <class Fmt = Bf16>
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int i, uint32_t zero2,
                                                  uint32_t scale2) {
-    const uint32_t magic = lop3_and_or(word >> (4 * i), 0x000F000Fu, 0x43004300u);
-    return bf16x2_mul(bf16x2_sub(magic, zero2), scale2);
+    const uint32_t magic = lop3_and_or(word >> (4 * i), 0x000F000Fu, Fmt::kMagic2);
+    return Fmt::mul2(Fmt::sub2(magic, zero2), scale2);
 }
 
-// Pair i (0..3) of a packed word as the exact integers (q - z), bf16x2: the
-// magic OR and the exact subtraction, without the scale.  Kernels that apply
-// the group scale to an fp32 sum over the group use this.
+// Pair i (0..3) of a packed word as the exact integers (q - z): the magic OR
+// and the exact subtraction, without the scale.  Kernels that apply the group
+// scale to an fp32 sum over the group use this.
+template <class Fmt = Bf16>
 __device__ __forceinline__ uint32_t code_pair(uint32_t word, int i, uint32_t zero2) {
-    return bf16x2_sub(lop3_and_or(word >> (4 * i), 0x000F000Fu, 0x43004300u), zero2);
+    return Fmt::sub2(lop3_and_or(word >> (4 * i), 0x000F000Fu, Fmt::kMagic2), zero2);
 }
 
 // All 8 rows of a packed word, out[i] = rows (2i, 2i+1).
+template <class Fmt = Bf16>
 __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t zero2, uint32_t scale2,
                                              uint32_t out[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = dequant_pair(word, i, zero2, scale2);
+    for (int i = 0; i < 4; ++i) out[i] = dequant_pair<Fmt>(word, i, zero2, scale2);
 }
 
 // Device check of a packed blob's tag (see launch.cuh): one 16-byte load.

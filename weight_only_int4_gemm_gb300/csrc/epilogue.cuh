@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "fmt16.cuh"
 #include "launch.cuh"
 
 namespace w4a16 {
@@ -56,12 +57,14 @@ static __device__ __forceinline__ void epi_store4_fused(uint16_t* y, int N, int 
     }
 }
 
-// Plain conversion of four consecutive columns n .. n+3 (n % 4 == 0) of row b.
+// Plain conversion of four consecutive columns n .. n+3 (n % 4 == 0) of row b
+// to bf16 or fp16 (fmt16.cuh).
+template <class Fmt = Bf16>
 __device__ __forceinline__ void epi_store4_plain(uint16_t* y, int N, int b, int n, float v0,
                                                  float v1, float v2, float v3, const Epilogue&) {
     *reinterpret_cast<uint2*>(y + (size_t)b * N + n) =
-        make_uint2(epi_f32_to_bf16(v0) | (epi_f32_to_bf16(v1) << 16),
-                   epi_f32_to_bf16(v2) | (epi_f32_to_bf16(v3) << 16));
+        make_uint2(Fmt::from_f32(v0) | (Fmt::from_f32(v1) << 16),
+                   Fmt::from_f32(v2) | (Fmt::from_f32(v3) << 16));
 }
 
 // One column per lane: column n of row b, where n runs over consecutive

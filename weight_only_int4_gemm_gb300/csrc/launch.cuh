@@ -61,6 +61,9 @@ constexpr int kEpiSiluMul = 2;  // y[b][j] = silu(acc[b][2j]) * acc[b][2j+1], y 
 struct Epilogue {
     const uint16_t* bias = nullptr;  // bf16 [N] with kEpiBias
     int mode = 0;
+    // fp16 activations, scales and output (fmt16.cuh) instead of bf16; only
+    // the plain epilogue (mode 0) has an fp16 form
+    bool f16 = false;
 };
 
 // Extent of the packed codes the kernels' bounds checks compare against:
@@ -81,7 +84,7 @@ cudaError_t launch_with_pdl(const void* func, dim3 grid, dim3 block, size_t smem
 cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K, int N,
                           void* packed, cudaStream_t stream);
 cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,
-                               int K, int N, cudaStream_t stream);
+                               int K, int N, bool f16, cudaStream_t stream);
 cudaError_t launch_quantize(const void* w, int K, int N, uint32_t* qweight, void* scales,
                             cudaStream_t stream);
 

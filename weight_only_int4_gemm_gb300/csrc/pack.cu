@@ -32,8 +32,8 @@ repack_kernel(const uint32_t* __restrict__ qweight, uint4* __restrict__ packed, 
 }
 
 // One thread per (chunk c, column n): decodes 32 weights with the shared
-// routine and writes them to W[32c .. 32c+31][n].
-template <bool kHasZeros>
+// routine and writes them to W[32c .. 32c+31][n] (bf16 or fp16, fmt16.cuh).
+template <bool kHasZeros, class Fmt>
 __global__ void __launch_bounds__(kPackThreads)
 dequant_ref_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict__ scales,
                    const uint32_t* __restrict__ zeros, uint16_t* __restrict__ w, int K, int N) {
@@ -43,12 +43,12 @@ dequant_ref_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict_
     const int g = c >> 2;  // 4 chunks of 32 rows per group of 128
     const uint4 q = packed[packed_index16(K, N, c, n)];
     const uint32_t s2 = scale_pair(__ldg(scales + (size_t)g * N + n));
-    const uint32_t z2 = kHasZeros ? zero_pair(load_zero(zeros, N, g, n)) : kSymmetricZeroPair;
+    const uint32_t z2 = kHasZeros ? zero_pair<Fmt>(load_zero(zeros, N, g, n)) : Fmt::kSymZero2;
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint32_t pairs[4];
-        dequant_word(words[j], z2, s2, pairs);
+        dequant_word<Fmt>(words[j], z2, s2, pairs);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const size_t k = (size_t)32 * c + 8 * j + 2 * i;
@@ -80,17 +80,24 @@ cudaError_t launch_repack(const uint32_t* qweight, const uint32_t* qzeros, int K
 }
 
 cudaError_t launch_dequant_ref(const void* packed, const void* scales, bool has_zeros, void* w,
-                               int K, int N, cudaStream_t stream) {
+                               int K, int N, bool f16, cudaStream_t stream) {
     dim3 grid((N + kPackThreads - 1) / kPackThreads, K / 32);
     const uint4* p = static_cast<const uint4*>(packed);
     const uint16_t* s = static_cast<const uint16_t*>(scales);
     const uint32_t* z = reinterpret_cast<const uint32_t*>(static_cast<const char*>(packed) +
                                                           packed_code_bytes(K, N));
     uint16_t* out = static_cast<uint16_t*>(w);
-    if (has_zeros)
-        dequant_ref_kernel<true><<<grid, kPackThreads, 0, stream>>>(p, s, z, out, K, N);
-    else
-        dequant_ref_kernel<false><<<grid, kPackThreads, 0, stream>>>(p, s, nullptr, out, K, N);
+    if (f16) {
+        if (has_zeros)
+            dequant_ref_kernel<true, F16><<<grid, kPackThreads, 0, stream>>>(p, s, z, out, K, N);
+        else
+            dequant_ref_kernel<false, F16><<<grid, kPackThreads, 0, stream>>>(p, s, nullptr, out, K,
+                                                                              N);
+    } else if (has_zeros) {
+        dequant_ref_kernel<true, Bf16><<<grid, kPackThreads, 0, stream>>>(p, s, z, out, K, N);
+    } else {
+        dequant_ref_kernel<false, Bf16><<<grid, kPackThreads, 0, stream>>>(p, s, nullptr, out, K, N);
+    }
     return cudaGetLastError();
 }
 

@@ -187,13 +187,22 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// Warp-level m16n8k16 product with fp32 accumulation, bf16 or fp16 operands.
+template <class Fmt>
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    if constexpr (Fmt::kIsF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Work unit u -> (batch chunk, tile, split index) and its extents.  bc counts
@@ -207,10 +216,11 @@ struct Unit {
     const uint32_t* zeros;
 };
 
-// Four fp32 values -> four bf16 (RNE) at a 8-byte aligned address.
-__device__ __forceinline__ void store4_bf16(uint16_t* dst, float v0, float v1, float v2, float v3) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(epi_f32_to_bf16(v0) | (epi_f32_to_bf16(v1) << 16),
-                                                epi_f32_to_bf16(v2) | (epi_f32_to_bf16(v3) << 16));
+// Four fp32 values -> four 16-bit values (RNE) at a 8-byte aligned address.
+template <class Fmt>
+__device__ __forceinline__ void store4(uint16_t* dst, float v0, float v1, float v2, float v3) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(Fmt::from_f32(v0) | (Fmt::from_f32(v1) << 16),
+                                                Fmt::from_f32(v2) | (Fmt::from_f32(v3) << 16));
 }
 
 // A slot's unit as the consumers see it, decoded once by the producer (the
@@ -263,7 +273,7 @@ __device__ __forceinline__ Unit decode_unit(const Args& a, const Tail* t, int u)
 
 // ------------------------------------------------------------ kernel
 
-template <int NT, bool kHasZeros, int kMode>
+template <int NT, bool kHasZeros, int kMode, class Fmt>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_t<NT>())
 skinny_kernel(const Args a) {
     constexpr int kRows = 8 * NT;
@@ -556,12 +566,12 @@ skinny_kernel(const Args a) {
                 if (gl < ngs) {
                     const uint4 qa = codes[(4 * gl + tig) * width + cla];
                     const uint4 qb = codes[(4 * gl + tig) * width + clb];
-                    const float sa = __uint_as_float((uint32_t)sc[gl * kTileCols + cla] << 16);
-                    const float sb = __uint_as_float((uint32_t)sc[gl * kTileCols + clb] << 16);
-                    uint32_t za = kSymmetricZeroPair, zb = kSymmetricZeroPair;
+                    const float sa = Fmt::to_f32(sc[gl * kTileCols + cla]);
+                    const float sb = Fmt::to_f32(sc[gl * kTileCols + clb]);
+                    uint32_t za = Fmt::kSymZero2, zb = Fmt::kSymZero2;
                     if (kHasZeros) {
-                        za = zero_pair((zs[gl * (kTileCols / 8) + (cla >> 3)] >> (4 * (cla & 7))) & 0xFu);
-                        zb = zero_pair((zs[gl * (kTileCols / 8) + (clb >> 3)] >> (4 * (clb & 7))) & 0xFu);
+                        za = zero_pair<Fmt>((zs[gl * (kTileCols / 8) + (cla >> 3)] >> (4 * (cla & 7))) & 0xFu);
+                        zb = zero_pair<Fmt>((zs[gl * (kTileCols / 8) + (clb >> 3)] >> (4 * (clb & 7))) & 0xFu);
                     }
                     const uint32_t wA[4] = {qa.x, qa.y, qa.z, qa.w};
                     const uint32_t wB[4] = {qb.x, qb.y, qb.z, qb.w};
@@ -579,14 +589,14 @@ skinny_kernel(const Args a) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             // step 2j + h: rows 4(2j+h) .. +3 of each lane's chunk
-                            const uint32_t a0 = code_pair(wA[j], 2 * h, za);
-                            const uint32_t a1 = code_pair(wB[j], 2 * h, zb);
-                            const uint32_t a2 = code_pair(wA[j], 2 * h + 1, za);
-                            const uint32_t a3 = code_pair(wB[j], 2 * h + 1, zb);
+                            const uint32_t a0 = code_pair<Fmt>(wA[j], 2 * h, za);
+                            const uint32_t a1 = code_pair<Fmt>(wB[j], 2 * h, zb);
+                            const uint32_t a2 = code_pair<Fmt>(wA[j], 2 * h + 1, za);
+                            const uint32_t a3 = code_pair<Fmt>(wB[j], 2 * h + 1, zb);
 #pragma unroll
                             for (int bt = 0; bt < NT; ++bt)
                                 if (bt * 8 < rows)  // warp-uniform: skip padding tiles
-                                    mma_bf16(t[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
+                                    mma_16816<Fmt>(t[bt], a0, a1, a2, a3, h ? xf[bt].z : xf[bt].x,
                                              h ? xf[bt].w : xf[bt].y);
                         }
                     }
@@ -650,7 +660,7 @@ skinny_kernel(const Args a) {
                     if constexpr (kMode == kFusedEpi)
                         epi_store4_fused(a.y, a.N, w.b0 + b, w.n0 + c4, v0, v1, v2, v3, a.epi);
                     else
-                        store4_bf16(a.y + off, v0, v1, v2, v3);
+                        store4<Fmt>(a.y + off, v0, v1, v2, v3);
                 } else {
                     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                                  ::"l"(a.partial + off), "f"(v0), "f"(v1), "f"(v2), "f"(v3)
@@ -692,7 +702,7 @@ skinny_kernel(const Args a) {
                                     epi_store4_fused(a.y, a.N, w.b0 + b0 + j, w.n0 + c4, v[j].x,
                                                      v[j].y, v[j].z, v[j].w, a.epi);
                                 else
-                                    store4_bf16(a.y + off, v[j].x, v[j].y, v[j].z, v[j].w);
+                                    store4<Fmt>(a.y + off, v[j].x, v[j].y, v[j].z, v[j].w);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
                             }
@@ -711,9 +721,10 @@ cudaError_t launch_t(const SkinnyPlan& p, Args a, cudaStream_t stream) {
     const size_t smem = (size_t)ring_slots<NT>() * slot_bytes<NT>() + 2 * result_bytes<NT>() +
                         sizeof(Tail);
     const void* kern =
-        a.offsets != nullptr ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kGrouped>)
-        : a.epi.mode != 0    ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kFusedEpi>)
-                             : reinterpret_cast<const void*>(skinny_kernel<NT, Z, kPlain>);
+        a.epi.f16            ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kPlain, F16>)
+        : a.offsets != nullptr ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kGrouped, Bf16>)
+        : a.epi.mode != 0    ? reinterpret_cast<const void*>(skinny_kernel<NT, Z, kFusedEpi, Bf16>)
+                             : reinterpret_cast<const void*>(skinny_kernel<NT, Z, kPlain, Bf16>);
     cudaError_t err = set_smem_limit(kern, smem);
     if (err != cudaSuccess) return err;
     void* args[] = {&a};

@@ -214,7 +214,7 @@ __device__ __forceinline__ void issue_x_copies(const Args& a, const CUtensorMap*
     }
 }
 
-template <bool kHasZeros, bool kFused>
+template <bool kHasZeros, bool kFused, class Fmt>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
           const __grid_constant__ CUtensorMap zmap, const Args a) {
@@ -347,7 +347,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
         // and every issuer reads every x slot it waits for in order (the x ring
         // depth times the blocks per stage is a multiple of I).
         if (lane == 0 && issuer < I) {
-            const uint32_t idesc = instr_desc_bf16(kTileN, a.bn);
+            const uint32_t idesc = instr_desc_f16kind(kTileN, a.bn, Fmt::kTcFormat);
             bool ok = true;
             if (a.force_timeout && issuer == 0)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
@@ -464,11 +464,11 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                     const int grow = ((kb0 + j) >> 1) - (kb0 >> 1);  // group row inside the stage
                     const uint32_t s2 = scale_pair(reinterpret_cast<const uint16_t*>(
                         slot + a.scale_off + grow * kScaleRowBytes)[rr]);
-                    uint32_t z2 = kSymmetricZeroPair;
+                    uint32_t z2 = Fmt::kSymZero2;
                     if (kHasZeros) {
                         const uint32_t zw = reinterpret_cast<const uint32_t*>(
                             slot + a.zero_off + grow * kZeroRowBytes)[rr >> 3];
-                        z2 = zero_pair((zw >> (4 * (rr & 7))) & 0xFu);
+                        z2 = zero_pair<Fmt>((zw >> (4 * (rr & 7))) & 0xFu);
                     }
                     // chunk h (rows 32h .. 32h+31 of the block) -> TMEM columns 16h .. 16h+15
                     const uint32_t col = lane_addr + (uint32_t)(sa * kACols);
@@ -479,7 +479,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                         for (int jw = 0; jw < 4; ++jw)
 #pragma unroll
                             for (int pp = 0; pp < 4; ++pp)
-                                v[4 * jw + pp] = dequant_pair(words[jw], pp, z2, s2);
+                                v[4 * jw + pp] = dequant_pair<Fmt>(words[jw], pp, z2, s2);
                         tmem_st_16(col, v);
                     }
                     {
@@ -489,7 +489,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                         for (int jw = 0; jw < 4; ++jw)
 #pragma unroll
                             for (int pp = 0; pp < 4; ++pp)
-                                v[4 * jw + pp] = dequant_pair(words[jw], pp, z2, s2);
+                                v[4 * jw + pp] = dequant_pair<Fmt>(words[jw], pp, z2, s2);
                         tmem_st_16(col + 16, v);
                     }
                     tmem_st_wait();
@@ -551,7 +551,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                             const int b = t.b0 + c0 + jj;
                             if (b < a.B) {
                                 if (a.split == 1)
-                                    a.y[(size_t)b * a.N + nn] = (uint16_t)epi_f32_to_bf16(v[jj]);
+                                    a.y[(size_t)b * a.N + nn] = (uint16_t)Fmt::from_f32(v[jj]);
                                 else
                                     asm volatile("red.global.add.f32 [%0], %1;"
                                                  ::"l"(a.partial + (size_t)b * a.N + nn), "f"(v[jj])
@@ -615,7 +615,7 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                                     epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x, v[jj].y,
                                            v[jj].z, v[jj].w, a.epi);
                                 else
-                                    epi_store4_plain(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x, v[jj].y,
+                                    epi_store4_plain<Fmt>(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x, v[jj].y,
                                            v[jj].z, v[jj].w, a.epi);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
@@ -817,7 +817,8 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
                 return cudaErrorInvalidValue;
         }
     }
-    // scales bf16 [K/128][N]: box of 128 columns x ng group rows
+    // scales [K/128][N] (bf16, or fp16: the copies move 16-bit patterns, so one
+    // map type serves both formats): box of 128 columns x ng group rows
     CUtensorMap smap;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)(K / kGroup)};
@@ -884,10 +885,12 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
     const size_t smem = lay.smem;
     const bool fused = epi.mode != 0;
     const void* kern =
-        has_zeros ? (fused ? reinterpret_cast<const void*>(tc_kernel<true, true>)
-                           : reinterpret_cast<const void*>(tc_kernel<true, false>))
-                  : (fused ? reinterpret_cast<const void*>(tc_kernel<false, true>)
-                           : reinterpret_cast<const void*>(tc_kernel<false, false>));
+        epi.f16 ? (has_zeros ? reinterpret_cast<const void*>(tc_kernel<true, false, F16>)
+                             : reinterpret_cast<const void*>(tc_kernel<false, false, F16>))
+        : has_zeros ? (fused ? reinterpret_cast<const void*>(tc_kernel<true, true, Bf16>)
+                             : reinterpret_cast<const void*>(tc_kernel<true, false, Bf16>))
+                    : (fused ? reinterpret_cast<const void*>(tc_kernel<false, true, Bf16>)
+                             : reinterpret_cast<const void*>(tc_kernel<false, false, Bf16>));
     cudaError_t err =
         set_smem_limit(kern, smem);
     if (err != cudaSuccess) return err;

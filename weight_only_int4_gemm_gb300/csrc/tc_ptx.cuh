@@ -165,11 +165,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// M = m, N = n.
-__device__ __forceinline__ uint32_t instr_desc_bf16(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+// Instruction descriptor, kind::f16: D fp32, A and B of operand type `fmt`
+// (0 fp16, 1 bf16), both K-major, M = m, N = n.
+__device__ __forceinline__ uint32_t instr_desc_f16kind(int m, int n, uint32_t fmt) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t instr_desc_bf16(int m, int n) {
+    return instr_desc_f16kind(m, n, 1u);
 }
 
 // D (TMEM) (+)= A (smem) . B (smem), bf16 operands, K = 16 per instruction.

@@ -212,7 +212,7 @@ __device__ __forceinline__ void issue_code_stage(const Args& a, const Item& t, i
 
 // kSub: 64-row sub-blocks per block (1 or 2).  A block is the unit of the
 // MMA thread's waits and commits and of the dequant groups' turns.
-template <bool kHasZeros, bool kFused, int kSub>
+template <bool kHasZeros, bool kFused, int kSub, class Fmt>
 __global__ void __launch_bounds__(kThreads, 1)
 wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     constexpr int kACols = kSubCols * kSub;         // TMEM columns per weight tile
@@ -341,7 +341,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // last MMA is still to be issued: the tensor pipe's queue holds about
         // one MMA, and the wait would otherwise leave it idle.
         if (lane == 0) {
-            const uint32_t idesc = instr_desc_bf16(kTileN, a.bn);
+            const uint32_t idesc = instr_desc_f16kind(kTileN, a.bn, Fmt::kTcFormat);
             bool ok = true;
             if (a.force_timeout)
                 ok = wait_bounded(smem_u32(&tail->never), 0, abort, a.status,
@@ -448,11 +448,11 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 const uint8_t* slot = code_slot(cs);
                 const uint32_t s2 = scale_pair(
                     reinterpret_cast<const uint16_t*>(slot + kStageCodeBytes)[rr]);
-                uint32_t z2 = kSymmetricZeroPair;
+                uint32_t z2 = Fmt::kSymZero2;
                 if (kHasZeros) {
                     const uint32_t zw = reinterpret_cast<const uint32_t*>(
                         slot + kStageCodeBytes + kScaleRowBytes)[rr >> 3];
-                    z2 = zero_pair((zw >> (4 * (rr & 7))) & 0xFu);
+                    z2 = zero_pair<Fmt>((zw >> (4 * (rr & 7))) & 0xFu);
                 }
                 const uint4* codes = reinterpret_cast<const uint4*>(slot) + (size_t)(2 * jb) * t.nvalid;
                 // chunk h (rows 32h .. 32h+31 of the block) -> TMEM columns 16h .. 16h+15
@@ -466,7 +466,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     for (int jw = 0; jw < 4; ++jw)
 #pragma unroll
                         for (int pp = 0; pp < 4; ++pp)
-                            v[4 * jw + pp] = dequant_pair(words[jw], pp, z2, s2);
+                            v[4 * jw + pp] = dequant_pair<Fmt>(words[jw], pp, z2, s2);
                     tmem_st_16(col + 16 * h, v);
                 }
                 tmem_st_wait();
@@ -542,10 +542,10 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                                     epi_store4_fused(a.y, a.N, b, n + 4, hi.x, hi.y, hi.z, hi.w, a.epi);
                                 } else {
                                     *reinterpret_cast<uint4*>(a.y + (size_t)b * a.N + n) = make_uint4(
-                                        epi_f32_to_bf16(lo.x) | (epi_f32_to_bf16(lo.y) << 16),
-                                        epi_f32_to_bf16(lo.z) | (epi_f32_to_bf16(lo.w) << 16),
-                                        epi_f32_to_bf16(hi.x) | (epi_f32_to_bf16(hi.y) << 16),
-                                        epi_f32_to_bf16(hi.z) | (epi_f32_to_bf16(hi.w) << 16));
+                                        Fmt::from_f32(lo.x) | (Fmt::from_f32(lo.y) << 16),
+                                        Fmt::from_f32(lo.z) | (Fmt::from_f32(lo.w) << 16),
+                                        Fmt::from_f32(hi.x) | (Fmt::from_f32(hi.y) << 16),
+                                        Fmt::from_f32(hi.z) | (Fmt::from_f32(hi.w) << 16));
                                 }
                             }
                         }
@@ -621,7 +621,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                                     epi_store4_fused(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x,
                                                      v[jj].y, v[jj].z, v[jj].w, a.epi);
                                 else
-                                    epi_store4_plain(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x,
+                                    epi_store4_plain<Fmt>(a.y, a.N, t.b0 + rr, t.n0 + cc, v[jj].x,
                                                      v[jj].y, v[jj].z, v[jj].w, a.epi);
                                 __stcg(reinterpret_cast<float4*>(a.partial + off),
                                        make_float4(0.f, 0.f, 0.f, 0.f));
@@ -791,6 +791,7 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)p.bn};  // 128-byte rows (swizzle span)
     const cuuint32_t estr[2] = {1, 1};
+    // (bf16 or fp16 x: the copy moves 16-bit patterns, one map type serves both)
     if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -842,15 +843,24 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     const size_t smem = lay.smem;
     const bool fused = epi.mode != 0;
     const void* kern = nullptr;
-    switch ((p.sub == 2 ? 4 : 0) + (has_zeros ? 2 : 0) + (fused ? 1 : 0)) {
-        case 0: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 1>); break;
-        case 1: kern = reinterpret_cast<const void*>(wide_kernel<false, true, 1>); break;
-        case 2: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 1>); break;
-        case 3: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 1>); break;
-        case 4: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 2>); break;
-        case 5: kern = reinterpret_cast<const void*>(wide_kernel<false, true, 2>); break;
-        case 6: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 2>); break;
-        default: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 2>); break;
+    if (epi.f16) {
+        switch ((p.sub == 2 ? 2 : 0) + (has_zeros ? 1 : 0)) {
+            case 0: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 1, F16>); break;
+            case 1: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 1, F16>); break;
+            case 2: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 2, F16>); break;
+            default: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 2, F16>); break;
+        }
+    } else {
+        switch ((p.sub == 2 ? 4 : 0) + (has_zeros ? 2 : 0) + (fused ? 1 : 0)) {
+            case 0: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 1, Bf16>); break;
+            case 1: kern = reinterpret_cast<const void*>(wide_kernel<false, true, 1, Bf16>); break;
+            case 2: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 1, Bf16>); break;
+            case 3: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 1, Bf16>); break;
+            case 4: kern = reinterpret_cast<const void*>(wide_kernel<false, false, 2, Bf16>); break;
+            case 5: kern = reinterpret_cast<const void*>(wide_kernel<false, true, 2, Bf16>); break;
+            case 6: kern = reinterpret_cast<const void*>(wide_kernel<true, false, 2, Bf16>); break;
+            default: kern = reinterpret_cast<const void*>(wide_kernel<true, true, 2, Bf16>); break;
+        }
     }
     cudaError_t err =
         set_smem_limit(kern, smem);

@@ -20,7 +20,9 @@ Recipe (shapes and value distributions of the workloads):
                 expert e's weights are drawn like one layer's, seed + e;
   * dense    -- bf16 weights W [K][N] for the quantisers and the FP8
                 comparison path: N(0, 1) * 0.02 rounded to bf16;
-  * bias     -- bf16 [N]: N(0, 1) * 0.5 rounded to bf16.
+  * bias     -- bf16 [N]: N(0, 1) * 0.5 rounded to bf16;
+  * fp16     -- the fp16-activation variant draws x and the scales the same
+                way and rounds them to fp16 instead (``dtype=torch.float16``).
 
 Draws use ``torch.Generator(device).manual_seed(seed)``; CPU and CUDA
 generators give different streams, so each comparison uses one generated copy
@@ -58,17 +60,19 @@ def random_words(shape, gen: torch.Generator, device) -> torch.Tensor:
     return torch.randint(-2**31, 2**31, shape, dtype=torch.int32, generator=gen, device=device)
 
 
-def make_weights(K: int, N: int, seed: int, *, zero_points: bool = False, device="cpu"):
+def make_weights(K: int, N: int, seed: int, *, zero_points: bool = False, device="cpu",
+                 dtype=torch.bfloat16):
     """(qweight, scales, qzeros-or-None) for one K x N layer."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     qweight = random_words((K // 8, N), gen, device)
-    scales = (torch.randn((K // GROUP, N), generator=gen, device=device).abs_() * 0.02).to(torch.bfloat16)
+    scales = (torch.randn((K // GROUP, N), generator=gen, device=device).abs_() * 0.02).to(dtype)
     qzeros = random_words((K // GROUP, N // 8), gen, device) if zero_points else None
     return qweight, scales, qzeros
 
 
-def make_activations(B: int, K: int, seed: int, *, outlier_frac: float = 0.0, device="cpu"):
+def make_activations(B: int, K: int, seed: int, *, outlier_frac: float = 0.0, device="cpu",
+                     dtype=torch.bfloat16):
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     x = torch.randn((B, K), generator=gen, device=device)
@@ -76,14 +80,17 @@ def make_activations(B: int, K: int, seed: int, *, outlier_frac: float = 0.0, de
     if n_out > 0:
         channels = torch.randperm(K, generator=gen, device=device)[:n_out]
         x[:, channels] *= 20.0
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
 def make_problem(B: int, K: int, N: int, seed: int, *, zero_points: bool = False,
-                 outlier_frac: float = 0.0, device="cpu") -> LinearProblem:
-    """One seeded layer: weights from ``seed``, activations from ``seed + 1``."""
-    qweight, scales, qzeros = make_weights(K, N, seed, zero_points=zero_points, device=device)
-    x = make_activations(B, K, seed + 1_000_003, outlier_frac=outlier_frac, device=device)
+                 outlier_frac: float = 0.0, device="cpu", dtype=torch.bfloat16) -> LinearProblem:
+    """One seeded layer: weights from ``seed``, activations from ``seed + 1``
+    (x and scales in ``dtype``: bf16, or fp16 for the fp16 variant)."""
+    qweight, scales, qzeros = make_weights(K, N, seed, zero_points=zero_points, device=device,
+                                           dtype=dtype)
+    x = make_activations(B, K, seed + 1_000_003, outlier_frac=outlier_frac, device=device,
+                         dtype=dtype)
     return LinearProblem(x, qweight, scales, qzeros)
 
 
