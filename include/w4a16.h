@@ -59,7 +59,7 @@ extern "C" {
 #endif
 
 #define W4A16_GROUP 128
-#define W4A16_PACKED_LAYOUT 3 /* version tag of the packed blob's layout */
+#define W4A16_PACKED_LAYOUT 4 /* version tag of the packed blob's layout */
 
 typedef enum {
     W4A16_OK = 0,

@@ -9,14 +9,18 @@
 // multiply by the group scale then gives w = RNE_bf16((q - z) * s).  One
 // lop3 builds two such values at once, one in each 16-bit half.
 //
-// Packed layout (version W4A16_PACKED_LAYOUT = 3):
+// Packed layout (version W4A16_PACKED_LAYOUT = 4):
 //   codes: the N columns are cut into tiles of 128 (the last tile holds
 //   w = N - 128*t columns when N is not a multiple of 128).  Tile t starts at
 //   byte 64*K*t; inside it, chunk c (rows 32c .. 32c+31) is w consecutive
 //   16-byte entries, one per column, so every (tile, run of chunks) is one
-//   contiguous block -- a single bulk copy.  The 16 bytes of (chunk c,
-//   column n) hold the 32 codes of rows 32c .. 32c+31 of column n; word j
-//   holds rows 32c + 8j .. 32c + 8j + 7.  Inside a word, the codes of rows
+//   contiguous block -- a single bulk copy.  Column n's entry of chunk c sits
+//   at position n XOR 2*(c mod 4) of the run (w is a multiple of 8, so the
+//   swizzle stays inside the run): a warp whose eight-lane phases read four
+//   chunks of two columns each then touches eight different bank groups of
+//   shared memory instead of two.  The 16 bytes of (chunk c, column n) hold
+//   the 32 codes of rows 32c .. 32c+31 of column n; word j holds rows
+//   32c + 8j .. 32c + 8j + 7.  Inside a word, the codes of rows
 //   (2i, 2i+1) (offsets within the word) sit in nibbles i and i + 4, i.e. in
 //   the low and high 16-bit halves at the same bit offset 4i, so
 //        (word >> 4i) & 0x000F000F  ==  { code(2i), code(2i+1) }.
@@ -45,11 +49,14 @@ __host__ __device__ inline size_t packed_tile_base(int K, int t) {
     return (size_t)64 * (size_t)K * (size_t)t;
 }
 
+// Swizzle of chunk c's run: column n of the tile sits at position n ^ swizzle.
+__host__ __device__ constexpr int packed_swizzle(int c) { return 2 * (c & 3); }
+
 // Index, in 16-byte units, of (chunk c, column n).
 __host__ __device__ inline size_t packed_index16(int K, int N, int c, int n) {
     const int t = n / kPackTileCols;
     return packed_tile_base(K, t) / 16 + (size_t)c * packed_tile_width(N, t) +
-           (size_t)(n - kPackTileCols * t);
+           (size_t)((n - kPackTileCols * t) ^ packed_swizzle(c));
 }
 
 // Nibble position of row offset r (0..7) inside a packed word.

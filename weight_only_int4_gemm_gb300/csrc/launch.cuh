@@ -23,7 +23,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // another shape); w4a16_packed_check reads it on the host.
 constexpr size_t kBlobTagBytes = 16;
 constexpr uint32_t kBlobMagic = 0x70413457u;  // bytes 'W' '4' 'A' 'p'
-constexpr uint32_t kBlobLayout = 3;           // W4A16_PACKED_LAYOUT
+constexpr uint32_t kBlobLayout = 4;           // W4A16_PACKED_LAYOUT
 constexpr unsigned int kStatusBadBlob = 4;    // W4A16_ERR_UNSUPPORTED
 inline size_t packed_tag_offset(int K, int N, bool has_zeros) {
     return packed_code_bytes(K, N) + (has_zeros ? packed_zero_bytes(K, N) : 0);

@@ -564,8 +564,9 @@ skinny_kernel(const Args a) {
 #pragma unroll
             for (int gl = 0; gl < kSlotGroups; ++gl) {
                 if (gl < ngs) {
-                    const uint4 qa = codes[(4 * gl + tig) * width + cla];
-                    const uint4 qb = codes[(4 * gl + tig) * width + clb];
+                    // chunk 4(g0 + gl) + tig: its run is swizzled by 2 * tig
+                    const uint4 qa = codes[(4 * gl + tig) * width + (cla ^ (2 * tig))];
+                    const uint4 qb = codes[(4 * gl + tig) * width + (clb ^ (2 * tig))];
                     const float sa = Fmt::to_f32(sc[gl * kTileCols + cla]);
                     const float sb = Fmt::to_f32(sc[gl * kTileCols + clb]);
                     uint32_t za = Fmt::kSymZero2, zb = Fmt::kSymZero2;

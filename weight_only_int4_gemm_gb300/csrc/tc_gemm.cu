@@ -458,8 +458,10 @@ tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUte
                     const uint8_t* slot = code_slot(q.s);
                     const uint4* codes = reinterpret_cast<const uint4*>(slot) +
                                          (size_t)(2 * j) * t.nvalid;
-                    const uint4 q0 = codes[rr];
-                    const uint4 q1 = codes[t.nvalid + rr];
+                    // chunks 2(kb0 + j) and 2(kb0 + j) + 1 (swizzled runs)
+                    const int swz = packed_swizzle(2 * (t.kb_begin + c * a.nsub + j));
+                    const uint4 q0 = codes[rr ^ swz];
+                    const uint4 q1 = codes[t.nvalid + (rr ^ (swz + 2))];
                     const int kb0 = t.kb_begin + c * a.nsub;
                     const int grow = ((kb0 + j) >> 1) - (kb0 >> 1);  // group row inside the stage
                     const uint32_t s2 = scale_pair(reinterpret_cast<const uint16_t*>(

@@ -459,7 +459,8 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 const uint32_t col = lane_addr + (uint32_t)(sa * kACols);
 #pragma unroll
                 for (int h = 0; h < 2 * kSub; ++h) {
-                    const uint4 qw = codes[h * t.nvalid + rr];
+                    // chunk 4g + 2jb + h of the group (swizzled run)
+                    const uint4 qw = codes[h * t.nvalid + (rr ^ packed_swizzle(2 * jb + h))];
                     const uint32_t words[4] = {qw.x, qw.y, qw.z, qw.w};
                     uint32_t v[16];
 #pragma unroll
