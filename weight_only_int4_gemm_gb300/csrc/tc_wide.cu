@@ -52,10 +52,12 @@
 //                 (q - z) * s) and stores them to its TMEM lane.
 // mbarrier waits test only the parity of a phase, so every waiter waits for a
 // barrier's uses in order: block b uses code slot b mod RC, A slot b mod SA
-// and x slot b mod RX, all three even, and the two dequant groups take
-// alternate blocks, so every slot always serves one group; the MMA thread
-// waits once per block (a block's tile is announced only once its x has
-// landed too) and commits twice (the A slot, the x slot).  Two TMEM
+// and x slot b mod SA (the x ring is as deep as the tile ring), both depths
+// even, and the two dequant groups take alternate blocks, so every slot
+// always serves one group; the MMA thread waits once per block (a block's
+// tile is announced only once its x has landed too) and commits once: the
+// commit frees the block's tile and its x slot together (the x copy thread
+// waits on the tile ring's barriers).  Two TMEM
 // accumulators alternate between items when TMEM has room for them
 // (bn <= 128), so the epilogue of one item overlaps the main loop of the next.
 // Every mbarrier wait is bounded; on expiry the kernel records
@@ -141,7 +143,6 @@ struct SharedTail {
     uint64_t code_full[kMaxCodeSlots];  // codes + scales (+ zero-points) of the stage landed
     uint64_t code_free[kMaxCodeSlots];  // read by every dequant warp
     uint64_t x_full[kMaxXSlots];        // x block landed
-    uint64_t x_free[kMaxXSlots];        // MMAs of its block finished (commit)
     uint64_t a_full[kMaxASlots];        // weight tile in TMEM and its x landed (one arrival
                                         // per warp of the dequant group)
     uint64_t a_free[kMaxASlots];        // MMAs reading the weight tile finished (commit)
@@ -241,7 +242,6 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         }
         for (int s = 0; s < RX; ++s) {
             mbar_init(smem_u32(&tail->x_full[s]), 1);
-            mbar_init(smem_u32(&tail->x_free[s]), 1);
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(smem_u32(&tail->a_full[s]), kDequantWarps);
@@ -315,7 +315,7 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 const Item t = decode_item(a, it);
                 for (int i = 0; i < t.ng * kBlocksPerStage; ++i, ++issued, q.next(RX)) {
                     if (issued >= RX &&
-                        !wait_fast(smem_u32(&tail->x_free[q.s]), q.ph ^ 1u, abort, a.status,
+                        !wait_fast(smem_u32(&tail->a_free[q.s]), q.ph ^ 1u, abort, a.status,
                                    kTimeoutNs)) {
                         ok = false;
                         break;
@@ -389,8 +389,10 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     }
                     mma_bf16_ts(tmem_d, ta + 8 * (4 * kSub - 1),
                                 xd + (uint64_t)((kSub - 1) * xsub16 + 6), idesc, 1u);
+                    // one commit per block releases both its weight tile and its x
+                    // slot (the two rings have the same depth, so slot sa == xs)
                     mma_commit(smem_u32(&tail->a_free[sa]));
-                    mma_commit(smem_u32(&tail->x_free[xs]));
+                    (void)xs;
                     if (!ok) break;
                 }
                 if (!ok) break;
@@ -824,10 +826,14 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.items = p.col_tiles * p.batch_tiles * p.split;
     a.acc_stride = tm.acc_stride;
     a.bufs = tm.bufs;
-    a.a_slots = tm.a_slots;
+    // The x ring and the weight-tile ring have one depth: block b's single
+    // commit then frees A slot b % SA and x slot b % SA together (a commit
+    // costs the MMA thread about as much as an MMA; measured: one commit per
+    // block instead of two, gate_up 4096 -> 28672 at B = 1024 183 -> 169 us).
+    a.a_slots = std::min(tm.a_slots, lay.x_slots);
     a.a_col0 = tm.a_col0;
     a.code_slots = lay.code_slots;
-    a.x_slots = lay.x_slots;
+    a.x_slots = a.a_slots;
     a.x_slot_bytes = lay.x_slot_bytes;
     a.code_base = lay.code_base;
     a.epi_base = lay.epi_base;
