@@ -177,11 +177,6 @@ int gemm_entry(const void* x, const void* packed, const void* scales, int has_ze
                      path, stream);
 }
 
-size_t auto_workspace_bytes(int B, int K, int N, int group_size) {
-    if (group_size != kGroup || !shape_ok(K, N) || B < 1 || B > kMaxB) return (size_t)-1;
-    return path_workspace(choose_path(B, K, N), B, K, N);
-}
-
 #ifdef W4A16_DEBUG
 static std::atomic<size_t> g_code_bound_cut{0};
 #endif

@@ -170,7 +170,5 @@ cudaError_t launch_fp8_gemm(const Fp8Plan& p, const void* xq, const float* sx,
 int gemm_entry(const void* x, const void* packed, const void* scales, int has_zeros, void* y,
                int B, int K, int N, int group_size, void* workspace, size_t ws_bytes, int path,
                void* stream);
-// Workspace the automatic path needs for this shape (SIZE_MAX for invalid shapes).
-size_t auto_workspace_bytes(int B, int K, int N, int group_size);
 
 }  // namespace w4a16

@@ -51,7 +51,9 @@ extern "C" w4a16_status w4a16_gemm_static_scratch(const void* x, const void* pac
                                                   int B, int K, int N, int group_size,
                                                   void* stream) {
     using namespace w4a16;
-    const size_t need = auto_workspace_bytes(B, K, N, group_size);
+    // The same bound a caller gets from w4a16_workspace_bytes (enough for any
+    // path), so the refusal below is exactly the documented one.
+    const size_t need = w4a16_workspace_bytes(B, K, N, group_size);
     if (need == (size_t)-1) {
         // let the common validation report the precise problem
         return static_cast<w4a16_status>(gemm_entry(x, packed, scales, has_zeros, y, B, K, N,

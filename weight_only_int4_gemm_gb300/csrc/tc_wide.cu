@@ -59,7 +59,8 @@
 // commit frees the block's tile and its x slot together (the x copy thread
 // waits on the tile ring's barriers).  Two TMEM
 // accumulators alternate between items when TMEM has room for them
-// (bn <= 128), so the epilogue of one item overlaps the main loop of the next.
+// (2 bn + 4 tiles <= 512 columns), so the epilogue of one item overlaps the
+// main loop of the next.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT in the device status word, drains and returns.
 #include <cuda.h>
@@ -670,11 +671,12 @@ EncodeTiledFn encode_fn() {
 }
 
 // 64-row sub-blocks per block: two (longer blocks, half the MMA thread's
-// per-block waits and commits per MMA) while both accumulators fit in TMEM
-// beside the tile ring (bn <= 128); one at wider tiles, where the single
-// accumulator and the smaller rings that twice-as-long blocks leave made them
-// slower (measured on the decode shapes at B = 384 .. 1024).
-int sub_blocks(int bn) { return bn <= 128 ? 2 : 1; }
+// per-block waits and commits per MMA) up to 160 batch rows; one at wider
+// tiles, where the x slots of twice-as-long blocks leave too shallow a ring.
+// Measured over the decode shapes: at bn = 144, 128-row blocks take gate_up
+// 4096 -> 28672 at B = 270 from 74.7 to 62.7 us; from bn = 176 on they are
+// 10-40 % slower.
+int sub_blocks(int bn) { return bn <= 160 ? 2 : 1; }
 
 // Shared memory: [x ring][code ring][epilogue buffer][tail] (+ 1 KB of
 // alignment slack).  Six code stages (the weights come from HBM), then as
@@ -728,17 +730,17 @@ TmemLayout tmem_layout(int bn, int sub) {
 // so the time is that of the busiest CTA: ceil(items / SMs) items.  Every
 // weight tile is decoded once per batch tile, so smaller batch tiles cost
 // dequantisation, larger ones leave SMs idle; a K split adds the partial
-// sums' reductions.  The cost of an item, in SM cycles, is a fit to the
-// measured times of the decode shapes (qkv 4096 -> 6144, o_proj 4096 -> 4096,
-// gate_up 4096 -> 28672, down 14336 -> 4096, lm_head 4096 -> 128256 at
-// B = 128 .. 1024, every batch tile, K split and block length), which picks
-// plans within 5 % of the fastest measured one on each of them:
-//   per 64 rows of K:  bn <= 128: about 560 cycles (the per-block waits,
-//                      commits and the decode, not the MMAs, set the pace);
-//                      wider:     about 360 + 2.6 bn;
-//   per item:          about 6300 (bn <= 128) or 120 cycles, plus, with a K
-//                      split, about 96 bn - 8900 (at least 1000) for the
-//                      reductions of its bn x 128 partial sums.
+// sums' reductions.  The cost of an item, in SM cycles, is a non-negative
+// least-squares fit (relative errors) to the measured times of the decode
+// shapes (qkv 4096 -> 6144, o_proj 4096 -> 4096, gate_up 4096 -> 28672,
+// down 14336 -> 4096, lm_head 4096 -> 128256 at B = 32 .. 1024, every batch
+// tile count in range and K split; median error 5 %), whose picks cost 0.9 %
+// more than the fastest measured plans over the decode step:
+//   per 64 rows of K:  bn <= 160 (128-row blocks): 433 + 0.7 bn cycles (the
+//                      per-block waits, commit and decode, not the MMAs, set
+//                      the pace);  wider (64-row blocks): 363 + 1.9 bn;
+//   per item with a K split: 73 bn more, the reductions of its bn x 128
+//                      partial sums.
 // The search stays inside the range the fit was made on -- the smallest
 // batch-tile count and the two above it, K splits of 1 to 4 -- where the
 // fit is checked against measurements; outside it the fit extrapolates.
@@ -754,18 +756,21 @@ TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
         if (bn < 32 && bt > min_bt) break;
         const int batch_tiles = (B + bn - 1) / bn;
         const long long tiles = (long long)col_tiles * batch_tiles;
-        const double rows64 =
-            bn <= 128 ? std::max(560.0 - 0.7 * bn, 2.2 * bn) : 356.5 + 2.6 * bn;
-        const double fixed = bn <= 128 ? 6290.0 : 120.0;
+        const double rows64 = sub_blocks(bn) == 2 ? 432.9 + 0.7 * bn : 362.9 + 1.9 * bn;
         for (int split = 1; split <= std::min(4, G); ++split) {
             const int gps = (G + split - 1) / split;
             const int s = (G + gps - 1) / gps;  // no empty splits
             if (s != split) continue;
+            // no K split beside tiles wider than 160 rows: their bn x 128
+            // reductions cost more than the fit expects (down 14336 -> 4096
+            // at B = 384: 59.8 us with bn = 192 and two splits, 55.7 us with
+            // bn = 128 and three)
+            if (s > 1 && bn > 160) break;
             if (s > 1 && tiles > kMaxCounters - 2) break;
             const long long items = tiles * s;
             const long long per_cta = (items + num_sms - 1) / num_sms;
-            const double reduce = s > 1 ? std::max(1000.0, 96.3 * bn - 8871.0) : 0.0;
-            const double cost = (double)per_cta * (2.0 * gps * rows64 + fixed + reduce);
+            const double reduce = s > 1 ? 73.2 * bn : 0.0;
+            const double cost = (double)per_cta * (2.0 * gps * rows64 + reduce);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.bn = bn;
