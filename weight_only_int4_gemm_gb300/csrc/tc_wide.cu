@@ -1,5 +1,5 @@
 // tc_wide.cu -- W4A16 GEMM on the tcgen05 tensor cores for batches of more
-// than 16 rows of x: one MMA-issuing thread, the dequantised weight tile in
+// than 16 rows of x: one or two MMA-issuing threads, the dequantised weight tile in
 // tensor memory.
 //
 // "Give Me BF16 or Give Me Death" (summary), "Inference with W4A16": the
@@ -40,8 +40,10 @@
 // Warp roles:
 //   warp 0      : code copies (one thread);
 //   warp 1      : x copies (one thread);
-//   warp 3      : TMEM allocator + the single MMA-issuing thread
-//                 (tcgen05.mma kind::f16, A from TMEM, 8 x K=16 per block);
+//   warp 3      : TMEM allocator + MMA-issuing thread 0 (tcgen05.mma
+//                 kind::f16, A from TMEM, 4 or 8 x K=16 per block);
+//   warp 2      : MMA-issuing thread 1 at tiles of <= 128 rows (the two
+//                 threads take alternate blocks into their own accumulators);
 //   warps 4..7  : epilogue (tcgen05.ld, one TMEM lane quadrant each), through a
 //                 small transpose buffer in shared memory so that every thread
 //                 stores 16 bytes of bf16 y (or reduces four fp32 partial sums
@@ -90,7 +92,8 @@ constexpr int kTmemCols = 512;               // all of TMEM (one CTA per SM)
 constexpr int kMaxCodeSlots = 16;            // ring of packed-code stages (128 rows each)
 constexpr int kMaxXSlots = 16;               // ring of x blocks
 constexpr size_t kSmemBudget = 227 * 1024;
-constexpr int kCodeWarp = 0, kXWarp = 1, kMmaWarp = 3;  // warp 2 has no role
+constexpr int kCodeWarp = 0, kXWarp = 1, kMmaWarp = 3;  // warp 3: TMEM allocator, issuer 0
+constexpr int kMmaWarp2 = 2;                 // issuer 1 (two issuers at tiles of <= 128 rows)
 constexpr int kEpilogueWarp0 = 4;            // 4..7: TMEM lane quadrant = warp % 4
 constexpr int kDequantWarp0 = 8;             // 8..15
 constexpr int kDequantGroups = 2;            // groups of four warps take alternate blocks
@@ -124,7 +127,8 @@ struct Args {
     int ngroups;        // K / 128
     int col_tiles, batch_tiles, items;
     uint32_t acc_stride;  // TMEM columns per accumulator (bn rounded up to 32)
-    int bufs;           // accumulators alternating between items (1 or 2)
+    int issuers;        // MMA-issuing threads (1 or 2), each with its own accumulator
+    int bufs;           // accumulator sets alternating between items (1 or 2)
     int a_slots;        // dequantised tiles in TMEM (even, 4 .. 8)
     uint32_t a_col0;    // first TMEM column of the tile ring (after the accumulators)
     int code_slots, x_slots;
@@ -249,10 +253,10 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             mbar_init(smem_u32(&tail->a_free[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&tail->tmem_full[b]), 1);
+            mbar_init(smem_u32(&tail->tmem_full[b]), a.issuers);  // one commit per issuer
             mbar_init(smem_u32(&tail->tmem_empty[b]), 4);
         }
-        mbar_init(smem_u32(&tail->mma_done), 1);
+        mbar_init(smem_u32(&tail->mma_done), a.issuers);
         mbar_init(smem_u32(&tail->never), 1);
         tail->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -335,13 +339,20 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     wait_bounded(smem_u32(&tail->x_full[i % RX]), (i / RX) & 1, abort, a.status,
                                  kTimeoutNs);
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer.  A block's weight tile is announced only
-        // once its x block has landed too (the dequant warps check it), so
-        // there is one wait per block, made for block i + 1 while block i's
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ---------------- MMA issuers.  Issuer `me` takes the CTA's blocks b
+        // with b % issuers == me -- with two issuers the same split as the
+        // dequant groups' -- into its own accumulator (the epilogue adds
+        // them): one thread issues a tcgen05.mma only every ~80 cycles at
+        // tiles of <= 128 rows, below the tensor pipe's rate, so there two
+        // threads issue.  A block's weight tile is announced only once its x
+        // block has landed too (the dequant warps check it), so there is one
+        // wait per block, made for the issuer's next block while this block's
         // last MMA is still to be issued: the tensor pipe's queue holds about
         // one MMA, and the wait would otherwise leave it idle.
-        if (lane == 0) {
+        const int me = warp == kMmaWarp ? 0 : 1;
+        const int I = a.issuers;
+        if (lane == 0 && me < I) {
             const uint32_t idesc = instr_desc_f16kind(kTileN, a.bn, Fmt::kTcFormat);
             bool ok = true;
             if (a.force_timeout)
@@ -352,7 +363,12 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             const uint64_t xdesc0 = smem_desc_sw128(smem_u32(x_tile(0)));
             const uint32_t xslot16 = a.x_slot_bytes >> 4;
             const uint32_t a_tmem0 = tmem_base + a.a_col0;
-            Ring qx, qa;
+            const uint32_t xsub16 = (uint32_t)a.bn * 8;  // one x sub-tile (bn x 128 B), 16-byte units
+            // ring position of this issuer's next block: A slot = x slot = b % SA
+            // (the two rings have one depth), stepped by I (SA is a multiple of I)
+            int sl = me;
+            uint32_t ph = 0;
+            int gb0 = 0;  // CTA-wide index of the item's first block
             int j = 0;
             for (int it = blockIdx.x; ok && it < a.items; it += gridDim.x, ++j) {
                 const Item t = decode_item(a, it);
@@ -363,41 +379,49 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     ok = false;
                     break;
                 }
-                const uint32_t tmem_d = tmem_base + (uint32_t)acc * a.acc_stride;
+                const uint32_t tmem_d =
+                    tmem_base + (uint32_t)(acc * I + me) * a.acc_stride;
                 const int nb = t.ng * kBlocksPerStage;
-                const uint32_t xsub16 = (uint32_t)a.bn * 8;  // one x sub-tile (bn x 128 B), 16-byte units
-                if (!wait_test_first(smem_u32(&tail->a_full[qa.s]), qa.ph, abort, a.status,
-                                     kTimeoutNs)) {
-                    ok = false;
-                    break;
+                int i = ((me - gb0) % I + I) % I;  // this issuer's first block of the item
+                if (i < nb) {
+                    if (!wait_test_first(smem_u32(&tail->a_full[sl]), ph, abort, a.status,
+                                         kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                 }
-                tc_fence_after();
-                for (int i = 0; i < nb; ++i) {
-                    const uint32_t ta = a_tmem0 + (uint32_t)(qa.s * kACols);
-                    const uint64_t xd = xdesc0 + (uint64_t)((uint32_t)qx.s * xslot16);
-                    mma_bf16_ts(tmem_d, ta, xd, idesc, i != 0 ? 1u : 0u);
+                for (bool first = true; i < nb; i += I, first = false) {
+                    const uint32_t ta = a_tmem0 + (uint32_t)(sl * kACols);
+                    const uint64_t xd = xdesc0 + (uint64_t)((uint32_t)sl * xslot16);
+                    mma_bf16_ts(tmem_d, ta, xd, idesc, first ? 0u : 1u);
 #pragma unroll
                     for (int kk = 1; kk < 4 * kSub - 1; ++kk)
                         mma_bf16_ts(tmem_d, ta + 8 * kk,
                                     xd + (uint64_t)((kk >> 2) * xsub16 + 2 * (kk & 3)), idesc, 1u);
-                    const int sa = qa.s, xs = qx.s;
-                    qa.next(SA);
-                    qx.next(RX);
-                    if (i + 1 < nb) {
-                        ok = wait_test_first(smem_u32(&tail->a_full[qa.s]), qa.ph, abort, a.status,
+                    const int done_slot = sl;
+                    sl += I;
+                    if (sl >= SA) {
+                        sl -= SA;
+                        ph ^= 1u;
+                    }
+                    if (i + I < nb) {
+                        ok = wait_test_first(smem_u32(&tail->a_full[sl]), ph, abort, a.status,
                                              kTimeoutNs);
                         tc_fence_after();
                     }
                     mma_bf16_ts(tmem_d, ta + 8 * (4 * kSub - 1),
                                 xd + (uint64_t)((kSub - 1) * xsub16 + 6), idesc, 1u);
                     // one commit per block releases both its weight tile and its x
-                    // slot (the two rings have the same depth, so slot sa == xs)
-                    mma_commit(smem_u32(&tail->a_free[sa]));
-                    (void)xs;
+                    // slot (the two rings have the same depth)
+                    mma_commit(smem_u32(&tail->a_free[done_slot]));
                     if (!ok) break;
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&tail->tmem_full[acc]));  // fires once this item's MMAs are done
+                // fires once this issuer's MMAs of the item are done (it may
+                // have none: then at once)
+                mma_commit(smem_u32(&tail->tmem_full[acc]));
+                gb0 += nb;
             }
             if (!ok) {
                 // let the epilogue drain: both accumulators "complete" once
@@ -509,22 +533,35 @@ wide_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // ---------------- epilogue (warps 4..7; TMEM lane quadrant = warp % 4)
         const int quad = warp & 3;
         float* buf = reinterpret_cast<float*>(smem + a.epi_base) + quad * 16 * kEpiRow;
+        const int I = a.issuers;
         int j = 0;
+        int gb0 = 0;  // CTA-wide index of the item's first block
         for (int it = blockIdx.x; it < a.items; it += gridDim.x, ++j) {
             const Item t = decode_item(a, it);
             const int acc = a.bufs == 2 ? (j & 1) : 0;
             const int use = a.bufs == 2 ? (j >> 1) : j;
+            // accumulators holding sums: issuer k's, if it had a block of this item
+            const int nb = t.ng * kBlocksPerStage;
+            const bool has0 = I == 1 || nb >= 2 || (gb0 & 1) == 0;
+            const bool has1 = I == 2 && (nb >= 2 || (gb0 & 1) == 1);
+            gb0 += nb;
             const bool done = wait_bounded(smem_u32(&tail->tmem_full[acc]), use & 1, abort,
                                            a.status, kTimeoutNs);
             tc_fence_after();
             const bool live = __all_sync(0xffffffffu, done && !*abort);
             if (live) {  // tcgen05.ld is warp-collective
                 const int nq = t.n0 + quad * 32;  // this warp's 32 columns
-                const uint32_t taddr =
-                    tmem_base + (uint32_t)acc * a.acc_stride + ((uint32_t)(quad * 32) << 16);
+                const uint32_t taddr = tmem_base + (uint32_t)(acc * I) * a.acc_stride +
+                                       ((uint32_t)(quad * 32) << 16);
                 for (int c0 = 0; c0 < a.bn; c0 += 16) {
                     float v[16];
-                    tmem_ld_16(taddr + c0, v);
+                    tmem_ld_16(taddr + (has0 ? 0u : a.acc_stride) + c0, v);
+                    if (has0 && has1) {
+                        float v1[16];
+                        tmem_ld_16(taddr + a.acc_stride + c0, v1);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += v1[i];
+                    }
                     // transpose through shared memory: row i of the chunk, 32 columns
 #pragma unroll
                     for (int i = 0; i < 16; ++i) buf[i * kEpiRow + lane] = v[i];
@@ -706,18 +743,24 @@ WideLayout wide_layout(int bn, int sub) {
     return l;
 }
 
-// TMEM: [accumulator 0][accumulator 1, when both fit with 4 tile slots][tiles].
+// TMEM: [accumulator set 0][set 1, when both fit with 4 tile slots][tiles]; a
+// set holds one accumulator per MMA-issuing thread (two at tiles of <= 128
+// rows, where one thread cannot issue MMAs as fast as the pipe runs them:
+// ~80 cycles per MMA from one thread, ~40-60 per MMA per SM from two or three
+// -- measured with a separate microbenchmark at N = 64).
 struct TmemLayout {
     uint32_t acc_stride, a_col0;
-    int bufs, a_slots;
+    int issuers, bufs, a_slots;
 };
 
 TmemLayout tmem_layout(int bn, int sub) {
     TmemLayout t;
     const uint32_t acols = (uint32_t)(kSubCols * sub);
     t.acc_stride = (uint32_t)((bn + 31) / 32 * 32);
-    t.bufs = 2 * t.acc_stride + 4 * acols <= (uint32_t)kTmemCols ? 2 : 1;
-    t.a_col0 = (uint32_t)t.bufs * t.acc_stride;
+    t.issuers = bn <= 128 ? 2 : 1;
+    const uint32_t set = (uint32_t)t.issuers * t.acc_stride;  // one accumulator per issuer
+    t.bufs = 2 * set + 4 * acols <= (uint32_t)kTmemCols ? 2 : 1;
+    t.a_col0 = (uint32_t)t.bufs * set;
     t.a_slots = std::min(kMaxASlots, (int)((kTmemCols - t.a_col0) / acols)) & ~1;
     return t;
 }
@@ -830,6 +873,7 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
     a.batch_tiles = p.batch_tiles;
     a.items = p.col_tiles * p.batch_tiles * p.split;
     a.acc_stride = tm.acc_stride;
+    a.issuers = tm.issuers;
     a.bufs = tm.bufs;
     // The x ring and the weight-tile ring have one depth: block b's single
     // commit then frees A slot b % SA and x slot b % SA together (a commit
