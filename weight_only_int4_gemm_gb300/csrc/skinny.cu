@@ -672,20 +672,23 @@ skinny_kernel(const Args a) {
             if (lane == 0) mbar_arrive(smem_u32(&tail->res_empty[buf]));  // buffer free again
             if (a.split > 1) {
                 // the last unit of this tile to arrive converts the fp32 sum to
-                // bf16 and clears the accumulator for the next call
-                __threadfence();
-                __syncwarp();
+                // bf16 and clears the accumulator for the next call.  Every lane
+                // counts itself in with an acq_rel atomic, which orders its own
+                // reductions before it -- no fence for the whole warp (measured:
+                // down 14336 -> 4096 at B = 1 13.35 -> 12.33 us) -- and the lane
+                // that sees 32 * split - 1 arrivals before it is the last.
                 uint32_t* counter = a.counters + (size_t)w.bc * a.tiles + w.tile;
                 if (!in_bounds((size_t)w.bc * a.tiles + w.tile < (size_t)kWorkCounter, a.status))
                     continue;
-                uint32_t prev = 0;
-                if (lane == 0)
-                    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                                 : "=r"(prev)
-                                 : "l"(counter)
-                                 : "memory");
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev == (uint32_t)(a.split - 1)) {
+                uint32_t prev;
+                asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                             : "=r"(prev)
+                             : "l"(counter)
+                             : "memory");
+                if (__any_sync(0xffffffffu, prev == (uint32_t)(32 * a.split - 1))) {
+                    // the last lane's acquire reaches the whole warp through the
+                    // warp barrier; the fence orders the reads below after it
+                    __syncwarp();
                     __threadfence();
                     for (int b0 = 0; b0 < w.rows && mine; b0 += 8) {
                         float4 v[8];

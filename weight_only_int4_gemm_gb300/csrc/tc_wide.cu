@@ -777,12 +777,12 @@ TmemLayout tmem_layout(int bn, int sub) {
 // least-squares fit (relative errors) to the measured times of the decode
 // shapes (qkv 4096 -> 6144, o_proj 4096 -> 4096, gate_up 4096 -> 28672,
 // down 14336 -> 4096, lm_head 4096 -> 128256 at B = 32 .. 1024, every batch
-// tile count in range and K split; median error 5 %), whose picks cost 0.9 %
+// tile count in range and K split; median error 5 %), whose picks cost 0.7 %
 // more than the fastest measured plans over the decode step:
-//   per 64 rows of K:  bn <= 160 (128-row blocks): 433 + 0.7 bn cycles (the
-//                      per-block waits, commit and decode, not the MMAs, set
-//                      the pace);  wider (64-row blocks): 363 + 1.9 bn;
-//   per item with a K split: 73 bn more, the reductions of its bn x 128
+//   per 64 rows of K:  bn <= 160 (128-row blocks): 302 + 1.5 bn cycles (the
+//                      issuing threads' per-block waits and commit, not the
+//                      MMAs, set the pace);  wider (64-row blocks): 332 + 2.0 bn;
+//   per item with a K split: 82 bn more, the reductions of its bn x 128
 //                      partial sums.
 // The search stays inside the range the fit was made on -- the smallest
 // batch-tile count and the two above it, K splits of 1 to 4 -- where the
@@ -799,7 +799,7 @@ TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
         if (bn < 32 && bt > min_bt) break;
         const int batch_tiles = (B + bn - 1) / bn;
         const long long tiles = (long long)col_tiles * batch_tiles;
-        const double rows64 = sub_blocks(bn) == 2 ? 432.9 + 0.7 * bn : 362.9 + 1.9 * bn;
+        const double rows64 = sub_blocks(bn) == 2 ? 302.1 + 1.5 * bn : 332.3 + 2.0 * bn;
         for (int split = 1; split <= std::min(4, G); ++split) {
             const int gps = (G + split - 1) / split;
             const int s = (G + gps - 1) / gps;  // no empty splits
@@ -812,7 +812,7 @@ TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
             if (s > 1 && tiles > kMaxCounters - 2) break;
             const long long items = tiles * s;
             const long long per_cta = (items + num_sms - 1) / num_sms;
-            const double reduce = s > 1 ? 73.2 * bn : 0.0;
+            const double reduce = s > 1 ? 82.4 * bn : 0.0;
             const double cost = (double)per_cta * (2.0 * gps * rows64 + reduce);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
