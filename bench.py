@@ -101,11 +101,12 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"skinny": ["skinny.cu", "dequant.cuh", "epilogue.cuh"],
-                "skinny_kernel": ["skinny.cu", "dequant.cuh", "epilogue.cuh"],
-                "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "dequant.cuh", "epilogue.cuh"],
-                "tc_kernel": ["tc_gemm.cu", "dequant.cuh", "epilogue.cuh"],
-                "wide_kernel": ["tc_wide.cu", "dequant.cuh", "epilogue.cuh"]}
+_COMMON = ["dequant.cuh", "epilogue.cuh", "fmt16.cuh", "checks.cuh", "launch.cuh"]
+KERNEL_FILES = {"skinny": ["skinny.cu"] + _COMMON,
+                "skinny_kernel": ["skinny.cu"] + _COMMON,
+                "tcgen05": ["tc_gemm.cu", "tc_wide.cu", "tc_ptx.cuh"] + _COMMON,
+                "tc_kernel": ["tc_gemm.cu", "tc_ptx.cuh"] + _COMMON,
+                "wide_kernel": ["tc_wide.cu", "tc_ptx.cuh"] + _COMMON}
 
 
 def traffic_from_profiles(kernel: str, workload_name: str):
