@@ -274,9 +274,12 @@ w4a16_status w4a16_quantize_rtn(const void *w, int K, int N, int group_size, uin
 int w4a16_select_path(int B, int K, int N);
 
 /* Name of the kernel w4a16_gemm launches for this shape on the current
- * device: "skinny_kernel" (small-batch split-K), "tc_kernel" (tensor cores,
- * weight tile in tensor memory) or "wide_kernel" (tensor cores, weight tile
- * in shared memory); "invalid" for invalid shapes.  For logs and for
+ * device by automatic selection: "skinny_kernel" (small-batch split-K, 16 or
+ * fewer rows) or "wide_kernel" (tensor cores, above 16 rows).  ("tc_kernel",
+ * tensor cores with several issuing threads, runs only when
+ * w4a16_gemm_path forces the tensor-core path at 16 or fewer rows.)  Both
+ * tensor-core kernels keep the dequantised weight tile in tensor memory.
+ * "invalid" for invalid shapes.  For logs and for
  * reporting which operator ran ("Quantization quality and performance":
  * report the operator actually used).  Never NULL; static storage. */
 const char *w4a16_kernel_name(int B, int K, int N);
