@@ -135,11 +135,11 @@ def test_decoder_layer_linear_set_full(B):
         assert_within_bound(run_gemm(p), p)
 
 
-@pytest.mark.parametrize("B", [1, 4, 16, 64, 128, 256, 270, 384, 512, 1024])
+@pytest.mark.parametrize("B", [1, 4, 8, 12, 16, 64, 128, 256, 270, 384, 512, 1024])
 def test_lm_head_sampled_columns(B):
     """4096 -> 128256 lm_head (largest N) at every batch of the decode-step
-    sweep (all three kernels, ragged batch tiles at 270 and 384): sampled
-    columns, all rows."""
+    sweep and at 8 and 12 rows (both kernels, full and ragged batch tiles):
+    sampled columns, all rows."""
     p = inputs.make_problem(B, 4096, 128256, seed=77)
     y = run_gemm(p)
     assert_within_bound(y, p, cols=sample_columns(128256, 96 if B > 64 else 384))

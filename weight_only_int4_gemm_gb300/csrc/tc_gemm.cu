@@ -788,9 +788,15 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
                                   int N, void* workspace, unsigned int* status,
                                   int force_timeout_ms, const Epilogue& epi,
                                   cudaStream_t stream) {
-    if (p.wide)
+    if (p.wide) {
+        // The wide kernel serves more than 16 batch rows, whose tiles its
+        // planner makes at least 32 rows tall; 16-row tiles are refused: a
+        // timing-only build that ran them (4096 -> 128256 at 8 rows) reported
+        // a device error whose cause was not found.
+        if (p.bn < 32) return cudaErrorInvalidConfiguration;
         return launch_tc_wide(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
                               force_timeout_ms, epi, stream);
+    }
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     const int ng = p.nsub > 1 ? p.nsub / 2 : 1;
