@@ -662,6 +662,8 @@ def run_sweep(args, rank, world, device):
         times = sorted(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps))
         e["ms"] = sum(times) / len(times)
         e["p50_ms"] = times[len(times) // 2]
+        e["p10_ms"] = times[(len(times) - 1) // 10]
+        e["p90_ms"] = times[len(times) - 1 - (len(times) - 1) // 10]
 
     # end to end through the public API with host buffers: per B, one H2D
     # copy of all of the decode step's activations from pinned host memory,
@@ -728,7 +730,8 @@ def sweep_line(args, per_b, step_ms, clocks, e2e_ms, h2d, d2h, e2e_steps, world,
         t = e["ms"] / 1e3
         r = sweep_roofline(e["bytes"], e["flops"], t, hbm, tf_sust)
         rows.append({"B": e["B"], "kernel": e["kernel"], "us_per_step": e["ms"] * 1e3,
-                     "p50_us": e["p50_ms"] * 1e3, "tb_s": e["bytes"] / t / 1e12,
+                     "p50_us": e["p50_ms"] * 1e3, "p10_us": e["p10_ms"] * 1e3,
+                     "p90_us": e["p90_ms"] * 1e3, "tb_s": e["bytes"] / t / 1e12,
                      "tflops": e["flops"] / t / 1e12, "roofline": {
                          k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac")},
                      "memory_us": r["memory_us"], "math_us": r["math_us"],
@@ -1206,6 +1209,15 @@ def run_sweep_main(args, rank, world, local):
                                 "extrapolated": True,
                                 "sample": sampler.describe(len(runs), time.perf_counter() - t0),
                                 "tb_s": sbytes / t_cpu / 1e12}
+        # the same oracle on one core, on a smaller column sample
+        oracle.set_threads(1)
+        sampler.cols = max(1, sampler.cols // 16)
+        t1 = time.perf_counter()
+        t_one = sampler.step()
+        line["cpu_baseline"]["single_core"] = {
+            "value": t_one * 1e6, "unit": "µs/step", "extrapolated": True,
+            "sample": sampler.describe(1, time.perf_counter() - t1)}
+        oracle.set_threads(oracle.omp_threads())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
