@@ -270,7 +270,11 @@ w4a16_status w4a16_quantize_rtn(const void *w, int K, int N, int group_size, uin
  * regimes" (weight-stream-bound at small B, tensor-core-bound past the ridge
  * batch), and the M-dependent kernel selection that page describes (a
  * small-batch kernel below a row threshold, the tiled tensor-core kernel
- * above it). */
+ * above it).  For tests and ablations the environment variable
+ * W4A16_FORCE_PATH=skinny|tcgen05 (read once per process) overrides the
+ * automatic choice of w4a16_gemm, w4a16_gemm_fused, w4a16_gemm_f16 and
+ * w4a16_workspace_bytes alike; a forced tensor-core path is ignored on a
+ * device without it. */
 int w4a16_select_path(int B, int K, int N);
 
 /* Name of the kernel w4a16_gemm launches for this shape on the current

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -121,9 +123,26 @@ TcPlan tc_plan(int B, int K, int N) {
 constexpr int kSkinnyMaxB = 16;
 constexpr int kMaxGroupedExperts = 256;
 
+// Override of the automatic choice for tests and ablations:
+// W4A16_FORCE_PATH=skinny (or 0) / tcgen05 (or 1), read once per process; a
+// forced tensor-core path is ignored on a device without it.
+int forced_path() {
+    static const int v = [] {
+        const char* e = std::getenv("W4A16_FORCE_PATH");
+        if (e == nullptr) return (int)W4A16_PATH_AUTO;
+        if (!std::strcmp(e, "skinny") || !std::strcmp(e, "0")) return (int)W4A16_PATH_SKINNY;
+        if (!std::strcmp(e, "tcgen05") || !std::strcmp(e, "1")) return (int)W4A16_PATH_TCGEN05;
+        return (int)W4A16_PATH_AUTO;
+    }();
+    return v;
+}
+
 int choose_path(int B, int K, int N) {
     (void)K;
     (void)N;
+    const int forced = forced_path();
+    if (forced == W4A16_PATH_SKINNY) return W4A16_PATH_SKINNY;
+    if (forced == W4A16_PATH_TCGEN05 && tc_available()) return W4A16_PATH_TCGEN05;
     if (B <= kSkinnyMaxB || !tc_available()) return W4A16_PATH_SKINNY;
     return W4A16_PATH_TCGEN05;
 }
