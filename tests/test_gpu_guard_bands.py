@@ -119,6 +119,8 @@ GEMM_CASES = [
     (64, 4096, 520, False, w.PATH_AUTO),     # wide kernel, K split
     (100, 1024, 264, True, w.PATH_AUTO),     # wide kernel, zero-points, ragged rows
     (257, 2048, 1032, False, w.PATH_AUTO),   # wide kernel, 128-row blocks + 1 row
+    (40, 256, 8, False, w.PATH_AUTO),        # wide kernel, an 8-column layer
+    (300, 512, 136, False, w.PATH_AUTO),     # wide kernel, tensor stores over a ragged edge
 ]
 
 

@@ -792,7 +792,8 @@ static cudaError_t launch_tc_impl(const TcPlan& p, const void* x, const void* pa
         // The wide kernel serves more than 16 batch rows, whose tiles its
         // planner makes at least 32 rows tall; 16-row tiles are refused: a
         // timing-only build that ran them (4096 -> 128256 at 8 rows) reported
-        // a device error whose cause was not found.
+        // a device error, most likely from a y tensor store whose box was
+        // taller than the whole output.
         if (p.bn < 32) return cudaErrorInvalidConfiguration;
         return launch_tc_wide(p, x, packed, scales, has_zeros, y, B, K, N, workspace, status,
                               force_timeout_ms, epi, stream);

@@ -886,11 +886,14 @@ static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     // y for the tensor-store epilogue: boxes of 16 rows x 32 columns (64-byte
-    // rows, unswizzled), used for the plain 16-bit output without a K split;
-    // if the encoder refuses (an unaligned y), the epilogue stores per thread
+    // rows, unswizzled), used for the plain 16-bit output without a K split
+    // when y is at least one box in each dimension (a box may then overhang
+    // the tensor's edge, whose elements the store skips; a box larger than
+    // the whole tensor is not used); otherwise, or if the encoder refuses (an
+    // unaligned y), the epilogue stores per thread
     CUtensorMap ymap;
     bool y_tma = false;
-    if (epi.mode == 0 && p.split == 1) {
+    if (epi.mode == 0 && p.split == 1 && N >= 32 && B >= 16) {
         const cuuint64_t ydims[2] = {(cuuint64_t)N, (cuuint64_t)B};
         const cuuint64_t ystrides[1] = {(cuuint64_t)N * 2};
         const cuuint32_t ybox[2] = {32, 16};
