@@ -288,6 +288,40 @@ int w4a16_select_path(int B, int K, int N);
  * report the operator actually used).  Never NULL; static storage. */
 const char *w4a16_kernel_name(int B, int K, int N);
 
+/* The launch plan w4a16_gemm uses for a shape, for logs and tests ("Quantization
+ * quality and performance": report the operator actually used; the path and
+ * its split change with the batch: "When quantization pays -- and when it
+ * does not", "The three regimes").  num_sms = 0 plans for the current device
+ * (its SM count and path availability); num_sms > 0 plans, without touching a
+ * device, for a GB300-class device with that many SMs (the tensor-core path
+ * assumed available).  Fields not used by the chosen kernel are 0. */
+typedef struct {
+    int kernel;          /* 0 skinny_kernel, 1 tc_kernel, 2 wide_kernel */
+    int batch_rows;      /* batch rows per tile (small-batch kernel: 8, 16 or 32;
+                            tensor-core kernels: the MMA's N) */
+    int batch_tiles;     /* tiles along B */
+    int col_tiles;       /* 128-column weight tiles */
+    int k_splits;        /* K splits (1: no workspace accumulator) */
+    int groups_per_split;/* 128-row groups of K per split (the last may be shorter) */
+    int grid;            /* CTAs launched */
+    int ctas_per_sm;     /* resident CTAs per SM the kernel is built for */
+    int issuers;         /* MMA-issuing threads (wide kernel) */
+    int acc_buffers;     /* accumulator sets in tensor memory (wide kernel) */
+    int tile_slots;      /* dequantised weight tiles in tensor memory (wide kernel) */
+    int x_slots;         /* activation blocks in shared memory (wide kernel) */
+    int code_slots;      /* packed-code stages in shared memory */
+    int block_rows;      /* K rows per pipeline block */
+    int tmem_cols;       /* tensor-memory columns in use, of 512 (wide kernel) */
+    size_t smem_bytes;   /* dynamic shared memory per CTA (small-batch and wide kernels) */
+    size_t workspace_bytes; /* workspace this plan needs (<= w4a16_workspace_bytes) */
+} w4a16_plan_info;
+
+/* Fills *out.  W4A16_ERR_NULL for out == NULL; W4A16_ERR_SHAPE / _UNSUPPORTED as
+ * w4a16_gemm validates (B, K, N, group_size); W4A16_ERR_CUDA if num_sms = 0 and
+ * the device cannot be queried. */
+w4a16_status w4a16_describe_plan(int B, int K, int N, int group_size, int num_sms,
+                                 w4a16_plan_info *out);
+
 /* Device-side status word of the GEMM kernels: W4A16_OK when every bounded
  * wait completed and every packed blob's tag matched its call, else
  * W4A16_ERR_TIMEOUT (a bounded wait ran out), W4A16_ERR_UNSUPPORTED (a GEMM

@@ -53,3 +53,16 @@ def test_force_tensor_cores_at_a_small_batch():
 def test_unknown_value_keeps_the_automatic_choice():
     assert run_child("bogus", 4) == (0, "skinny_kernel")
     assert run_child("bogus", 300) == (1, "wide_kernel")
+
+
+def test_device_plan_matches_the_dispatch():
+    """w4a16_describe_plan on the current device names the kernel
+    w4a16_kernel_name reports and equals the plan for its SM count."""
+    import torch
+    import weight_only_int4_gemm_gb300 as w
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, K, N in ((1, 4096, 4096), (16, 4096, 28672), (17, 384, 64), (270, 14336, 4096),
+                    (1024, 4096, 128256)):
+        dev = w.w4a16_describe_plan(B, K, N)
+        assert dev["kernel_name"] == w.w4a16_kernel_name(B, K, N)
+        assert dev == w.w4a16_describe_plan(B, K, N, sms)

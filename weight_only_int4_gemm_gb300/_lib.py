@@ -52,6 +52,7 @@ SIGNATURES = {
     "w4a16_gemm_f16_path": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _S, _I, _P]),
     "w4a16_dequant_ref_f16": (_I, [_P, _P, _I, _P, _I, _I, _I, _P]),
     "w4a16_debug_shrink_code_bound": (_I, [_S]),
+    "w4a16_describe_plan": (_I, [_I, _I, _I, _I, _I, _P]),
     # include/w8a8_fp8.h
     "w8a8_fp8_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
     "w8a8_fp8_quantize_weight": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -164,6 +165,29 @@ def w4a16_workspace_bytes(B: int, K: int, N: int) -> int:
 
 def w4a16_select_path(B: int, K: int, N: int) -> int:
     return int(load().w4a16_select_path(B, K, N))
+
+
+class PlanInfo(ctypes.Structure):
+    """w4a16_plan_info (include/w4a16.h)."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "kernel", "batch_rows", "batch_tiles", "col_tiles", "k_splits", "groups_per_split",
+        "grid", "ctas_per_sm", "issuers", "acc_buffers", "tile_slots", "x_slots", "code_slots",
+        "block_rows", "tmem_cols")] + [("smem_bytes", ctypes.c_size_t),
+                                       ("workspace_bytes", ctypes.c_size_t)]
+
+
+KERNEL_NAMES = {0: "skinny_kernel", 1: "tc_kernel", 2: "wide_kernel"}
+
+
+def w4a16_describe_plan(B: int, K: int, N: int, num_sms: int = 0) -> dict:
+    """The launch plan of w4a16_gemm for (B, K, N): for the current device
+    (num_sms = 0) or, without a device, for one with num_sms SMs."""
+    info = PlanInfo()
+    _check("w4a16_describe_plan",
+           load().w4a16_describe_plan(B, K, N, GROUP, num_sms, ctypes.addressof(info)))
+    d = {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+    d["kernel_name"] = KERNEL_NAMES[d["kernel"]]
+    return d
 
 
 def w4a16_kernel_name(B: int, K: int, N: int) -> str:

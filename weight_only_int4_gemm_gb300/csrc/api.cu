@@ -448,6 +448,71 @@ int w4a16_select_path(int B, int K, int N) {
     return choose_path(B, K, N);
 }
 
+w4a16_status w4a16_describe_plan(int B, int K, int N, int group_size, int num_sms_arg,
+                                 w4a16_plan_info* out) {
+    if (out == nullptr) return W4A16_ERR_NULL;
+    *out = w4a16_plan_info{};
+    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (!shape_ok(K, N) || B < 1 || B > kMaxB || num_sms_arg < 0) return W4A16_ERR_SHAPE;
+    int sms = num_sms_arg;
+    int path;
+    if (sms == 0) {  // the current device
+        if (device_info().sms <= 0) return W4A16_ERR_CUDA;
+        sms = num_sms();
+        path = choose_path(B, K, N);
+    } else {  // a GB300-class device with that many SMs
+        const int forced = forced_path();
+        path = forced == W4A16_PATH_SKINNY ? W4A16_PATH_SKINNY
+               : forced == W4A16_PATH_TCGEN05 ? W4A16_PATH_TCGEN05
+               : (B <= kSkinnyMaxB ? W4A16_PATH_SKINNY : W4A16_PATH_TCGEN05);
+    }
+    if (path == W4A16_PATH_SKINNY) {
+        const SkinnyPlan p = num_sms_arg == 0 ? skinny_plan(B, K, N) : plan_skinny(B, K, N, sms);
+        const PlanResources r = skinny_resources(p);
+        out->kernel = 0;
+        out->batch_rows = 8 * p.nt;
+        out->batch_tiles = p.batch_chunks;
+        out->col_tiles = p.col_blocks;
+        out->k_splits = p.split;
+        out->groups_per_split = p.gps;
+        out->grid = p.grid;
+        out->ctas_per_sm = r.ctas_per_sm;
+        out->code_slots = r.code_slots;
+        out->block_rows = r.block_rows;
+        out->smem_bytes = r.smem;
+        out->workspace_bytes = skinny_workspace_bytes(p, B, N);
+        return W4A16_OK;
+    }
+    const TcPlan p = num_sms_arg == 0 ? tc_plan(B, K, N) : plan_tc(B, K, N, sms);
+    out->batch_rows = p.bn;
+    out->batch_tiles = p.batch_tiles;
+    out->col_tiles = p.col_tiles;
+    out->k_splits = p.split;
+    out->groups_per_split = p.kb_per_split / 2;
+    out->grid = p.grid;
+    out->ctas_per_sm = 1;
+    out->workspace_bytes = tc_workspace_bytes(p, B, N);
+    if (!p.wide) {  // the multi-issuer TMEM kernel (forced path at <= 16 rows)
+        out->kernel = 1;
+        out->issuers = p.issuers;
+        out->acc_buffers = p.bufs;
+        out->tile_slots = p.a_slots;
+        out->block_rows = 64;
+        return W4A16_OK;
+    }
+    const PlanResources r = wide_resources(p, B, N);
+    out->kernel = 2;
+    out->issuers = r.issuers;
+    out->acc_buffers = r.acc_bufs;
+    out->tile_slots = r.tile_slots;
+    out->x_slots = r.x_slots;
+    out->code_slots = r.code_slots;
+    out->block_rows = r.block_rows;
+    out->tmem_cols = r.tmem_cols;
+    out->smem_bytes = r.smem;
+    return W4A16_OK;
+}
+
 const char* w4a16_kernel_name(int B, int K, int N) {
     if (!shape_ok(K, N) || B < 1 || B > kMaxB) return "invalid";
     if (choose_path(B, K, N) == W4A16_PATH_SKINNY) return "skinny_kernel";

@@ -100,6 +100,8 @@ struct SkinnyPlan {
 };
 SkinnyPlan plan_skinny(int B, int K, int N, int num_sms);
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N);
+struct PlanResources;
+PlanResources skinny_resources(const SkinnyPlan& p);
 // grouped (mixture-of-experts) variant: T rows of x sorted by expert, device
 // offsets[E+1]; max_rows bounds one expert's rows (picks the batch tile)
 SkinnyPlan plan_skinny_grouped(int T, int E, int max_rows, int K, int N, int num_sms);
@@ -128,6 +130,13 @@ struct TcPlan {
     int sub;         // wide kernel: 64-row sub-blocks per block (1 or 2)
 };
 TcPlan plan_tc(int B, int K, int N, int num_sms);
+// Launch resources of a plan (for w4a16_describe_plan): shared memory per CTA,
+// the rings, the tensor-memory columns in use, the MMA-issuing threads.
+struct PlanResources {
+    size_t smem;
+    int ctas_per_sm, issuers, acc_bufs, tile_slots, x_slots, code_slots, tmem_cols, block_rows;
+};
+PlanResources wide_resources(const TcPlan& p, int B, int N);
 size_t tc_workspace_bytes(const TcPlan& p, int B, int N);
 cudaError_t launch_tc(const TcPlan& p, const void* x, const void* packed, const void* scales,
                       bool has_zeros, void* y, int B, int K, int N, void* workspace,

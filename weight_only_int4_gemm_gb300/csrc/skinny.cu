@@ -810,6 +810,19 @@ SkinnyPlan plan_skinny_grouped(int T, int E, int max_rows, int K, int N, int num
     return p;
 }
 
+PlanResources skinny_resources(const SkinnyPlan& p) {
+    PlanResources r{};
+    const int nt = p.nt;
+    const int slots = nt == 1 ? ring_slots<1>() : (nt == 2 ? ring_slots<2>() : ring_slots<4>());
+    const size_t sb = nt == 1 ? slot_bytes<1>() : (nt == 2 ? slot_bytes<2>() : slot_bytes<4>());
+    const size_t rb = nt == 1 ? result_bytes<1>() : (nt == 2 ? result_bytes<2>() : result_bytes<4>());
+    r.smem = (size_t)slots * sb + 2 * rb + sizeof(Tail);
+    r.ctas_per_sm = ctas_per_sm(nt);
+    r.code_slots = slots;
+    r.block_rows = kSlotGroups * kGroup;  // K rows per ring slot
+    return r;
+}
+
 size_t skinny_workspace_bytes(const SkinnyPlan& p, int B, int N) {
     // counter prefix (also holds the scheduler's words) + one fp32 accumulator
     return p.split > 1 ? kCounterBytes + (size_t)B * N * sizeof(float) : kCounterBytes;

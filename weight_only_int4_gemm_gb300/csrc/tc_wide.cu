@@ -869,6 +869,25 @@ TcPlan plan_tc_wide(int B, int K, int N, int num_sms) {
     return best;
 }
 
+PlanResources wide_resources(const TcPlan& p, int B, int N) {
+    (void)B;
+    (void)N;
+    PlanResources r{};
+    const WideLayout lay = wide_layout(p.bn, p.sub);
+    const TmemLayout tm = tmem_layout(p.bn, p.sub);
+    r.smem = lay.smem;
+    r.ctas_per_sm = 1;
+    r.issuers = tm.issuers;
+    r.acc_bufs = tm.bufs;
+    // as launched: the x ring as deep as the tile ring
+    r.tile_slots = std::min(tm.a_slots, lay.x_slots);
+    r.x_slots = r.tile_slots;
+    r.code_slots = lay.code_slots;
+    r.tmem_cols = (int)tm.a_col0 + r.tile_slots * kSubCols * p.sub;
+    r.block_rows = kSubK * p.sub;
+    return r;
+}
+
 static cudaError_t launch_wide_impl(const TcPlan& p, const void* x, const void* packed, const void* scales,
                            bool has_zeros, void* y, int B, int K, int N, void* workspace,
                            unsigned int* status, int force_timeout_ms, const Epilogue& epi,
