@@ -729,7 +729,15 @@ def sweep_line(args, per_b, step_ms, clocks, e2e_ms, h2d, d2h, e2e_steps, world,
     for e in per_b:
         t = e["ms"] / 1e3
         r = sweep_roofline(e["bytes"], e["flops"], t, hbm, tf_sust)
-        rows.append({"B": e["B"], "kernel": e["kernel"], "us_per_step": e["ms"] * 1e3,
+        # the launch plan of each distinct shape at this batch (what ran)
+        plans = {}
+        for lbl, K, N in (list(LAYER) + [LM_HEAD] if FORCE == -1 else []):
+            pl = w.w4a16_describe_plan(e["B"], K, N)
+            plans[f"{lbl} {K}x{N}"] = (f"{pl['kernel_name']} rows {pl['batch_rows']} x "
+                                       f"{pl['batch_tiles']}, K splits {pl['k_splits']}, "
+                                       f"grid {pl['grid']}")
+        rows.append({"B": e["B"], "kernel": e["kernel"], "plans": plans,
+                     "us_per_step": e["ms"] * 1e3,
                      "p50_us": e["p50_ms"] * 1e3, "p10_us": e["p10_ms"] * 1e3,
                      "p90_us": e["p90_ms"] * 1e3, "tb_s": e["bytes"] / t / 1e12,
                      "tflops": e["flops"] / t / 1e12, "roofline": {
